@@ -1,0 +1,453 @@
+#!/usr/bin/env python
+"""Benchmark of ReplaySSM prefix materialization on GB300.
+
+Workload (default): the large-hybrid shape, 48 layers x 256 heads x 64x128
+bf16 state, bf16 x/B rings of 8 rows, fp32 dt/A, batch 256 with all 256
+requests active and replay_prefix_len ~ U[0, 8].  One step = one call of the
+whole path (one kernel launch over every layer).  Inputs are synthetic and
+seeded, drawn on the device; 51.5 GB of state move per step, far more than L2.
+
+Printed (rank 0, one JSON line): state GB/s of the step (`value`), ms per
+step, microseconds per active request ((T(n) - T(0)) / n, the "additional
+cost" convention) for n in {1, 16, 256}, the empty-list latency, the roofline
+of the kernel against the measured HBM copy bandwidth, an end-to-end figure
+through the public API with pinned host buffers, the oracle timed on a
+bounded sample on the host cores, and the SM clocks seen while timing.
+
+`--impl reference` times the CPU oracle (the only reference this method has)
+on bounded samples of the same workload instead.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mamba_replayssm_state_gb300 import dist  # noqa: E402
+from mamba_replayssm_state_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "state GB/s & µs/active request (48L×256H×64×128); empty-active-list µs"
+KERNEL_NAME = "materialize_kernel"
+KERNEL_SOURCES = ["rsm_kernel.cuh", "rsm_formats.cuh", "rsm_ptx.cuh", "rsm_params.h", "rsm_api.cu"]
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    p.add_argument("--workload", default="hybrid48_bf16", choices=sorted(wl.SHAPES))
+    p.add_argument("--n-active", type=int, default=None, help="active requests per step (default: the workload's)")
+    p.add_argument("--no-extras", action="store_true", help="skip the n sweep, empty latency, e2e and CPU baseline")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work for the oracle baseline sample")
+    p.add_argument("--e2e-requests", type=int, default=16)
+    p.add_argument("--e2e-steps", type=int, default=5)
+    return p.parse_args()
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "mamba_replayssm_state_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def workload_bytes(shape, active, prefix, src, dst):
+    """Algorithmic bytes of one call: state read + write (+ scales) of every
+    non-padded (layer, request), and the ring rows it replays (x per head,
+    B per group, dt per head)."""
+    import numpy as np
+    n = int(np.argmax(active == -1)) if (active == -1).any() else len(active)
+    es = wl.ELEM_SIZE[shape.state_dtype]
+    tile = shape.H * shape.D * shape.N * es + (shape.H * shape.D * 4 if shape.state_dtype in wl.QUANTIZED else 0)
+    per_tok = wl.ring_bytes_per_token(shape)
+    state_b = ring_b = 0
+    for b in active[:n]:
+        b = int(b)
+        for l in range(shape.L):
+            if src[l, b] == shape.pad_slot_id or dst[l, b] == shape.pad_slot_id:
+                continue
+            state_b += 2 * tile
+            ring_b += int(prefix[b]) * per_tok
+    return state_b, ring_b, n
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while timing."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device_uuid=None):
+        self.proc = None
+        self.uuid = device_uuid
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        sm, smax, reasons, power = [], [], set(), []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, v in zip(self.REASONS, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def profile_traffic(workload: str, src_hash: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m_hash = re.search(r"source_hash:\s*([0-9a-f]+)", txt)
+    m_bytes = re.search(r"dram_bytes_per_launch_full:\s*([0-9.eE+]+)", txt)
+    if not m_hash or not m_bytes or m_hash.group(1) != src_hash:
+        return None
+    return float(m_bytes.group(1))
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            return float(json.load(open(path))["hbm_gbs"]), "measured"
+        except (KeyError, ValueError):
+            pass
+    return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline / reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_pair_seconds(hw):
+    import oracle
+    w = hw.copy()
+    t0 = time.perf_counter()
+    oracle.materialize(w)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline_from_device(dw, shape, seconds):
+    """Times the oracle, as it stands, on (layer, request) pairs of the device
+    world (their inputs copied to the host) until ~`seconds` of CPU work."""
+    import numpy as np
+    active = dw.active.cpu().numpy()
+    n = int(np.argmax(active == -1)) if (active == -1).any() else len(active)
+    rng = np.random.default_rng(123)
+    spent, pairs, state_b = 0.0, 0, 0
+    tile = shape.H * shape.D * shape.N * wl.ELEM_SIZE[shape.state_dtype]
+    while spent < seconds and pairs < 400:
+        l = int(rng.integers(shape.L))
+        b = int(active[int(rng.integers(n))])
+        sub = wl.host_subworld(dw, l, b)
+        spent += oracle_pair_seconds(sub)
+        pairs += 1
+        state_b += 2 * tile
+    gbs = state_b / spent / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{pairs} (layer, request) pairs of the timed workload, single-threaded C oracle, "
+                      f"{spent:.1f} s of CPU work",
+            "us_per_request": spent / pairs * shape.L * 1e6}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle timed on bounded samples of the workload."""
+    if rank != 0:
+        return 0
+    import numpy as np
+    shape = wl.SHAPES[args.workload]
+    one = shape.replace(L=1, Bt=1, n_active=1, pool=2, special="", pad_frac=0.0)
+    tile = shape.H * shape.D * shape.N * wl.ELEM_SIZE[shape.state_dtype]
+    rng = np.random.default_rng(0)
+
+    def step(seed):
+        meta = wl.draw_metadata(one, np.random.default_rng(seed))
+        hw = wl.host_world(one, seed=seed, metadata=meta)
+        return oracle_pair_seconds(hw)
+
+    for i in range(args.warmup):
+        step(10_000 + i)
+    times = [step(int(rng.integers(1 << 30))) for _ in range(args.steps)]
+    total = sum(times)
+    gbs = args.steps * 2 * tile / total / 1e9
+    sample = (f"each step: one (layer, request) pair of {shape.name} (all {shape.H} heads, prefix ~ the "
+              f"workload's distribution), single-threaded C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": shape.name, "layers": shape.L, "heads": shape.H, "dim": shape.D,
+                   "dstate": shape.N, "state_dtype": shape.state_dtype, "batch": shape.Bt,
+                   "sample": "one (layer, request) per step"},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "us_per_request": total / args.steps * shape.L * 1e6,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# the GPU arm
+# ----------------------------------------------------------------------------
+
+def time_graph(torch, fn_list, reps=3):
+    """Mean device time (ms) of one launch, from a CUDA graph of the given launches."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for fn in fn_list[:2]:
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for fn in fn_list:
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * len(fn_list))
+
+
+def e2e_measure(torch, rsm, shape, n_req, steps, device):
+    """End to end through the public API: every step copies the inputs of n_req
+    requests (their source state slots, rings and the call's metadata) from
+    pinned host memory, materializes, and copies the destination slots back."""
+    import numpy as np
+    sh = shape.replace(Bt=n_req, n_active=n_req)
+    meta = wl.draw_metadata(sh, np.random.default_rng(77))
+    # contiguous source block (slots 0..n-1) and destination block (n..2n-1) per layer
+    meta["src_slots"] = np.tile(np.arange(n_req, dtype=np.int32), (sh.L, 1))
+    meta["dst_slots"] = np.tile(np.arange(n_req, 2 * n_req, dtype=np.int32), (sh.L, 1))
+    dw = wl.device_world_random(sh, seed=77, device=device, metadata=meta)
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+    h_state = [pin(s[:n_req]) for s in dw.state]
+    h_x = [pin(x[:n_req]) for x in dw.x]
+    h_B = [pin(b[:n_req]) for b in dw.B]
+    h_dt = [pin(d[:n_req]) for d in dw.dt]
+    h_meta = {k: pin(getattr(dw, k)) for k in ("src_slots", "dst_slots", "ring_start", "replay_prefix_len",
+                                               "active")}
+    h_out = [torch.empty(s[n_req:].shape, dtype=s.dtype, pin_memory=True) for s in dw.state]
+    h2d = sum(t.numel() * t.element_size() for t in h_state + h_x + h_B + h_dt + list(h_meta.values()))
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    call = rsm.prepare(**dw.call_kwargs())
+    stream = torch.cuda.current_stream()
+
+    def one_step():
+        for l in range(sh.L):
+            dw.state[l][:n_req].copy_(h_state[l], non_blocking=True)
+            dw.x[l][:n_req].copy_(h_x[l], non_blocking=True)
+            dw.B[l][:n_req].copy_(h_B[l], non_blocking=True)
+            dw.dt[l][:n_req].copy_(h_dt[l], non_blocking=True)
+        for k, t in h_meta.items():
+            getattr(dw, k).copy_(t, non_blocking=True)
+        call(stream)
+        for l in range(sh.L):
+            h_out[l].copy_(dw.state[l][n_req:], non_blocking=True)
+
+    for _ in range(2):
+        one_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one_step()
+    torch.cuda.synchronize()
+    sec = (time.perf_counter() - t0) / steps
+    state_b, _, _ = workload_bytes(sh, meta["active"], meta["replay_prefix_len"], meta["src_slots"],
+                                   meta["dst_slots"])
+    del dw, h_state, h_x, h_B, h_dt, h_out
+    torch.cuda.empty_cache()
+    return {"value": state_b / sec / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": sec * 1e3,
+            "workload": f"{sh.name} with {n_req} active requests, inputs from pinned host memory"}
+
+
+def main():
+    args = parse_args()
+    rank, local_rank, world = dist.env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import numpy as np
+    import torch
+
+    import mamba_replayssm_state_gb300 as rsm
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist.init("nccl")
+    rsm.load_library()
+
+    shape = wl.SHAPES[args.workload]
+    if args.n_active is not None:
+        shape = shape.replace(n_active=args.n_active)
+    # each rank materializes its own batch (weak scaling: independent shards)
+    dw = wl.device_world_random(shape, seed=1000 * rank, device=device)
+    active = dw.active.cpu().numpy()
+    prefix = dw.replay_prefix_len.cpu().numpy()
+    src, dst = dw.src_slots.cpu().numpy(), dw.dst_slots.cpu().numpy()
+    state_b, ring_b, n = workload_bytes(shape, active, prefix, src, dst)
+    call = rsm.prepare(**dw.call_kwargs())
+    cfg = rsm.launch_config(**dw.call_kwargs())
+    stream = torch.cuda.current_stream()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+
+    for _ in range(max(args.warmup, 0)):
+        call(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        call(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clock_info = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = dist.max_over_ranks(ms, device)
+    status = int(dw.status.item())
+
+    out = {
+        "metric": METRIC,
+        "value": world * state_b / (ms_max * 1e-3) / 1e9,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": shape.name, "layers": shape.L, "heads": shape.H, "heads_per_group": shape.hpg,
+                   "dim": shape.D, "dstate": shape.N, "state_dtype": shape.state_dtype,
+                   "input_dtype": shape.input_dtype, "batch": shape.Bt, "n_active": n,
+                   "ring_buffer_len": shape.R, "max_window": shape.W,
+                   "prefix": "U[0,8]" if shape.prefix[0] == "uniform" else f"fixed {shape.prefix[1]}",
+                   "l2": f"inputs larger than L2 ({state_b / 1e9:.1f} GB of state per step), no flush",
+                   "launch": cfg, "parallelism": f"dp{world} (independent request shards)" if world > 1 else "1 GPU"},
+        "gpu_launches": args.steps,
+        "device_status": status,
+    }
+    peak, peak_kind = measured_peak()
+    achieved = (state_b + ring_b) / (ms * 1e-3) / 1e9
+    src_hash = kernel_source_hash()
+    traffic = profile_traffic(shape.name, src_hash) if n == shape.Bt else None
+    out["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                       "frac": achieved / peak, "traffic": traffic,
+                       "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
+                       "algorithmic_bytes_per_launch": state_b + ring_b, "kernel": KERNEL_NAME,
+                       "source_hash": src_hash}
+    out["clocks"] = clock_info
+
+    if not args.no_extras:
+        # latency with an empty active list: a CUDA graph of 1000 launches
+        kw = dw.call_kwargs()
+        empty = torch.full_like(dw.active, -1)
+        kw["active_request_indices"] = empty
+        empty_call = rsm.prepare(**kw)
+        t_empty = time_graph(torch, [empty_call] * 1000)
+        # host cost of one call (argument marshalling done once)
+        t0 = time.perf_counter()
+        for _ in range(1000):
+            empty_call(stream)
+        host_us = (time.perf_counter() - t0) / 1000 * 1e6
+        torch.cuda.synchronize()
+        # T(n) for small n, rotating over requests so no launch re-reads what the previous one read
+        sweep = {}
+        rng = np.random.default_rng(9)
+        for nn in (1, 16):
+            if nn > shape.Bt:
+                continue
+            calls, keep = [], []
+            for r in range(max(64 // nn, 8)):
+                a = np.full(shape.Bt, -1, np.int32)
+                a[:nn] = rng.permutation(shape.Bt)[:nn]
+                t = torch.from_numpy(a).to(device)
+                keep.append(t)
+                kw2 = dw.call_kwargs()
+                kw2["active_request_indices"] = t
+                calls.append(rsm.prepare(**kw2))
+            sweep[nn] = time_graph(torch, calls, reps=2)
+        sweep[n] = ms
+        out["empty_us"] = t_empty * 1e3
+        out["host_call_us"] = host_us
+        out["ms_per_call"] = {str(k): v for k, v in sorted(sweep.items())}
+        out["us_per_request"] = {str(k): (v - t_empty) * 1e3 / k for k, v in sorted(sweep.items()) if k > 0}
+        out["us_per_request_total"] = {str(k): v * 1e3 / k for k, v in sorted(sweep.items()) if k > 0}
+        if rank == 0:
+            try:
+                out["e2e"] = e2e_measure(torch, rsm, shape, min(args.e2e_requests, shape.Bt), args.e2e_steps,
+                                         device)
+            except RuntimeError as ex:  # pinned memory exhausted etc.
+                out["e2e"] = {"value": None, "error": str(ex)[:200]}
+            if world == 1:
+                out["cpu_baseline"] = cpu_baseline_from_device(dw, shape, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    dist.barrier()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,163 @@
+/*
+ * replayssm.h -- C ABI of libreplayssm.so: ReplaySSM prefix materialization on
+ * GB300 (sm_103a).
+ *
+ * One entry point, rsm_materialize(), mirrors flashinfer.mamba.replayssm_materialize
+ * (API page: signature, Parameters, Notes).  The page's torch.compile
+ * dependency anchors (dependency_inputs / dependency_outputs) are torch
+ * plumbing and are not part of a C call.
+ *
+ * What it computes.  For every request b selected by the -1-terminated
+ * active_request_indices and every layer l, read the source state slot
+ * src_slots[l, b], apply replay_prefix_len[b] ring entries starting at ring
+ * row ring_start[b] (modulo ring_buffer_len) through
+ *     state[h, i, j] = state[h, i, j] * exp(dt[p, h] * A[h]) + dt[p, h] * x[p, h, i] * B[p, g(h), j]
+ * and write the result to dst_slots[l, b].  The ring and the source slot are
+ * only read.  Prefix 0 is an exact copy of the state (and of the scales of a
+ * one-byte state).  A (layer, request) whose source or destination slot equals
+ * pad_slot_id is skipped and its destination is not touched.  The work runs in
+ * one launch over all layers; with an empty active list (first entry -1) the
+ * launch does one load and exits.
+ *
+ * Memory layout (per layer; every stride below is in ELEMENTS of the table's
+ * own element type and steps from one slot to the next):
+ *   state  slot = [num_heads, dim, dstate], contiguous, state_dtype
+ *   scale  slot = [num_heads, dim] fp32 (one-byte state only): value = code * scale
+ *   x      slot = [ring_buffer_len, num_heads, dim]   input_dtype
+ *   B      slot = [ring_buffer_len, num_heads/heads_per_group, dstate]   input_dtype
+ *   dt     slot = [ring_buffer_len, num_heads] fp32, the final step size
+ *   A           = [num_heads] matrixA_dtype (fp32), the final negative value
+ * The caches of a (layer, request) are the ones of its SOURCE slot.  Head h
+ * uses B group h / heads_per_group.
+ *
+ * Ownership.  The caller owns every buffer.  All table and metadata pointers
+ * are DEVICE pointers.  The library allocates nothing, reads no device memory
+ * on the host and does not synchronize: the call enqueues one kernel on
+ * `stream` (a cudaStream_t, NULL = the legacy default stream) and returns.
+ *
+ * Errors.  Host-checkable arguments are validated before anything is
+ * launched; on error nothing is enqueued, the return value is negative and
+ * rsm_last_error() (thread-local) describes it.  Device-resident metadata is
+ * not read on the host: out-of-contract values there are undefined behaviour
+ * as on the API page, except that the kernel skips any (layer, request) whose
+ * active index, ring_start, replay_prefix_len or slot is out of range instead
+ * of touching memory for it, and ORs an RSM_STATUS_* bit into *device_status
+ * when that optional word is given.
+ *
+ * Aliasing.  Destination slots must be distinct and must not be a source slot
+ * read by the same call; otherwise the result is undefined.
+ */
+#ifndef REPLAYSSM_H
+#define REPLAYSSM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RSM_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define RSM_API __attribute__((visibility("default")))
+#else
+#define RSM_API
+#endif
+
+/* return codes */
+#define RSM_OK 0
+#define RSM_EINVAL (-1)  /* an argument fails a host-side check */
+#define RSM_ENOTSUP (-2) /* valid, but no compiled kernel for this (dtype, dim, dstate) */
+#define RSM_ECUDA (-3)   /* the CUDA runtime refused the launch */
+
+/* bits the kernel ORs into *device_status (when device_status != NULL) */
+#define RSM_STATUS_BAD_ACTIVE_INDEX 1u /* an active entry outside [0, batch) */
+#define RSM_STATUS_BAD_RING_START 2u   /* ring_start outside [0, ring_buffer_len) */
+#define RSM_STATUS_BAD_PREFIX_LEN 4u   /* replay_prefix_len outside [0, max_window] */
+#define RSM_STATUS_BAD_SLOT 8u         /* a negative slot that is not pad_slot_id */
+#define RSM_STATUS_WAIT_TIMEOUT 16u    /* an internal pipeline wait gave up (never expected) */
+
+typedef enum rsm_dtype {
+  RSM_F32 = 0,
+  RSM_BF16 = 1,
+  RSM_F16 = 2,
+  RSM_I8 = 3,       /* one-byte state: symmetric int8 codes, |code| <= 127 */
+  RSM_FP8_E4M3 = 4  /* one-byte state: OCP FP8 E4M3 "fn" codes, |value| <= 448 */
+} rsm_dtype;
+
+typedef struct rsm_materialize_args {
+  /* per-layer tables, each [num_layers], device int64 */
+  const int64_t *state_ptrs, *state_slot_strides;
+  const int64_t *x_cache_ptrs, *x_cache_slot_strides;
+  const int64_t *B_cache_ptrs, *B_cache_slot_strides;
+  const int64_t *dt_cache_ptrs, *dt_cache_slot_strides;
+  const int64_t *A_ptrs;
+  /* one-byte state only; otherwise may be NULL or hold zero entries */
+  const int64_t *state_scale_ptrs, *state_scale_slot_strides;
+  /* slot tables [num_layers, batch] row-major, device int32 */
+  const int32_t *src_slots, *dst_slots;
+  /* per-request metadata [batch], device int32 */
+  const int32_t *ring_start, *replay_prefix_len;
+  /* [batch] device int32: selected request indices, each once, then -1s */
+  const int32_t *active_request_indices;
+  /* one device int64 seed, required when philox_rounds > 0 */
+  const int64_t *rand_seed;
+  /* optional device uint32 word that receives RSM_STATUS_* bits; may be NULL */
+  uint32_t *device_status;
+
+  int32_t num_layers; /* L, rows of the slot tables */
+  int32_t batch;      /* B, columns of the slot tables, length of the [B] tensors */
+  int32_t state_dtype, input_dtype, matrixA_dtype; /* rsm_dtype values */
+  int32_t dim, dstate;
+  int64_t num_heads;        /* 1 .. INT32_MAX */
+  int32_t heads_per_group;  /* divides num_heads */
+  int32_t max_window;       /* 1 .. 64: largest replay_prefix_len the call may see */
+  int32_t ring_buffer_len;  /* >= 1 */
+  int32_t pad_slot_id;      /* slot sentinel to skip (the API page's default is -1) */
+  int32_t philox_rounds;    /* 0 = round to nearest even; > 0 = Philox stochastic rounding */
+} rsm_materialize_args;
+
+/*
+ * Enqueue the materialization described by *args on `stream`.
+ * Returns RSM_OK when the kernel was enqueued (or there was nothing to
+ * enqueue), RSM_EINVAL / RSM_ENOTSUP / RSM_ECUDA otherwise.
+ *
+ * Supported: state_dtype F32, BF16, F16 with (dim, dstate) in {(16,16),
+ * (64,64), (64,128)}; I8 and FP8_E4M3 with (64,128) only (the API page's rule
+ * for one-byte state); input_dtype BF16 (the API page's requirement) or F32;
+ * matrixA_dtype F32.
+ *
+ * Rounding of the written state: fp32 as is; bf16/fp16 round to nearest even;
+ * one-byte state rewrites each (head, dim-row) with scale = amax/qmax and
+ * codes = round(value * (qmax/amax)) (qmax 127 or 448, saturating), a row whose
+ * qmax/amax is not finite becoming zero codes with scale 0.  With
+ * philox_rounds > 0 every non-fp32 format rounds stochastically instead: the
+ * magnitude goes up with probability equal to its distance from the lower
+ * neighbour over the grid spacing, driven by Philox-4x32 (philox_rounds
+ * rounds, key = (lo32, hi32) of *rand_seed, counter = (e>>2, dst_slot, layer, 0)
+ * with e = (h*dim + i)*dstate + j, word e&3).
+ */
+RSM_API int rsm_materialize(const rsm_materialize_args *args, void *stream);
+
+/* Message of the last failing call on this thread ("" if none). */
+RSM_API const char *rsm_last_error(void);
+
+/* sizeof(rsm_materialize_args), so that bindings can check their layout. */
+RSM_API int rsm_args_size(void);
+
+/* RSM_ABI_VERSION of the built library. */
+RSM_API int rsm_abi_version(void);
+
+/*
+ * The launch rsm_materialize would make for *args on the current device,
+ * without launching: grid CTAs, threads per CTA, dynamic shared memory bytes
+ * and pipeline stages.  Same validation and return codes as rsm_materialize.
+ */
+RSM_API int rsm_launch_config(const rsm_materialize_args *args, int *grid, int *block,
+                      int *smem_bytes, int *stages);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* REPLAYSSM_H */

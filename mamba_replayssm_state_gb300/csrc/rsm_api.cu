@@ -1,0 +1,293 @@
+// rsm_api.cu -- host side of libreplayssm.so: argument validation, choice of
+// the compiled kernel instance, launch sizing and the launch itself.
+//
+// The checks follow the flashinfer.mamba.replayssm_materialize API page
+// (Parameters: heads_per_group divides num_heads, max_window range, one-byte
+// state needs dim=64/dstate=128, BF16 inputs, a seed when philox_rounds > 0)
+// and FlashInfer PR #4815's review fixes (num_heads must fit a 32-bit int;
+// the thread count is a compile-time 32-wide warp multiple).  Nothing here
+// reads device memory, allocates or synchronizes.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <string>
+
+#include "../../include/replayssm.h"
+#include "rsm_instances.h"
+#include "rsm_params.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+struct Instance {
+  int sf, inf, dim, dstate;
+  const void* (*kernel)();
+};
+
+#define RSM_ENTRY(SF, IF, D, N) {SF, IF, D, N, &rsm::kernel_for<SF, IF, D, N>},
+const Instance kInstances[] = {RSM_FOR_EACH_INSTANCE(RSM_ENTRY)};
+#undef RSM_ENTRY
+
+int elem_bytes(int dt) {
+  switch (dt) {
+    case RSM_F32: return 4;
+    case RSM_BF16:
+    case RSM_F16: return 2;
+    case RSM_I8:
+    case RSM_FP8_E4M3: return 1;
+    default: return 0;
+  }
+}
+
+const char* dtype_name(int dt) {
+  switch (dt) {
+    case RSM_F32: return "f32";
+    case RSM_BF16: return "bf16";
+    case RSM_F16: return "f16";
+    case RSM_I8: return "i8";
+    case RSM_FP8_E4M3: return "fp8_e4m3";
+    default: return "?";
+  }
+}
+
+struct DeviceInfo {
+  bool valid = false;
+  int sms = 0, smem_per_sm = 0, smem_optin = 0, smem_reserved = 0;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+constexpr size_t kNumInstances = sizeof(kInstances) / sizeof(kInstances[0]);
+// largest dynamic shared memory size already configured per (device, instance),
+// and the occupancy found for the last size queried (so that calls made while
+// a stream is being captured issue no queries)
+int g_smem_set[kMaxDevices][kNumInstances];
+int g_occ_smem[kMaxDevices][kNumInstances];
+int g_occ_blocks[kMaxDevices][kNumInstances];
+
+int device_info(int dev, DeviceInfo* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (dev < 0 || dev >= kMaxDevices) return fail(RSM_ECUDA, "device ordinal %d out of range", dev);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.valid) {
+    cudaError_t e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (e != cudaSuccess) return fail(RSM_ECUDA, "device query failed: %s", cudaGetErrorString(e));
+    d.valid = true;
+  }
+  *out = d;
+  return RSM_OK;
+}
+
+bool verbose() {
+  static const bool v = [] {
+    const char* s = std::getenv("RSM_VERBOSE");
+    return s != nullptr && s[0] != '\0' && s[0] != '0';
+  }();
+  return v;
+}
+
+// Host-side validation; returns the instance index or a negative code.
+int validate(const rsm_materialize_args* a) {
+  if (a == nullptr) return fail(RSM_EINVAL, "args is NULL");
+  const struct {
+    const void* p;
+    const char* name;
+  } tables[] = {
+      {a->state_ptrs, "state_ptrs"},
+      {a->state_slot_strides, "state_slot_strides"},
+      {a->x_cache_ptrs, "x_cache_ptrs"},
+      {a->x_cache_slot_strides, "x_cache_slot_strides"},
+      {a->B_cache_ptrs, "B_cache_ptrs"},
+      {a->B_cache_slot_strides, "B_cache_slot_strides"},
+      {a->dt_cache_ptrs, "dt_cache_ptrs"},
+      {a->dt_cache_slot_strides, "dt_cache_slot_strides"},
+      {a->A_ptrs, "A_ptrs"},
+      {a->src_slots, "src_slots"},
+      {a->dst_slots, "dst_slots"},
+      {a->ring_start, "ring_start"},
+      {a->replay_prefix_len, "replay_prefix_len"},
+      {a->active_request_indices, "active_request_indices"},
+  };
+  for (const auto& t : tables)
+    if (t.p == nullptr) return fail(RSM_EINVAL, "%s is NULL", t.name);
+  if (a->num_layers <= 0) return fail(RSM_EINVAL, "num_layers must be positive (got %d)", a->num_layers);
+  if (a->batch <= 0) return fail(RSM_EINVAL, "batch must be positive (got %d)", a->batch);
+  if (a->num_heads <= 0 || a->num_heads > 0x7FFFFFFFLL)
+    return fail(RSM_EINVAL, "num_heads must be in [1, 2^31-1] (got %lld)", static_cast<long long>(a->num_heads));
+  if (a->heads_per_group <= 0 || a->num_heads % a->heads_per_group != 0)
+    return fail(RSM_EINVAL, "heads_per_group (%d) must divide num_heads (%lld)", a->heads_per_group,
+                static_cast<long long>(a->num_heads));
+  if (a->max_window < 1 || a->max_window > rsm::kMaxWindow)
+    return fail(RSM_EINVAL, "max_window must be in [1, %d] (got %d)", rsm::kMaxWindow, a->max_window);
+  if (a->ring_buffer_len < 1) return fail(RSM_EINVAL, "ring_buffer_len must be >= 1 (got %d)", a->ring_buffer_len);
+  if (a->dim <= 0 || a->dstate <= 0) return fail(RSM_EINVAL, "dim and dstate must be positive");
+  if (elem_bytes(a->state_dtype) == 0) return fail(RSM_EINVAL, "unknown state_dtype %d", a->state_dtype);
+  if (a->input_dtype != RSM_BF16 && a->input_dtype != RSM_F32)
+    return fail(RSM_EINVAL, "input_dtype must be BF16 or F32 (got %s)", dtype_name(a->input_dtype));
+  if (a->matrixA_dtype != RSM_F32)
+    return fail(RSM_EINVAL, "matrixA_dtype must be F32 (got %s)", dtype_name(a->matrixA_dtype));
+  const bool quant = elem_bytes(a->state_dtype) == 1;
+  if (quant && (a->dim != 64 || a->dstate != 128))
+    return fail(RSM_EINVAL, "one-byte state requires dim=64 and dstate=128 (got %d, %d)", a->dim, a->dstate);
+  if (quant && (a->state_scale_ptrs == nullptr || a->state_scale_slot_strides == nullptr))
+    return fail(RSM_EINVAL, "one-byte state needs state_scale_ptrs and state_scale_slot_strides");
+  if (a->philox_rounds < 0) return fail(RSM_EINVAL, "philox_rounds must be >= 0 (got %d)", a->philox_rounds);
+  if (a->philox_rounds > 0 && a->rand_seed == nullptr)
+    return fail(RSM_EINVAL, "rand_seed is required when philox_rounds > 0");
+  for (size_t i = 0; i < sizeof(kInstances) / sizeof(kInstances[0]); ++i) {
+    const Instance& in = kInstances[i];
+    if (in.sf == a->state_dtype && in.inf == a->input_dtype && in.dim == a->dim && in.dstate == a->dstate)
+      return static_cast<int>(i);
+  }
+  return fail(RSM_ENOTSUP, "no kernel compiled for state %s, input %s, dim %d, dstate %d",
+              dtype_name(a->state_dtype), dtype_name(a->input_dtype), a->dim, a->dstate);
+}
+
+struct Launch {
+  const void* fn;
+  int grid, smem, stages;
+  rsm::Params params;
+};
+
+int plan_launch(const rsm_materialize_args* a, Launch* L) {
+  const int inst = validate(a);
+  if (inst < 0) return inst;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(RSM_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  DeviceInfo di;
+  int rc = device_info(dev, &di);
+  if (rc != RSM_OK) return rc;
+
+  const bool quant = elem_bytes(a->state_dtype) == 1;
+  const rsm::Plan plan = rsm::make_plan(a->dim, a->dstate, elem_bytes(a->state_dtype), quant,
+                                        elem_bytes(a->input_dtype), a->max_window);
+  // Prefer two CTAs per SM (two loaders in flight) when each still gets >= 3
+  // stages; otherwise one CTA per SM with a deeper ring.
+  const int two_cta = di.smem_per_sm / 2 - di.smem_reserved - static_cast<int>(rsm::kStageBase);
+  const int one_cta = di.smem_optin - static_cast<int>(rsm::kStageBase);
+  int stages = two_cta > 0 ? two_cta / static_cast<int>(plan.stage_bytes) : 0;
+  if (stages < 3) stages = one_cta / static_cast<int>(plan.stage_bytes);
+  if (stages > 8) stages = 8;
+  if (stages < 2)
+    return fail(RSM_ENOTSUP, "a pipeline stage of %u bytes does not fit twice in shared memory", plan.stage_bytes);
+  const int smem = static_cast<int>(rsm::kStageBase + stages * plan.stage_bytes);
+
+  const void* fn = kInstances[inst].kernel();
+  int per_sm = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_smem_set[dev][inst] < smem) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return fail(RSM_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+      g_smem_set[dev][inst] = smem;
+    }
+    if (g_occ_smem[dev][inst] == smem) {
+      per_sm = g_occ_blocks[dev][inst];
+    } else {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, rsm::kThreads, smem);
+      if (e != cudaSuccess) return fail(RSM_ECUDA, "occupancy query: %s", cudaGetErrorString(e));
+      g_occ_smem[dev][inst] = smem;
+      g_occ_blocks[dev][inst] = per_sm;
+    }
+  }
+  if (per_sm < 1) return fail(RSM_ENOTSUP, "kernel does not fit on an SM with %d bytes of shared memory", smem);
+
+  rsm::Params& p = L->params;
+  p.state_ptrs = a->state_ptrs;
+  p.state_strides = a->state_slot_strides;
+  p.x_ptrs = a->x_cache_ptrs;
+  p.x_strides = a->x_cache_slot_strides;
+  p.B_ptrs = a->B_cache_ptrs;
+  p.B_strides = a->B_cache_slot_strides;
+  p.dt_ptrs = a->dt_cache_ptrs;
+  p.dt_strides = a->dt_cache_slot_strides;
+  p.A_ptrs = a->A_ptrs;
+  p.scale_ptrs = quant ? a->state_scale_ptrs : nullptr;
+  p.scale_strides = quant ? a->state_scale_slot_strides : nullptr;
+  p.src_slots = a->src_slots;
+  p.dst_slots = a->dst_slots;
+  p.ring_start = a->ring_start;
+  p.prefix_len = a->replay_prefix_len;
+  p.active = a->active_request_indices;
+  p.rand_seed = a->philox_rounds > 0 ? a->rand_seed : nullptr;
+  p.status = a->device_status;
+  p.L = a->num_layers;
+  p.Bt = a->batch;
+  p.H = static_cast<int32_t>(a->num_heads);
+  p.hpg = a->heads_per_group;
+  p.W = a->max_window;
+  p.R = a->ring_buffer_len;
+  p.pad = a->pad_slot_id;
+  p.philox_rounds = a->philox_rounds;
+  p.stages = static_cast<uint32_t>(stages);
+  p.stage_bytes = plan.stage_bytes;
+  p.off_state = plan.off_state;
+  p.off_scale = plan.off_scale;
+  p.off_x = plan.off_x;
+  p.off_B = plan.off_B;
+  p.off_dt = plan.off_dt;
+
+  L->fn = fn;
+  L->grid = di.sms * per_sm;
+  L->smem = smem;
+  L->stages = stages;
+  return RSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int rsm_materialize(const rsm_materialize_args* args, void* stream) {
+  Launch L;
+  const int rc = plan_launch(args, &L);
+  if (rc != RSM_OK) return rc;
+  if (verbose())
+    std::fprintf(stderr, "[replayssm] state=%s input=%s dim=%d dstate=%d grid=%d block=%d smem=%d stages=%d\n",
+                 dtype_name(args->state_dtype), dtype_name(args->input_dtype), args->dim, args->dstate, L.grid,
+                 rsm::kThreads, L.smem, L.stages);
+  void* kargs[] = {&L.params};
+  cudaError_t e = cudaLaunchKernel(L.fn, dim3(L.grid), dim3(rsm::kThreads), kargs, static_cast<size_t>(L.smem),
+                                   static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(RSM_ECUDA, "launch failed: %s", cudaGetErrorString(e));
+  g_last_error.clear();
+  return RSM_OK;
+}
+
+int rsm_launch_config(const rsm_materialize_args* args, int* grid, int* block, int* smem_bytes, int* stages) {
+  Launch L;
+  const int rc = plan_launch(args, &L);
+  if (rc != RSM_OK) return rc;
+  if (grid) *grid = L.grid;
+  if (block) *block = rsm::kThreads;
+  if (smem_bytes) *smem_bytes = L.smem;
+  if (stages) *stages = L.stages;
+  return RSM_OK;
+}
+
+const char* rsm_last_error(void) { return g_last_error.c_str(); }
+
+int rsm_args_size(void) { return static_cast<int>(sizeof(rsm_materialize_args)); }
+
+int rsm_abi_version(void) { return RSM_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,229 @@
+// rsm_formats.cuh -- device-side state/input element formats: 16-byte vector
+// unpack to fp32, fp32 pack with round-to-nearest-even or stochastic rounding,
+// and the Philox-4x32 generator that drives stochastic rounding.
+//
+// Conversions use the hardware cvt instructions (exact for decoding; RNE with
+// IEEE overflow for bf16/fp16, RNE-satfinite for fp8 e4m3).  Stochastic
+// rounding is integer arithmetic on the fp32 bit pattern and takes exactly
+// the decision "round the magnitude up iff word < frac * 2^32", frac being the
+// distance to the lower grid neighbour over the grid spacing.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "../../include/replayssm.h"
+
+namespace rsm {
+
+template <int F> struct Fmt;
+template <> struct Fmt<RSM_F32> { static constexpr int bytes = 4; static constexpr bool quant = false; };
+template <> struct Fmt<RSM_BF16> { static constexpr int bytes = 2; static constexpr bool quant = false; };
+template <> struct Fmt<RSM_F16> { static constexpr int bytes = 2; static constexpr bool quant = false; };
+template <> struct Fmt<RSM_I8> { static constexpr int bytes = 1; static constexpr bool quant = true; };
+template <> struct Fmt<RSM_FP8_E4M3> { static constexpr int bytes = 1; static constexpr bool quant = true; };
+
+// ---------------------------------------------------------------------------
+// scalar helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float2 f16x2_to_f32(uint32_t w) {
+  __half2 h = *reinterpret_cast<__half2*>(&w);
+  return __half22float2(h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// two e4m3 codes (in the low 16 bits) -> two fp32 values, exactly
+__device__ __forceinline__ float2 e4m3x2_to_f32(uint32_t codes16) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(h2) : "r"(codes16));
+  return f16x2_to_f32(h2);
+}
+
+// two fp32 -> two e4m3 codes (low 16 bits), round to nearest even, saturating
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 c;\n\tcvt.rn.satfinite.e4m3x2.f32 c, %1, %2;\n\tcvt.u32.u16 %0, c;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Philox-4x32 (Salmon, Moraes, Dror, Shaw, SC'11, section 5.2)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint4 philox4x32(uint4 c, uint32_t k0, uint32_t k1, int rounds) {
+  constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
+  constexpr uint32_t kWeylA = 0x9E3779B9u, kWeylB = 0xBB67AE85u;
+  for (int r = 0; r < rounds; ++r) {
+    if (r > 0) {
+      k0 += kWeylA;
+      k1 += kWeylB;
+    }
+    const uint32_t hiA = __umulhi(kMulA, c.x), loA = kMulA * c.x;
+    const uint32_t hiB = __umulhi(kMulB, c.z), loB = kMulB * c.z;
+    c = make_uint4(hiB ^ c.y ^ k0, loB, hiA ^ c.w ^ k1, loA);
+  }
+  return c;
+}
+
+// ---------------------------------------------------------------------------
+// stochastic rounding of an fp32 value to a target grid
+// ---------------------------------------------------------------------------
+// The grid: spacing 2^(max(floor(log2|y|), emin) - mant) (integer grid: 1).
+// Returns the rounded value as fp32 (exactly on the grid), saturated to maxfin.
+template <int MANT, int EMIN, bool INTEGER>
+__device__ __forceinline__ float sr_round(float y, uint32_t word, float maxfin) {
+  const uint32_t bits = __float_as_uint(y);
+  const uint32_t sign = bits & 0x80000000u;
+  const uint32_t ab = bits ^ sign;
+  if (ab == 0u) return y;
+  if (ab >= 0x7F800000u) return ab == 0x7F800000u ? __uint_as_float(__float_as_uint(maxfin) | sign) : y;
+  const int eb = static_cast<int>(ab >> 23);
+  const int E = eb ? eb - 127 : -126;                              // a = M * 2^(E-23)
+  const uint32_t M = (ab & 0x7FFFFFu) | (eb ? 0x800000u : 0u);
+  const int ulp_exp = INTEGER ? 0 : (E > EMIN ? E : EMIN) - MANT;  // grid spacing 2^ulp_exp
+  const int d = ulp_exp - (E - 23);                                // bits of M below the spacing
+  float r;
+  if (d <= 0) {
+    r = __uint_as_float(ab);  // already on the grid
+  } else if (d < 24) {
+    const uint32_t low = ab & ((1u << d) - 1u);
+    const uint32_t lo_bits = ab - low;
+    const bool up = (word >> (32 - d)) < low;
+    r = __uint_as_float(up ? lo_bits + (1u << d) : lo_bits);
+  } else {  // |y| below one spacing: neighbours are 0 and the spacing itself
+    bool up;
+    if (d <= 32)
+      up = (word >> (32 - d)) < M;
+    else if (d < 56)
+      up = (static_cast<uint64_t>(word) << (d - 32)) < M;
+    else
+      up = (word == 0u);
+    const float spacing = ulp_exp >= -126 ? __uint_as_float(static_cast<uint32_t>(ulp_exp + 127) << 23)
+                                          : __uint_as_float(1u << (ulp_exp + 149));
+    r = up ? spacing : 0.0f;
+  }
+  r = fminf(r, maxfin);
+  return __uint_as_float(__float_as_uint(r) | sign);
+}
+
+__device__ __forceinline__ float sr_bf16(float y, uint32_t w) {
+  return sr_round<7, -126, false>(y, w, __uint_as_float(0x7F7F0000u));
+}
+__device__ __forceinline__ float sr_f16(float y, uint32_t w) { return sr_round<10, -14, false>(y, w, 65504.0f); }
+__device__ __forceinline__ float sr_e4m3(float y, uint32_t w) { return sr_round<3, -6, false>(y, w, 448.0f); }
+__device__ __forceinline__ float sr_i8(float y, uint32_t w) { return sr_round<0, 0, true>(y, w, 127.0f); }
+
+// ---------------------------------------------------------------------------
+// 16-byte vectors of state elements: VEC = 16 / bytes elements
+// ---------------------------------------------------------------------------
+
+template <int F>
+struct Vec {
+  static constexpr int N = 16 / Fmt<F>::bytes;
+};
+
+// raw 16 bytes -> fp32 values (one-byte formats: codes only; the caller scales)
+template <int F>
+__device__ __forceinline__ void unpack16(const uint4 raw, float* v) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  if constexpr (F == RSM_F32) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = __uint_as_float(w[q]);
+  } else if constexpr (F == RSM_BF16) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v[2 * q] = bf16lo(w[q]);
+      v[2 * q + 1] = bf16hi(w[q]);
+    }
+  } else if constexpr (F == RSM_F16) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = f16x2_to_f32(w[q]);
+      v[2 * q] = f.x;
+      v[2 * q + 1] = f.y;
+    }
+  } else if constexpr (F == RSM_I8) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) v[4 * q + b] = static_cast<float>(static_cast<int8_t>((w[q] >> (8 * b)) & 0xFF));
+    }
+  } else {  // FP8 e4m3
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 a = e4m3x2_to_f32(w[q] & 0xFFFFu);
+      const float2 b = e4m3x2_to_f32(w[q] >> 16);
+      v[4 * q + 0] = a.x;
+      v[4 * q + 1] = a.y;
+      v[4 * q + 2] = b.x;
+      v[4 * q + 3] = b.y;
+    }
+  }
+}
+
+// fp32 values (already scaled into code units for one-byte formats) -> raw
+// 16 bytes, round to nearest even (saturating for one-byte formats)
+template <int F>
+__device__ __forceinline__ uint4 pack16_rne(const float* v) {
+  uint32_t w[4];
+  if constexpr (F == RSM_F32) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) w[q] = __float_as_uint(v[q]);
+  } else if constexpr (F == RSM_BF16) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) w[q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
+  } else if constexpr (F == RSM_F16) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) w[q] = pack_f16x2(v[2 * q], v[2 * q + 1]);
+  } else if constexpr (F == RSM_I8) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t acc = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        int c = __float2int_rn(v[4 * q + b]);
+        c = c > 127 ? 127 : (c < -127 ? -127 : c);
+        acc |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * b);
+      }
+      w[q] = acc;
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      w[q] = f32x2_to_e4m3x2(v[4 * q], v[4 * q + 1]) | (f32x2_to_e4m3x2(v[4 * q + 2], v[4 * q + 3]) << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// stochastic rounding in place (values become exact grid points), then pack
+template <int F>
+__device__ __forceinline__ uint4 pack16_sr(float* v, const uint32_t* words) {
+  constexpr int n = Vec<F>::N;
+#pragma unroll
+  for (int u = 0; u < n; ++u) {
+    if constexpr (F == RSM_BF16) v[u] = sr_bf16(v[u], words[u]);
+    else if constexpr (F == RSM_F16) v[u] = sr_f16(v[u], words[u]);
+    else if constexpr (F == RSM_I8) v[u] = sr_i8(v[u], words[u]);
+    else if constexpr (F == RSM_FP8_E4M3) v[u] = sr_e4m3(v[u], words[u]);
+  }
+  return pack16_rne<F>(v);  // exact: every value is already representable
+}
+
+}  // namespace rsm

@@ -1,0 +1,616 @@
+// rsm_kernel.cuh -- the persistent sm_103a kernel for ReplaySSM prefix
+// materialization (flashinfer.mamba.replayssm_materialize, API page; the
+// persistent work-queue design of FlashInfer PR #4815, Description).
+//
+// Work item = (active request i, layer l, head h): one [dim, dstate] state tile.
+// Items are numbered request-major -> layer -> head and every CTA takes one
+// contiguous range of them, so consecutive items of a CTA share their
+// (request, layer) metadata and stream through contiguous state memory.
+//
+// One CTA = 1 loader warp + 8 consumer warps, joined by an S-stage ring in
+// shared memory:
+//   loader   : finds n (the first -1 of the active list), resolves the slot
+//              and pointer tables once per (request, layer), and per item
+//              issues bulk asynchronous copies (cp.async.bulk) of the source
+//              state tile (+ its scales), the k ring rows of x and of B, and
+//              4-byte cp.async copies of the k dt values and of A[h], all
+//              completing on the stage's "full" mbarrier.  Pads, out-of-range
+//              metadata and misaligned addresses are handled here.
+//   consumers: wait for "full", compute the decay of every token once per
+//              warp (exp(dt*A) with a shuffle suffix-product scan), apply the
+//              whole prefix to the tile in registers, requantize, store with
+//              16-byte streaming stores, and release the stage ("empty").
+// Every state element is read once and written once; the ring is only read.
+// Every wait is bounded in wall time (a logic error ends the kernel with a
+// status bit instead of hanging).
+//
+// The prefix is applied in closed form, which is the sequential recurrence
+// S <- a_t*S + dt_t x_t B_t^T unrolled exactly:
+//   S_k = P * S_0 + sum_t w_t x_t B_t^T,  P = prod_t a_t,  w_t = dt_t prod_{s>t} a_s,
+// costing one FFMA per element per token (plus one FMUL per element).
+#pragma once
+#include <cfloat>
+#include <cstdint>
+
+#include "rsm_formats.cuh"
+#include "rsm_params.h"
+#include "rsm_ptx.cuh"
+
+namespace rsm {
+
+struct alignas(16) ItemDesc {
+  unsigned long long dst_state;  // global address of the destination head tile
+  unsigned long long dst_scale;  // global address of the destination head's scales
+  int32_t k;                     // ring entries to apply; 0 = exact copy
+  uint32_t flags;
+  int32_t layer;
+  int32_t dst_slot;
+  int32_t head;
+  float A;                       // A[h]; landed by cp.async
+  uint32_t unused[2];
+};
+static_assert(sizeof(ItemDesc) == 48, "descriptor size");
+constexpr uint32_t kFlagEnd = 1u, kFlagDstAligned = 2u, kFlagScaleAligned = 4u;
+
+__device__ __forceinline__ void flag_status(uint32_t* status, uint32_t bits) {
+  if (status != nullptr && bits != 0u) atomicOr(status, bits);
+}
+
+// Warp-cooperative byte copy global -> shared for the rare misaligned item.
+__device__ __forceinline__ void copy_bytes_warp(unsigned char* dst, const unsigned char* src, uint32_t n,
+                                                int lane) {
+  for (uint32_t o = lane; o < n; o += 32) dst[o] = src[o];
+}
+
+template <int IF>
+struct In {
+  static constexpr int bytes = IF == RSM_F32 ? 4 : 2;
+};
+
+// CNT consecutive input elements (bf16 or fp32) from shared memory -> fp32.
+template <int IF, int CNT>
+__device__ __forceinline__ void load_inputs(const unsigned char* p, float* out) {
+  constexpr int bytes = CNT * In<IF>::bytes;
+  if constexpr (IF == RSM_F32) {
+    if constexpr (bytes % 16 == 0) {
+#pragma unroll
+      for (int q = 0; q < CNT / 4; ++q) {
+        const float4 v = reinterpret_cast<const float4*>(p)[q];
+        out[4 * q] = v.x;
+        out[4 * q + 1] = v.y;
+        out[4 * q + 2] = v.z;
+        out[4 * q + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < CNT; ++q) out[q] = reinterpret_cast<const float*>(p)[q];
+    }
+  } else {  // bf16
+    if constexpr (bytes % 16 == 0) {
+#pragma unroll
+      for (int q = 0; q < CNT / 8; ++q) {
+        const uint4 v = reinterpret_cast<const uint4*>(p)[q];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          out[8 * q + 2 * e] = bf16lo(w[e]);
+          out[8 * q + 2 * e + 1] = bf16hi(w[e]);
+        }
+      }
+    } else if constexpr (bytes == 8) {
+      const uint2 v = *reinterpret_cast<const uint2*>(p);
+      out[0] = bf16lo(v.x);
+      out[1] = bf16hi(v.x);
+      out[2] = bf16lo(v.y);
+      out[3] = bf16hi(v.y);
+    } else if constexpr (bytes == 4) {
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+      out[0] = bf16lo(v);
+      out[1] = bf16hi(v);
+    } else {
+#pragma unroll
+      for (int q = 0; q < CNT; ++q)
+        out[q] = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(p)[q]) << 16);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// loader warp
+// ---------------------------------------------------------------------------
+template <int SF, int IF, int D, int N>
+__device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem, int lane) {
+  constexpr int ES = Fmt<SF>::bytes;
+  constexpr int IE = In<IF>::bytes;
+  constexpr bool Q = Fmt<SF>::quant;
+  constexpr uint32_t kTileBytes = D * N * ES;
+  static_assert(kTileBytes % 16 == 0 && (D * IE) % 16 == 0 && (N * IE) % 16 == 0, "bulk copy sizes");
+
+  const uint32_t full0 = smem_addr(smem);
+  const uint32_t empty0 = full0 + 8u * kMaxStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
+
+  // n = position of the first -1 (entries after it are ignored)
+  int n = p.Bt;
+  for (int base = 0; base < p.Bt; base += 256) {
+    int v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int idx = base + 32 * q + lane;
+      v[q] = idx < p.Bt ? __ldg(p.active + idx) : 0;
+    }
+    int pos = -1;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint32_t m = __ballot_sync(0xFFFFFFFFu, v[q] == -1 && base + 32 * q + lane < p.Bt);
+      if (pos < 0 && m != 0u) pos = base + 32 * q + __ffs(m) - 1;
+    }
+    if (pos >= 0) {
+      n = pos;
+      break;
+    }
+  }
+
+  const int64_t LH = static_cast<int64_t>(p.L) * p.H;
+  const int64_t total = static_cast<int64_t>(n) * LH;
+  const int64_t w_begin = total * blockIdx.x / gridDim.x;
+  const int64_t w_end = total * (blockIdx.x + 1) / gridDim.x;
+  const int G = p.H / p.hpg;
+  const uint64_t policy = l2_policy_evict_first();
+
+  uint32_t stage = 0, phase = 0, fills = 0;
+  bool aborted = false;
+  int cur_i = -1, b = 0;
+  int64_t w = w_begin;
+  while (w < w_end && !aborted) {
+    const int i = static_cast<int>(w / LH);
+    const int64_t rem = w - static_cast<int64_t>(i) * LH;
+    const int l = static_cast<int>(rem / p.H);
+    int h = static_cast<int>(rem - static_cast<int64_t>(l) * p.H);
+    const int64_t seg_end = min(w_end, (static_cast<int64_t>(i) * p.L + l + 1) * p.H);
+
+    // per-layer table entries, one per lane, fetched together
+    int64_t tab = 0;
+    {
+      const int64_t* t = nullptr;
+      switch (lane) {
+        case 0: t = p.state_ptrs; break;
+        case 1: t = p.state_strides; break;
+        case 2: t = p.x_ptrs; break;
+        case 3: t = p.x_strides; break;
+        case 4: t = p.B_ptrs; break;
+        case 5: t = p.B_strides; break;
+        case 6: t = p.dt_ptrs; break;
+        case 7: t = p.dt_strides; break;
+        case 8: t = p.A_ptrs; break;
+        case 9: t = Q ? p.scale_ptrs : nullptr; break;
+        case 10: t = Q ? p.scale_strides : nullptr; break;
+        default: break;
+      }
+      if (t != nullptr) tab = __ldg(t + l);
+    }
+    if (i != cur_i) {
+      b = __ldg(p.active + i);
+      cur_i = i;
+    }
+    uint32_t bad = 0;
+    bool ok = true;
+    int src = p.pad, dst = p.pad, k = 0, rs = 0;
+    if (b < 0 || b >= p.Bt) {
+      bad |= RSM_STATUS_BAD_ACTIVE_INDEX;
+      ok = false;
+    } else {
+      src = __ldg(p.src_slots + static_cast<int64_t>(l) * p.Bt + b);
+      dst = __ldg(p.dst_slots + static_cast<int64_t>(l) * p.Bt + b);
+      k = __ldg(p.prefix_len + b);
+      rs = __ldg(p.ring_start + b);
+      if (k < 0 || k > p.W) {
+        bad |= RSM_STATUS_BAD_PREFIX_LEN;
+        ok = false;
+      }
+      if (rs < 0 || rs >= p.R) {
+        bad |= RSM_STATUS_BAD_RING_START;
+        ok = false;
+      }
+      if (src == p.pad || dst == p.pad) {
+        ok = false;
+      } else if (src < 0 || dst < 0) {
+        bad |= RSM_STATUS_BAD_SLOT;
+        ok = false;
+      }
+    }
+    if (lane == 0) flag_status(p.status, bad);
+    if (!ok) {
+      w = seg_end;
+      continue;
+    }
+    const unsigned char* state_base = reinterpret_cast<const unsigned char*>(__shfl_sync(0xFFFFFFFFu, tab, 0));
+    const int64_t state_stride = __shfl_sync(0xFFFFFFFFu, tab, 1);
+    const unsigned char* x_base = reinterpret_cast<const unsigned char*>(__shfl_sync(0xFFFFFFFFu, tab, 2));
+    const int64_t x_stride = __shfl_sync(0xFFFFFFFFu, tab, 3);
+    const unsigned char* B_base = reinterpret_cast<const unsigned char*>(__shfl_sync(0xFFFFFFFFu, tab, 4));
+    const int64_t B_stride = __shfl_sync(0xFFFFFFFFu, tab, 5);
+    const float* dt_base = reinterpret_cast<const float*>(__shfl_sync(0xFFFFFFFFu, tab, 6));
+    const int64_t dt_stride = __shfl_sync(0xFFFFFFFFu, tab, 7);
+    const float* A_base = reinterpret_cast<const float*>(__shfl_sync(0xFFFFFFFFu, tab, 8));
+    float* scale_base = reinterpret_cast<float*>(__shfl_sync(0xFFFFFFFFu, tab, 9));
+    const int64_t scale_stride = __shfl_sync(0xFFFFFFFFu, tab, 10);
+
+    const unsigned char* src_slot = state_base + static_cast<int64_t>(src) * state_stride * ES;
+    unsigned char* dst_slot = const_cast<unsigned char*>(state_base) + static_cast<int64_t>(dst) * state_stride * ES;
+    const unsigned char* x_slot = x_base + static_cast<int64_t>(src) * x_stride * IE;
+    const unsigned char* B_slot = B_base + static_cast<int64_t>(src) * B_stride * IE;
+    const float* dt_slot = dt_base + static_cast<int64_t>(src) * dt_stride;
+
+    for (; w < seg_end; ++w, ++h) {
+      if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, kWaitTimeoutNs) || *abort_flag) {
+        aborted = true;
+        break;
+      }
+      unsigned char* sb = smem + kStageBase + stage * p.stage_bytes;
+      const uint32_t sba = smem_addr(sb);
+      const uint32_t fullb = full0 + 8u * stage;
+      ItemDesc* desc = reinterpret_cast<ItemDesc*>(sb);
+
+      const int64_t tile_off = static_cast<int64_t>(h) * D * N * ES;
+      const unsigned char* src_tile = src_slot + tile_off;
+      unsigned char* dst_tile = dst_slot + tile_off;
+      const float* src_sc = nullptr;
+      float* dst_sc = nullptr;
+      if constexpr (Q) {
+        src_sc = scale_base + static_cast<int64_t>(src) * scale_stride + static_cast<int64_t>(h) * D;
+        dst_sc = scale_base + static_cast<int64_t>(dst) * scale_stride + static_cast<int64_t>(h) * D;
+      }
+      const int g = h / p.hpg;
+      const float* A_ptr = A_base + h;
+
+      // this lane's tokens: t = lane and t = lane + 32
+      const unsigned char* xrow[2] = {nullptr, nullptr};
+      const unsigned char* brow[2] = {nullptr, nullptr};
+      const float* dtp[2] = {nullptr, nullptr};
+      bool aligned = (reinterpret_cast<uintptr_t>(src_tile) & 15u) == 0u;
+      if constexpr (Q) aligned = aligned && (reinterpret_cast<uintptr_t>(src_sc) & 15u) == 0u;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int t = lane + 32 * q;
+        if (t < k) {
+          const int pr = (rs + t) % p.R;
+          xrow[q] = x_slot + (static_cast<int64_t>(pr) * p.H + h) * D * IE;
+          brow[q] = B_slot + (static_cast<int64_t>(pr) * G + g) * N * IE;
+          dtp[q] = dt_slot + static_cast<int64_t>(pr) * p.H + h;
+          aligned = aligned && (reinterpret_cast<uintptr_t>(xrow[q]) & 15u) == 0u &&
+                    (reinterpret_cast<uintptr_t>(brow[q]) & 15u) == 0u &&
+                    (reinterpret_cast<uintptr_t>(dtp[q]) & 3u) == 0u;
+        }
+      }
+      if (k > 0) aligned = aligned && (reinterpret_cast<uintptr_t>(A_ptr) & 3u) == 0u;
+      aligned = __all_sync(0xFFFFFFFFu, aligned);
+
+      if (lane == 0) {
+        desc->dst_state = reinterpret_cast<unsigned long long>(dst_tile);
+        desc->dst_scale = reinterpret_cast<unsigned long long>(dst_sc);
+        desc->k = k;
+        desc->flags = ((reinterpret_cast<uintptr_t>(dst_tile) & 15u) == 0u ? kFlagDstAligned : 0u) |
+                      ((reinterpret_cast<uintptr_t>(dst_sc) & 3u) == 0u ? kFlagScaleAligned : 0u);
+        desc->layer = l;
+        desc->dst_slot = dst;
+        desc->head = h;
+      }
+      if (aligned) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          mbar_expect_tx(fullb, kTileBytes + (Q ? D * 4u : 0u) + static_cast<uint32_t>(k) * (D + N) * IE);
+        }
+        __syncwarp();
+        if (lane == 0) {
+          bulk_g2s_hint(sba + p.off_state, src_tile, kTileBytes, fullb, policy);
+          if constexpr (Q) bulk_g2s(sba + p.off_scale, src_sc, D * 4u, fullb);
+          if (k > 0) cp_async_4(sba + static_cast<uint32_t>(offsetof(ItemDesc, A)), A_ptr);
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int t = lane + 32 * q;
+          if (t < k) {
+            bulk_g2s(sba + p.off_x + static_cast<uint32_t>(t) * D * IE, xrow[q], D * IE, fullb);
+            bulk_g2s(sba + p.off_B + static_cast<uint32_t>(t) * N * IE, brow[q], N * IE, fullb);
+            cp_async_4(sba + p.off_dt + 4u * t, dtp[q]);
+          }
+        }
+        cp_async_mbar_arrive(fullb);
+      } else {
+        // any alignment: plain byte copies by the whole warp
+        copy_bytes_warp(sb + p.off_state, src_tile, kTileBytes, lane);
+        if constexpr (Q)
+          copy_bytes_warp(sb + p.off_scale, reinterpret_cast<const unsigned char*>(src_sc), D * 4u, lane);
+        for (int t = 0; t < k; ++t) {
+          const int pr = (rs + t) % p.R;
+          copy_bytes_warp(sb + p.off_x + t * D * IE, x_slot + (static_cast<int64_t>(pr) * p.H + h) * D * IE,
+                          D * IE, lane);
+          copy_bytes_warp(sb + p.off_B + t * N * IE, B_slot + (static_cast<int64_t>(pr) * G + g) * N * IE,
+                          N * IE, lane);
+          copy_bytes_warp(sb + p.off_dt + 4 * t,
+                          reinterpret_cast<const unsigned char*>(dt_slot + static_cast<int64_t>(pr) * p.H + h), 4,
+                          lane);
+        }
+        if (k > 0)
+          copy_bytes_warp(sb + offsetof(ItemDesc, A), reinterpret_cast<const unsigned char*>(A_ptr), 4, lane);
+        __threadfence_block();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(fullb);
+      ++fills;
+      if (++stage == p.stages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+
+  // end marker for the consumers
+  bool ended = false;
+  if (!aborted && mbar_wait(empty0 + 8u * stage, phase ^ 1u, kWaitTimeoutNs)) {
+    if (lane == 0) reinterpret_cast<ItemDesc*>(smem + kStageBase + stage * p.stage_bytes)->flags = kFlagEnd;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(full0 + 8u * stage);
+    ended = true;
+  }
+  if (!ended) {
+    if (lane == 0) {
+      *abort_flag = 1;
+      flag_status(p.status, RSM_STATUS_WAIT_TIMEOUT);
+    }
+    // let copies already issued into the ring land before the CTA exits: the
+    // last fill of stage s completed the full-barrier phase of parity `phase`
+    // (s < stage) or `phase ^ 1` (s >= stage, if the ring went round once)
+    for (uint32_t s = 0; s < p.stages; ++s) {
+      if (s < stage)
+        (void)mbar_wait(full0 + 8u * s, phase, 1000000ull);
+      else if (fills >= p.stages)
+        (void)mbar_wait(full0 + 8u * s, phase ^ 1u, 1000000ull);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// consumer warps
+// ---------------------------------------------------------------------------
+template <int SF, int IF, int D, int N>
+__device__ __forceinline__ void run_consumer(const Params& p, unsigned char* smem, int cw, int lane) {
+  constexpr int ES = Fmt<SF>::bytes;
+  constexpr int IE = In<IF>::bytes;
+  constexpr bool Q = Fmt<SF>::quant;
+  constexpr int VEC = Vec<SF>::N;          // elements per 16-byte vector
+  constexpr int TC = N / VEC;              // threads across one row
+  constexpr int TR_ALL = kConsumerThreads / TC;
+  constexpr int TR = TR_ALL < D ? TR_ALL : D;  // row groups that hold work
+  constexpr int RPT = D / TR;              // rows per thread
+  static_assert(N % VEC == 0 && TC <= 32 && 32 % TC == 0, "thread layout");
+  static_assert(D % TR == 0, "rows must split evenly");
+  static_assert(!Q || TR_ALL <= D, "one-byte formats need every consumer thread busy");
+
+  const uint32_t full0 = smem_addr(smem);
+  const uint32_t empty0 = full0 + 8u * kMaxStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
+  float* wbuf = reinterpret_cast<float*>(smem + kWeightOff) + cw * kWeightStride;
+
+  const int ct = cw * 32 + lane;
+  const int tc = ct % TC, rg = ct / TC;
+  const bool worker = rg < TR;
+  const int row0 = rg * RPT, col0 = tc * VEC;
+
+  uint32_t key0 = 0, key1 = 0;
+  const bool sr = p.philox_rounds > 0;
+  if (sr) {
+    const uint64_t s = static_cast<uint64_t>(__ldg(p.rand_seed));
+    key0 = static_cast<uint32_t>(s);
+    key1 = static_cast<uint32_t>(s >> 32);
+  }
+
+  uint32_t stage = 0, phase = 0;
+  for (;;) {
+    if (!mbar_wait(full0 + 8u * stage, phase, kWaitTimeoutNs) || *abort_flag) {
+      if (lane == 0) {
+        *abort_flag = 1;
+        flag_status(p.status, RSM_STATUS_WAIT_TIMEOUT);
+      }
+      break;
+    }
+    const unsigned char* sb = smem + kStageBase + stage * p.stage_bytes;
+    const ItemDesc* desc = reinterpret_cast<const ItemDesc*>(sb);
+    const uint32_t flags = desc->flags;
+    if (flags & kFlagEnd) break;
+    const int k = desc->k;
+    unsigned char* dst_tile = reinterpret_cast<unsigned char*>(desc->dst_state);
+    float* dst_sc = reinterpret_cast<float*>(desc->dst_scale);
+    const bool dst_aligned = (flags & kFlagDstAligned) != 0u;
+
+    if (k == 0) {
+      // exact copy of the source tile (and scales)
+      if (worker) {
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+          const uint32_t off = ((row0 + r) * N + col0) * ES;
+          const uint4 raw = *reinterpret_cast<const uint4*>(sb + p.off_state + off);
+          if (dst_aligned) {
+            stg128_stream(dst_tile + off, raw);
+          } else {
+            const unsigned char* rb = reinterpret_cast<const unsigned char*>(&raw);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) dst_tile[off + q] = rb[q];
+          }
+        }
+      }
+      if constexpr (Q) {
+        for (int r = ct; r < D; r += kConsumerThreads) {
+          const float v = reinterpret_cast<const float*>(sb + p.off_scale)[r];
+          if (flags & kFlagScaleAligned) {
+            dst_sc[r] = v;
+          } else {
+            const unsigned char* vb = reinterpret_cast<const unsigned char*>(&v);
+            unsigned char* db = reinterpret_cast<unsigned char*>(dst_sc + r);
+            for (int q = 0; q < 4; ++q) db[q] = vb[q];
+          }
+        }
+      }
+    } else {
+      // decay of each token, once per warp: a_t = exp(dt_t*A), then
+      // w_t = dt_t * prod_{s>t} a_s and P = prod_t a_t by a suffix-product scan
+      const float A = desc->A;
+      const float* dts = reinterpret_cast<const float*>(sb + p.off_dt);
+      float carry = 1.0f;
+      for (int c = (k - 1) >> 5; c >= 0; --c) {
+        const int t = 32 * c + lane;
+        const float dtv = t < k ? dts[t] : 0.0f;
+        const float a = t < k ? expf(dtv * A) : 1.0f;
+        float incl = a;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float v = __shfl_down_sync(0xFFFFFFFFu, incl, off);
+          if (lane + off < 32) incl *= v;
+        }
+        float excl = __shfl_down_sync(0xFFFFFFFFu, incl, 1);
+        if (lane == 31) excl = 1.0f;
+        if (t < k) wbuf[t] = dtv * (excl * carry);
+        carry *= __shfl_sync(0xFFFFFFFFu, incl, 0);
+      }
+      if (lane == 0) wbuf[kMaxWindow] = carry;
+      __syncwarp();
+
+      // load + dequantize this thread's [RPT, VEC] block of the tile
+      float s[RPT][VEC];
+      if (worker) {
+        const float P = wbuf[kMaxWindow];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+          const uint4 raw =
+              *reinterpret_cast<const uint4*>(sb + p.off_state + ((row0 + r) * N + col0) * ES);
+          unpack16<SF>(raw, s[r]);
+          if constexpr (Q) {
+            const float sc = reinterpret_cast<const float*>(sb + p.off_scale)[row0 + r];
+#pragma unroll
+            for (int u = 0; u < VEC; ++u) s[r][u] = __fmul_rn(s[r][u], sc);
+          }
+#pragma unroll
+          for (int u = 0; u < VEC; ++u) s[r][u] *= P;
+        }
+        // the whole prefix, one rank-1 update per token
+        const unsigned char* xs = sb + p.off_x;
+        const unsigned char* Bs = sb + p.off_B;
+#pragma unroll 2
+        for (int t = 0; t < k; ++t) {
+          const float wt = wbuf[t];
+          float c[RPT], bv[VEC];
+          load_inputs<IF, RPT>(xs + (t * D + row0) * IE, c);
+          load_inputs<IF, VEC>(Bs + (t * N + col0) * IE, bv);
+#pragma unroll
+          for (int r = 0; r < RPT; ++r) {
+            const float cr = c[r] * wt;
+#pragma unroll
+            for (int u = 0; u < VEC; ++u) s[r][u] = fmaf(cr, bv[u], s[r][u]);
+          }
+        }
+      }
+
+      // requantize + store
+      const int h = desc->head;
+#pragma unroll
+      for (int r = 0; r < RPT; ++r) {
+        float scale_out = 0.0f;
+        if constexpr (Q) {
+          // symmetric per-(head, row) scale; all threads take part in the shuffles
+          float amax = 0.0f;
+#pragma unroll
+          for (int u = 0; u < VEC; ++u) amax = fmaxf(amax, fabsf(s[r][u]));
+#pragma unroll
+          for (int off = TC / 2; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+          constexpr float qmax = SF == RSM_I8 ? 127.0f : 448.0f;
+          const float scale = __fdiv_rn(amax, qmax);
+          const float inv = __fdiv_rn(qmax, amax);
+          const bool zero_row = !(inv <= FLT_MAX);
+#pragma unroll
+          for (int u = 0; u < VEC; ++u) s[r][u] = zero_row ? 0.0f : __fmul_rn(s[r][u], inv);
+          scale_out = zero_row ? 0.0f : scale;
+        }
+        if (!worker) continue;
+        uint4 out;
+        bool use_sr = false;
+        if constexpr (SF != RSM_F32) use_sr = sr;
+        if (use_sr) {
+          uint32_t words[VEC];
+          const int64_t e0 = (static_cast<int64_t>(h) * D + row0 + r) * N + col0;
+#pragma unroll
+          for (int q = 0; q < (VEC >= 4 ? VEC / 4 : 1); ++q) {
+            const uint4 rnd = philox4x32(
+                make_uint4(static_cast<uint32_t>((e0 >> 2) + q), static_cast<uint32_t>(desc->dst_slot),
+                           static_cast<uint32_t>(desc->layer), 0u),
+                key0, key1, p.philox_rounds);
+            if (4 * q + 0 < VEC) words[4 * q + 0] = rnd.x;
+            if (4 * q + 1 < VEC) words[4 * q + 1] = rnd.y;
+            if (4 * q + 2 < VEC) words[4 * q + 2] = rnd.z;
+            if (4 * q + 3 < VEC) words[4 * q + 3] = rnd.w;
+          }
+          out = pack16_sr<SF>(s[r], words);
+        } else {
+          out = pack16_rne<SF>(s[r]);
+        }
+        const uint32_t off = ((row0 + r) * N + col0) * ES;
+        if (dst_aligned) {
+          stg128_stream(dst_tile + off, out);
+        } else {
+          const unsigned char* ob = reinterpret_cast<const unsigned char*>(&out);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) dst_tile[off + q] = ob[q];
+        }
+        if constexpr (Q) {
+          if (tc == 0) {
+            if (flags & kFlagScaleAligned) {
+              dst_sc[row0 + r] = scale_out;
+            } else {
+              const unsigned char* vb = reinterpret_cast<const unsigned char*>(&scale_out);
+              unsigned char* db = reinterpret_cast<unsigned char*>(dst_sc + row0 + r);
+              for (int q = 0; q < 4; ++q) db[q] = vb[q];
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8u * stage);
+    if (++stage == p.stages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
+template <int SF, int IF, int D, int N>
+__global__ void __launch_bounds__(kThreads, 2) materialize_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  // empty active list: one load, then out
+  if (__ldg(p.active) == -1) return;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    const uint32_t full0 = smem_addr(smem);
+    for (uint32_t s = 0; s < p.stages; ++s) {
+      mbar_init(full0 + 8u * s, 1u);
+      mbar_init(full0 + 8u * kMaxStages + 8u * s, kConsumerWarps);
+    }
+    *reinterpret_cast<volatile int*>(smem + kAbortOff) = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == 0)
+    run_loader<SF, IF, D, N>(p, smem, lane);
+  else
+    run_consumer<SF, IF, D, N>(p, smem, warp - 1, lane);
+}
+
+// Instantiation hook: each translation unit that includes this header with
+// RSM_INSTANTIATE defined provides kernel_for<...>() for its formats.
+template <int SF, int IF, int D, int N>
+const void* kernel_for() {
+  return reinterpret_cast<const void*>(&materialize_kernel<SF, IF, D, N>);
+}
+
+}  // namespace rsm

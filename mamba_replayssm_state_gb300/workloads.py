@@ -248,3 +248,176 @@ def ring_bytes_per_token(shape: Shape) -> int:
     """Algorithmic ring bytes per (layer, replayed token): x per head, B per group, dt per head."""
     ie = ELEM_SIZE[shape.input_dtype]
     return shape.H * shape.D * ie + shape.G * shape.N * ie + shape.H * 4
+
+
+# ---------------------------------------------------------------------------
+# device-side worlds (torch CUDA tensors + the call's pointer tables)
+# ---------------------------------------------------------------------------
+
+TORCH_STORAGE = {"f32": "float32", "bf16": "bfloat16", "f16": "float16", "i8": "int8", "fp8_e4m3": "uint8"}
+
+
+@dataclass
+class DeviceWorld:
+    """All inputs of one call on a CUDA device, with the call's pointer tables."""
+    shape: Shape
+    state: list
+    scale: list
+    x: list
+    B: list
+    dt: list
+    A: list
+    src_slots: object
+    dst_slots: object
+    ring_start: object
+    replay_prefix_len: object
+    active: object
+    rand_seed: object
+    status: object
+    tables: dict
+    pool: int
+
+    def call_kwargs(self) -> dict:
+        s = self.shape
+        t = self.tables
+        return dict(
+            state_ptrs=t["state_ptrs"], state_slot_strides=t["state_slot_strides"],
+            x_cache_ptrs=t["x_cache_ptrs"], x_cache_slot_strides=t["x_cache_slot_strides"],
+            B_cache_ptrs=t["B_cache_ptrs"], B_cache_slot_strides=t["B_cache_slot_strides"],
+            dt_cache_ptrs=t["dt_cache_ptrs"], dt_cache_slot_strides=t["dt_cache_slot_strides"],
+            A_ptrs=t["A_ptrs"], state_scale_ptrs=t["state_scale_ptrs"],
+            state_scale_slot_strides=t["state_scale_slot_strides"],
+            src_slots=self.src_slots, dst_slots=self.dst_slots, ring_start=self.ring_start,
+            replay_prefix_len=self.replay_prefix_len, active_request_indices=self.active,
+            state_dtype=s.state_dtype, input_dtype=s.input_dtype, matrixA_dtype=s.A_dtype, dim=s.D,
+            dstate=s.N, num_heads=s.H, heads_per_group=s.hpg, max_window=s.W, ring_buffer_len=s.R,
+            pad_slot_id=s.pad_slot_id, rand_seed=self.rand_seed, philox_rounds=s.philox_rounds,
+            device_status=self.status)
+
+    def set_active(self, active_np) -> None:
+        import torch
+        self.active.copy_(torch.from_numpy(np.ascontiguousarray(active_np, np.int32)))
+
+
+def _tables(state, scale, x, B, dt, A, device):
+    import torch
+
+    def ptrs(lst):
+        return torch.tensor([0 if t is None else t.data_ptr() for t in lst], dtype=torch.int64, device=device)
+
+    def strides(lst):
+        return torch.tensor([0 if t is None else t.stride(0) for t in lst], dtype=torch.int64, device=device)
+
+    return dict(state_ptrs=ptrs(state), state_slot_strides=strides(state), x_cache_ptrs=ptrs(x),
+                x_cache_slot_strides=strides(x), B_cache_ptrs=ptrs(B), B_cache_slot_strides=strides(B),
+                dt_cache_ptrs=ptrs(dt), dt_cache_slot_strides=strides(dt), A_ptrs=ptrs(A),
+                state_scale_ptrs=ptrs(scale), state_scale_slot_strides=strides(scale))
+
+
+def _np_to_torch(a: np.ndarray):
+    import torch
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(np.ascontiguousarray(a))
+
+
+def _meta_tensors(meta_arrays: dict, device):
+    return {k: _np_to_torch(v).to(device) for k, v in meta_arrays.items()}
+
+
+def device_world_from_host(hw: HostWorld, device="cuda") -> DeviceWorld:
+    """Copies a host world to the device, byte for byte."""
+    import torch
+    mv = lambda lst: [None if a is None else _np_to_torch(a).to(device) for a in lst]
+    state, scale, x, B, dt, A = mv(hw.state), mv(hw.scale), mv(hw.x), mv(hw.B), mv(hw.dt), mv(hw.A)
+    meta = _meta_tensors(dict(src_slots=hw.src_slots, dst_slots=hw.dst_slots, ring_start=hw.ring_start,
+                              replay_prefix_len=hw.replay_prefix_len, active=hw.active), device)
+    seed = torch.tensor([hw.rand_seed], dtype=torch.int64, device=device) if hw.philox_rounds > 0 else None
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    return DeviceWorld(hw.shape, state, scale, x, B, dt, A, meta["src_slots"], meta["dst_slots"],
+                       meta["ring_start"], meta["replay_prefix_len"], meta["active"], seed, status,
+                       _tables(state, scale, x, B, dt, A, device), hw.meta["pool"])
+
+
+def device_world_random(shape: Shape, seed: int = 0, device="cuda", metadata: dict | None = None) -> DeviceWorld:
+    """Draws a full-size world directly on the device (torch's seeded CUDA
+    generator), same recipe as host_world; metadata is drawn on the host."""
+    import torch
+    rng = np.random.default_rng(seed)
+    meta = metadata if metadata is not None else draw_metadata(shape, rng)
+    pool = meta["pool"]
+    half = pool // 2
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    L, H, G, D, N, R = shape.L, shape.H, shape.G, shape.D, shape.N, shape.R
+    sd, idt = shape.state_dtype, shape.input_dtype
+    tdt = getattr(torch, TORCH_STORAGE[sd])
+    in_t = torch.float32 if idt == "f32" else torch.bfloat16
+    state, scale, x, B, dt, A = [], [], [], [], [], []
+    for _ in range(L):
+        if sd in ("f32", "bf16", "f16"):
+            st = torch.randn((pool, H, D, N), generator=g, device=device, dtype=tdt)
+        elif sd == "i8":
+            st = torch.randint(-127, 128, (pool, H, D, N), generator=g, device=device, dtype=torch.int8)
+        else:  # fp8 codes: any byte except the two NaN patterns
+            st = torch.randint(0, 254, (pool, H, D, N), generator=g, device=device, dtype=torch.uint8)
+            st = torch.where(st >= 0x7F, st + 1, st)
+        st.view(torch.uint8).view(pool, -1)[half:].fill_(0xFF)
+        state.append(st)
+        if sd in QUANTIZED:
+            qmax = 127.0 if sd == "i8" else 448.0
+            sc = torch.empty((pool, H, D), device=device, dtype=torch.float32).uniform_(0.5, 2.0, generator=g)
+            sc.mul_(4.0 / qmax)
+            sc.view(torch.uint8).view(pool, -1)[half:].fill_(0xFF)
+            scale.append(sc)
+        else:
+            scale.append(None)
+        x.append(torch.randn((pool, R, H, D), generator=g, device=device, dtype=in_t))
+        B.append(torch.randn((pool, R, G, N), generator=g, device=device, dtype=in_t))
+        dt.append(torch.empty((pool, R, H), device=device, dtype=torch.float32).uniform_(0.001, 0.1, generator=g))
+        A.append(-torch.empty(H, device=device, dtype=torch.float32).uniform_(0.5, 2.0, generator=g))
+    mt = _meta_tensors(dict(src_slots=meta["src_slots"], dst_slots=meta["dst_slots"],
+                            ring_start=meta["ring_start"], replay_prefix_len=meta["replay_prefix_len"],
+                            active=meta["active"]), device)
+    seed_t = torch.tensor([shape.rand_seed], dtype=torch.int64, device=device) if shape.philox_rounds > 0 else None
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    return DeviceWorld(shape, state, scale, x, B, dt, A, mt["src_slots"], mt["dst_slots"], mt["ring_start"],
+                       mt["replay_prefix_len"], mt["active"], seed_t, status,
+                       _tables(state, scale, x, B, dt, A, device), pool)
+
+
+def _to_np(t) -> np.ndarray:
+    import torch
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16).copy()
+    return t.numpy().copy()
+
+
+def host_subworld(dw: DeviceWorld, layer: int, request: int, k=None, rs=None) -> HostWorld:
+    """A one-layer, one-request host world holding the source slot (as slot 0,
+    with its ring) of (layer, request) of a device world; the destination is
+    slot 1.  Used to check sampled outputs of full-size calls one by one."""
+    src = int(dw.src_slots[layer, request])
+    shape = dw.shape.replace(L=1, Bt=1, n_active=1, pool=2, special="", pad_frac=0.0)
+    grab = lambda t: None if t is None else _to_np(t[src:src + 1])
+    state = _to_np(dw.state[layer][src:src + 1])
+    state = np.concatenate([state, np.full_like(state, 0)])
+    state.view(np.uint8)[1:] = 0xFF
+    scale = None
+    if dw.scale[layer] is not None:
+        sc = _to_np(dw.scale[layer][src:src + 1])
+        scale = np.concatenate([sc, np.zeros_like(sc)])
+        scale.view(np.uint8)[1:] = 0xFF
+    x = np.concatenate([grab(dw.x[layer])] * 2)
+    B = np.concatenate([grab(dw.B[layer])] * 2)
+    dt = np.concatenate([grab(dw.dt[layer])] * 2)
+    A = _to_np(dw.A[layer])
+    kk = int(dw.replay_prefix_len[request]) if k is None else k
+    rr = int(dw.ring_start[request]) if rs is None else rs
+    dst = int(dw.dst_slots[layer, request])
+    w = HostWorld(shape, [np.ascontiguousarray(state)], [scale], [x], [B], [dt], [A],
+                  np.array([[0]], np.int32), np.array([[1]], np.int32), np.array([rr], np.int32),
+                  np.array([kk], np.int32), np.array([0], np.int32),
+                  rand_seed=dw.shape.rand_seed, meta={"pool": 2, "dst_slot_in_call": dst, "layer_in_call": layer})
+    return w

@@ -1,0 +1,278 @@
+"""CUDA path against the CPU oracle, element by element, through the C ABI.
+
+Small worlds are compared in full (every slot of every layer); the full-size
+headline call is checked on sampled (layer, request) outputs, each recomputed
+by the oracle from its own copy of the inputs, plus properties that hold at
+any size.  Tolerances are in tests/parity.py.
+"""
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+import mamba_replayssm_state_gb300 as rsm
+from mamba_replayssm_state_gb300 import workloads as wl
+
+from parity import compare_slot, compare_worlds, written_dsts
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+
+def run_cuda(hw, status_expected=0):
+    """Runs the CUDA path on a copy of host world `hw`; returns the host copy of the result."""
+    dw = wl.device_world_from_host(hw)
+    rsm.replayssm_materialize(**dw.call_kwargs())
+    torch.cuda.synchronize()
+    got = hw.copy()
+    got.state = [wl._to_np(t).view(a.dtype) for t, a in zip(dw.state, hw.state)]
+    got.scale = [None if t is None else wl._to_np(t) for t in dw.scale]
+    status = int(dw.status.item())
+    assert status == status_expected, f"device status {status:#x}"
+    return got
+
+
+def run_oracle(hw):
+    ref = hw.copy()
+    oracle.materialize(ref)
+    return ref
+
+
+def check(hw, exact=False):
+    got = run_cuda(hw)
+    ref = run_oracle(hw)
+    return compare_worlds(got, ref, hw, exact=exact)
+
+
+# ----------------------------------------------------------------------------
+# the named workloads, reduced so that the oracle takes seconds
+# ----------------------------------------------------------------------------
+
+def test_tiny_all_active():
+    hw = wl.host_world(wl.SHAPES["tiny_fp32"], seed=0)
+    assert check(hw) >= 4
+
+
+def test_tiny_three_active_then_terminator():
+    hw = wl.host_world(wl.SHAPES["tiny_fp32"], seed=1)
+    hw.active[3] = -1
+    assert check(hw) >= 3
+
+
+def test_tiny_entries_after_terminator_ignored():
+    hw = wl.host_world(wl.SHAPES["tiny_fp32"], seed=2)
+    b = hw.active.copy()
+    hw.active[:] = [b[0], -1, b[2], b[3]]
+    check(hw)
+
+
+def test_empty_active_list_writes_nothing():
+    hw = wl.host_world(wl.SHAPES["tiny_fp32"], seed=3)
+    hw.active[:] = -1
+    got = run_cuda(hw)
+    for l in range(hw.L):
+        assert got.state[l].tobytes() == hw.state[l].tobytes()
+
+
+REDUCED = [
+    ("mamba2_2p7b_fp32", dict(L=3, Bt=8, n_active=6)),
+    ("hybrid48_bf16", dict(L=2, Bt=6, n_active=5)),
+    ("hybrid48_int8", dict(L=2, Bt=4, n_active=3)),
+    ("hybrid48_fp8_sr", dict(L=2, Bt=4, n_active=3)),
+    ("ring_sweep_fp16", dict(L=2, Bt=6, n_active=6, prefix=("fixed", 16))),
+]
+
+
+@pytest.mark.parametrize("name,over", REDUCED, ids=[r[0] for r in REDUCED])
+def test_named_workload_reduced(name, over):
+    hw = wl.host_world(wl.SHAPES[name].replace(**over), seed=11)
+    assert check(hw) >= 1
+
+
+@pytest.mark.parametrize("k", [0, 1, 4, 16, 64])
+def test_ring_sweep_prefix_lengths(k):
+    shape = wl.SHAPES["ring_sweep_fp16"].replace(L=2, Bt=5, n_active=5, prefix=("fixed", k), pad_frac=0.2)
+    hw = wl.host_world(shape, seed=100 + k)
+    check(hw)
+
+
+# ----------------------------------------------------------------------------
+# every compiled instance
+# ----------------------------------------------------------------------------
+
+WIDE = [(sd, idt, d, n) for sd in ("f32", "bf16", "f16") for idt in ("bf16", "f32")
+        for d, n in ((16, 16), (64, 64), (64, 128))]
+BYTE = [(sd, idt, 64, 128) for sd in ("i8", "fp8_e4m3") for idt in ("bf16", "f32")]
+
+
+@pytest.mark.parametrize("sd,idt,D,N", WIDE + BYTE, ids=lambda v: str(v))
+def test_every_instance(sd, idt, D, N):
+    shape = wl.Shape("inst", L=2, Bt=5, H=6, hpg=3, D=D, N=N, R=8, W=8, state_dtype=sd, input_dtype=idt,
+                     n_active=4, ring_start=(0, 8), prefix=("uniform", 0, 8))
+    hw = wl.host_world(shape, seed=zlib.crc32(repr((sd, idt, D, N)).encode()) % 1000)
+    check(hw)
+
+
+@pytest.mark.parametrize("sd", ["bf16", "f16", "i8", "fp8_e4m3"])
+def test_stochastic_rounding_every_format(sd):
+    shape = wl.Shape("sr", L=2, Bt=4, H=4, hpg=2, D=64, N=128, R=8, W=8, state_dtype=sd, n_active=4,
+                     philox_rounds=10, rand_seed=0x1234_5678_9ABC)
+    hw = wl.host_world(shape, seed=7)
+    check(hw)
+
+
+@pytest.mark.parametrize("sd", ["bf16", "f16", "i8", "fp8_e4m3"])
+@pytest.mark.parametrize("rounds", [0, 10])
+def test_requantization_is_bit_exact_when_state_is_unchanged(sd, rounds):
+    """dt = 0 makes the replay an identity in any precision, so the rewrite of the
+    source state (RNE or stochastic: same words, same decisions) is bit-exact."""
+    shape = wl.Shape("dt0", L=2, Bt=4, H=4, hpg=2, D=64, N=128, R=8, W=8, state_dtype=sd, n_active=4,
+                     prefix=("uniform", 1, 8), philox_rounds=rounds, rand_seed=0x5EED)
+    hw = wl.host_world(shape, seed=9)
+    for a in hw.dt:
+        a[:] = 0.0
+    check(hw, exact=True)
+
+
+# ----------------------------------------------------------------------------
+# edge cases
+# ----------------------------------------------------------------------------
+
+def _offset_copy(a: np.ndarray, offset_elems: int) -> np.ndarray:
+    """Same contents, stored `offset_elems` elements past an aligned base."""
+    buf = np.zeros(a.size + offset_elems, dtype=a.dtype)
+    v = buf[offset_elems:].reshape(a.shape)
+    v[...] = a
+    return v
+
+
+def test_misaligned_state_and_ring_take_the_byte_path():
+    shape = wl.Shape("mis", L=2, Bt=4, H=4, hpg=2, D=64, N=128, R=8, W=8, state_dtype="bf16", n_active=4)
+    hw = wl.host_world(shape, seed=21)
+    hw.state[0] = _offset_copy(hw.state[0], 1)   # 2-byte offset: source and destination tiles misaligned
+    hw.x[1] = _offset_copy(hw.x[1], 1)           # ring rows misaligned in layer 1
+    # device copies keep the offset: build the device world by hand
+    dw = wl.device_world_from_host(hw)
+    for l, arr in ((0, hw.state[0]),):
+        buf = torch.zeros(arr.size + 1, dtype=torch.int16, device="cuda")
+        view = buf[1:].view(arr.shape)
+        view.copy_(torch.from_numpy(arr.view(np.int16).copy()))
+        dw.state[l] = view
+    buf = torch.zeros(hw.x[1].size + 1, dtype=torch.int16, device="cuda")
+    xv = buf[1:].view(hw.x[1].shape)
+    xv.copy_(torch.from_numpy(hw.x[1].view(np.int16).copy()))
+    dw.x[1] = xv
+    dw.tables = wl._tables(dw.state, dw.scale, dw.x, dw.B, dw.dt, dw.A, "cuda")
+    assert dw.state[0].data_ptr() % 16 == 2
+    rsm.replayssm_materialize(**dw.call_kwargs())
+    torch.cuda.synchronize()
+    got = hw.copy()
+    got.state = [wl._to_np(t).view(a.dtype) for t, a in zip(dw.state, hw.state)]
+    compare_worlds(got, run_oracle(hw), hw)
+
+
+def test_misaligned_scales():
+    shape = wl.Shape("mis8", L=1, Bt=3, H=4, hpg=2, D=64, N=128, R=8, W=8, state_dtype="i8", n_active=3)
+    hw = wl.host_world(shape, seed=22)
+    dw = wl.device_world_from_host(hw)
+    sc = hw.scale[0]
+    buf = torch.zeros(sc.size + 1, dtype=torch.float32, device="cuda")
+    v = buf[1:].view(sc.shape)
+    v.copy_(torch.from_numpy(sc))
+    dw.scale[0] = v
+    dw.tables = wl._tables(dw.state, dw.scale, dw.x, dw.B, dw.dt, dw.A, "cuda")
+    rsm.replayssm_materialize(**dw.call_kwargs())
+    torch.cuda.synchronize()
+    got = hw.copy()
+    got.state = [wl._to_np(t) for t in dw.state]
+    got.scale = [wl._to_np(t) for t in dw.scale]
+    compare_worlds(got, run_oracle(hw), hw)
+
+
+def test_pad_slot_id_zero():
+    """With pad_slot_id = 0, slot 0 is the sentinel and -1 is not."""
+    shape = wl.SHAPES["tiny_fp32"].replace(pad_slot_id=0, special="")
+    hw = wl.host_world(shape, seed=31)
+    hw.src_slots[0, int(hw.active[0])] = 0
+    assert (0, int(hw.dst_slots[0, int(hw.active[0])])) not in written_dsts(hw)
+    check(hw)
+
+
+@pytest.mark.parametrize("bad,bit", [("prefix", 4), ("ring_start", 2), ("active", 1), ("slot", 8)])
+def test_out_of_range_metadata_is_skipped_and_flagged(bad, bit):
+    shape = wl.Shape("bad", L=2, Bt=4, H=4, hpg=2, D=64, N=128, R=8, W=8, state_dtype="bf16", n_active=4)
+    hw = wl.host_world(shape, seed=41)
+    victim = int(hw.active[1])
+    if bad == "prefix":
+        hw.replay_prefix_len[victim] = shape.W + 1
+    elif bad == "ring_start":
+        hw.ring_start[victim] = shape.R
+    elif bad == "active":
+        hw.active[1] = shape.Bt + 5
+    else:
+        hw.src_slots[0, victim] = -7
+    got = run_cuda(hw, status_expected=bit)
+    # reference: the oracle without the offending entry
+    ref_in = hw.copy()
+    if bad == "slot":
+        ref_in.dst_slots[0, victim] = ref_in.pad_slot_id
+        ref_in.src_slots[0, victim] = 0
+    else:
+        keep = [a for i, a in enumerate(hw.active) if i != 1]
+        ref_in.active[:] = keep + [-1]
+        if bad != "active":
+            ref_in.replay_prefix_len[victim] = 0
+            ref_in.ring_start[victim] = 0
+    compare_worlds(got, run_oracle(ref_in), ref_in)
+
+
+def test_repeated_calls_are_identical():
+    shape = wl.Shape("rep", L=2, Bt=4, H=8, hpg=4, D=64, N=128, R=8, W=8, state_dtype="fp8_e4m3", n_active=4,
+                     philox_rounds=7, rand_seed=99)
+    hw = wl.host_world(shape, seed=51)
+    a = run_cuda(hw)
+    b = run_cuda(hw)
+    for l in range(hw.L):
+        assert a.state[l].tobytes() == b.state[l].tobytes()
+        assert a.scale[l].tobytes() == b.scale[l].tobytes()
+
+
+# ----------------------------------------------------------------------------
+# full size: the 48-layer x 256-head x 64x128 bf16 call that the benchmark times
+# ----------------------------------------------------------------------------
+
+@pytest.mark.slow
+def test_headline_full_size_sampled():
+    shape = wl.SHAPES["hybrid48_bf16"]
+    dw = wl.device_world_random(shape, seed=0)
+    cfg = rsm.launch_config(**dw.call_kwargs())
+    assert cfg["grid"] > 0
+    rsm.replayssm_materialize(**dw.call_kwargs())
+    torch.cuda.synchronize()
+    assert int(dw.status.item()) == 0
+    active = dw.active.cpu().numpy()
+    prefix = dw.replay_prefix_len.cpu().numpy()
+    src = dw.src_slots.cpu().numpy()
+    dst = dw.dst_slots.cpu().numpy()
+    rng = np.random.default_rng(5)
+    # property at full size: every prefix-0 request is a bit-exact copy in every layer
+    zero = [int(b) for b in active[active >= 0] if prefix[b] == 0]
+    for b in zero[:8]:
+        for l in range(shape.L):
+            assert torch.equal(dw.state[l][dst[l, b]], dw.state[l][src[l, b]])
+    # sampled outputs, each recomputed by the oracle from its own inputs
+    picks = [(int(rng.integers(shape.L)), int(active[int(rng.integers(shape.Bt))])) for _ in range(6)]
+    picks.append((shape.L - 1, int(active[-1])))
+    for l, b in picks:
+        sub = wl.host_subworld(dw, l, b)
+        oracle.materialize(sub)
+        got = wl._to_np(dw.state[l][dst[l, b]])
+        ref = sub.state[0][1]
+        if prefix[b] == 0:
+            assert got.tobytes() == ref.tobytes()
+        else:
+            compare_slot(got, ref, "bf16", where=f"layer {l} request {b}")
+    del dw
+    torch.cuda.empty_cache()
