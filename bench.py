@@ -46,6 +46,7 @@ def parse_args():
     p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     p.add_argument("--workload", default="hybrid48_bf16", choices=sorted(wl.SHAPES))
     p.add_argument("--n-active", type=int, default=None, help="active requests per step (default: the workload's)")
+    p.add_argument("--batch", type=int, default=None, help="batch size (default: the workload's)")
     p.add_argument("--no-extras", action="store_true", help="skip the n sweep, empty latency, e2e and CPU baseline")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work for the oracle baseline sample")
     p.add_argument("--e2e-requests", type=int, default=16)
@@ -327,6 +328,8 @@ def main():
     rsm.load_library()
 
     shape = wl.SHAPES[args.workload]
+    if args.batch is not None:
+        shape = shape.replace(Bt=args.batch, n_active=min(shape.n_active, args.batch))
     if args.n_active is not None:
         shape = shape.replace(n_active=args.n_active)
     # each rank materializes its own batch (weak scaling: independent shards)
@@ -355,10 +358,12 @@ def main():
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist.barrier()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed")
     e0.record(stream)
     for _ in range(args.steps):
         call(stream)
     e1.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     dist.barrier()
     clock_info = clocks.stop()
