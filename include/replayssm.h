@@ -45,7 +45,10 @@
  * when that optional word is given.
  *
  * Aliasing.  Destination slots must be distinct and must not be a source slot
- * read by the same call; otherwise the result is undefined.
+ * that another (layer, request) of the same call reads; otherwise the result
+ * is undefined.  dst_slots[l, b] == src_slots[l, b] is allowed: the prefix is
+ * then committed into the source slot in place (each head tile is read whole
+ * before it is written).
  */
 #ifndef REPLAYSSM_H
 #define REPLAYSSM_H

@@ -339,7 +339,10 @@ static int active_count(const oracle_args *a, int32_t *n_out) {
   return 0;
 }
 
-/* Destination slots must be distinct and must not alias a slot read here. */
+/* Destination slots must be distinct and must not alias a slot that another
+ * (layer, request) reads.  A destination equal to its own source slot is the
+ * in-place case (the prefix committed into the source slot): each head tile is
+ * read completely before it is written, so it is well defined. */
 static int check_aliasing(const oracle_args *a, int32_t n) {
   for (int32_t l = 0; l < a->num_layers; ++l) {
     for (int32_t i = 0; i < n; ++i) {
@@ -353,7 +356,7 @@ static int check_aliasing(const oracle_args *a, int32_t n) {
         int32_t s2 = a->src_slots[(int64_t)l * a->batch + b2];
         int32_t d2 = a->dst_slots[(int64_t)l * a->batch + b2];
         if (s2 == a->pad_slot_id || d2 == a->pad_slot_id) continue;
-        if (d == s2) return fail("destination slot is also a source slot", d);
+        if (d == s2 && q != i) return fail("destination slot is also a source slot", d);
         if (q != i && d == d2) return fail("destination slot repeated", d);
       }
     }
@@ -443,8 +446,8 @@ int oracle_materialize(const oracle_args *a) {
       }
 
       if (k == 0) { /* exact state and scale copy */
-        memcpy(dst_state, src_state, (size_t)(H * tile * esz));
-        if (is_quantized(fmt)) memcpy(dst_scale, src_scale, (size_t)(H * D) * sizeof(float));
+        memmove(dst_state, src_state, (size_t)(H * tile * esz));
+        if (is_quantized(fmt)) memmove(dst_scale, src_scale, (size_t)(H * D) * sizeof(float));
         continue;
       }
 

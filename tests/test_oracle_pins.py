@@ -218,6 +218,25 @@ def test_ring_is_read_from_the_source_slot_only():
     assert run(w2).state[0][dst].tobytes() != ref
 
 
+@pytest.mark.parametrize("sd", ["f32", "bf16", "i8"])
+def test_in_place_equals_out_of_place(sd):
+    """dst == src (the prefix committed into the source slot itself) gives the
+    same bytes as writing a separate slot: every head tile is read whole first."""
+    inp = "f32" if sd == "f32" else "bf16"
+    D, N = (64, 128) if sd in wl.QUANTIZED else (16, 16)
+    w0 = single_request_world(seed=61, state_dtype=sd, input_dtype=inp, D=D, N=N, H=4, hpg=2)
+    w0.replay_prefix_len[0] = 5
+    w0.ring_start[0] = 6
+    out = run(w0)
+    dst = int(w0.dst_slots[0, 0])
+    w1 = w0.copy()
+    w1.dst_slots[0, 0] = 0
+    inplace = run(w1)
+    assert inplace.state[0][0].tobytes() == out.state[0][dst].tobytes()
+    if sd in wl.QUANTIZED:
+        assert inplace.scale[0][0].tobytes() == out.scale[0][dst].tobytes()
+
+
 def test_pad_and_terminator_leave_destinations_untouched():
     """Pads skip a (layer, request); entries after the first -1 are ignored even when >= 0."""
     shape = TINY.replace(L=2, Bt=4, n_active=4, special="", pool=16)

@@ -228,6 +228,17 @@ def test_out_of_range_metadata_is_skipped_and_flagged(bad, bit):
     compare_worlds(got, run_oracle(ref_in), ref_in)
 
 
+@pytest.mark.parametrize("sd", ["f32", "bf16", "fp8_e4m3"])
+def test_in_place_commit(sd):
+    """dst_slots == src_slots: the prefix is committed into the source slots."""
+    shape = wl.Shape("inplace", L=2, Bt=5, H=6, hpg=3, D=64, N=128, R=8, W=8, state_dtype=sd,
+                     input_dtype="f32" if sd == "f32" else "bf16", n_active=4, philox_rounds=3 if sd == "fp8_e4m3" else 0,
+                     rand_seed=5)
+    hw = wl.host_world(shape, seed=71)
+    hw.dst_slots[:] = hw.src_slots
+    assert check(hw) >= 4
+
+
 def test_repeated_calls_are_identical():
     shape = wl.Shape("rep", L=2, Bt=4, H=8, hpg=4, D=64, N=128, R=8, W=8, state_dtype="fp8_e4m3", n_active=4,
                      philox_rounds=7, rand_seed=99)
