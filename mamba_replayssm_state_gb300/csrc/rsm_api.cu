@@ -182,14 +182,15 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
                                         elem_bytes(a->input_dtype), a->max_window);
   // Prefer two CTAs per SM (two loaders in flight) when each still gets >= 3
   // stages; otherwise one CTA per SM with a deeper ring.
-  const int two_cta = di.smem_per_sm / 2 - di.smem_reserved - static_cast<int>(rsm::kStageBase);
-  const int one_cta = di.smem_optin - static_cast<int>(rsm::kStageBase);
+  const int base = static_cast<int>(rsm::stage_base(a->dim, a->dstate, elem_bytes(a->state_dtype)));
+  const int two_cta = di.smem_per_sm / 2 - di.smem_reserved - base;
+  const int one_cta = di.smem_optin - base;
   int stages = two_cta > 0 ? two_cta / static_cast<int>(plan.stage_bytes) : 0;
   if (stages < 3) stages = one_cta / static_cast<int>(plan.stage_bytes);
   if (stages > 8) stages = 8;
   if (stages < 2)
     return fail(RSM_ENOTSUP, "a pipeline stage of %u bytes does not fit twice in shared memory", plan.stage_bytes);
-  const int smem = static_cast<int>(rsm::kStageBase + stages * plan.stage_bytes);
+  const int smem = base + stages * static_cast<int>(plan.stage_bytes);
 
   const void* fn = kInstances[inst].kernel();
   int per_sm = 0;
@@ -238,6 +239,7 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   p.R = a->ring_buffer_len;
   p.pad = a->pad_slot_id;
   p.philox_rounds = a->philox_rounds;
+  p.stage0 = static_cast<uint32_t>(base);
   p.stages = static_cast<uint32_t>(stages);
   p.stage_bytes = plan.stage_bytes;
   p.off_state = plan.off_state;

@@ -226,4 +226,39 @@ __device__ __forceinline__ uint4 pack16_sr(float* v, const uint32_t* words) {
   return pack16_rne<F>(v);  // exact: every value is already representable
 }
 
+// ---------------------------------------------------------------------------
+// the same conversions on float2 pairs (the accumulators of the packed
+// fp32x2 FMA path): element 2u is .x, element 2u+1 is .y
+// ---------------------------------------------------------------------------
+
+template <int F>
+__device__ __forceinline__ void unpack16x2(const uint4 raw, float2* v) {
+  float t[Vec<F>::N];
+  unpack16<F>(raw, t);
+#pragma unroll
+  for (int u = 0; u < Vec<F>::N / 2; ++u) v[u] = make_float2(t[2 * u], t[2 * u + 1]);
+}
+
+template <int F>
+__device__ __forceinline__ uint4 pack16x2_rne(const float2* v) {
+  float t[Vec<F>::N];
+#pragma unroll
+  for (int u = 0; u < Vec<F>::N / 2; ++u) {
+    t[2 * u] = v[u].x;
+    t[2 * u + 1] = v[u].y;
+  }
+  return pack16_rne<F>(t);
+}
+
+template <int F>
+__device__ __forceinline__ uint4 pack16x2_sr(const float2* v, const uint32_t* words) {
+  float t[Vec<F>::N];
+#pragma unroll
+  for (int u = 0; u < Vec<F>::N / 2; ++u) {
+    t[2 * u] = v[u].x;
+    t[2 * u + 1] = v[u].y;
+  }
+  return pack16_sr<F>(t, words);
+}
+
 }  // namespace rsm

@@ -247,7 +247,7 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
         aborted = true;
         break;
       }
-      unsigned char* sb = smem + kStageBase + stage * p.stage_bytes;
+      unsigned char* sb = smem + p.stage0 + stage * p.stage_bytes;
       const uint32_t sba = smem_addr(sb);
       const uint32_t fullb = full0 + 8u * stage;
       ItemDesc* desc = reinterpret_cast<ItemDesc*>(sb);
@@ -349,7 +349,7 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
   // end marker for the consumers
   bool ended = false;
   if (!aborted && mbar_wait(empty0 + 8u * stage, phase ^ 1u, kWaitTimeoutNs)) {
-    if (lane == 0) reinterpret_cast<ItemDesc*>(smem + kStageBase + stage * p.stage_bytes)->flags = kFlagEnd;
+    if (lane == 0) reinterpret_cast<ItemDesc*>(smem + p.stage0 + stage * p.stage_bytes)->flags = kFlagEnd;
     __syncwarp();
     if (lane == 0) mbar_arrive(full0 + 8u * stage);
     ended = true;
@@ -379,24 +379,36 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
   constexpr int ES = Fmt<SF>::bytes;
   constexpr int IE = In<IF>::bytes;
   constexpr bool Q = Fmt<SF>::quant;
-  constexpr int VEC = Vec<SF>::N;          // elements per 16-byte vector
-  constexpr int TC = N / VEC;              // threads across one row
-  constexpr int TR_ALL = kConsumerThreads / TC;
-  constexpr int TR = TR_ALL < D ? TR_ALL : D;  // row groups that hold work
-  constexpr int RPT = D / TR;              // rows per thread
-  static_assert(N % VEC == 0 && TC <= 32 && 32 % TC == 0, "thread layout");
-  static_assert(D % TR == 0, "rows must split evenly");
-  static_assert(!Q || TR_ALL <= D, "one-byte formats need every consumer thread busy");
+  constexpr ThreadLayout TL = thread_layout(D, N, ES);
+  constexpr int VEC = TL.vec, LPR = TL.lpr, CT = TL.ct, SLAB_ROWS = TL.slab_rows, RPT = TL.rpt, COLS = TL.cols;
+  constexpr int V2 = VEC / 2;
+  static_assert(VEC == Vec<SF>::N && VEC % 2 == 0, "vector width");
+  static_assert(TL.tct % LPR == 0 && kConsumerWarps % CT == 0 && D % TL.slabs == 0, "thread layout");
+  static_assert(SLAB_ROWS % TL.rpw == 0 || SLAB_ROWS < TL.rpw, "rows must split evenly");
+  static_assert(!Q || SLAB_ROWS >= TL.rpw, "one-byte formats need every consumer lane busy");
+  static_assert(COLS % 8 == 0, "token-chunk buffer vectors");
+  constexpr int XW = SLAB_ROWS % 4 == 0 ? 4 : (SLAB_ROWS % 2 == 0 ? 2 : 1);  // rows per c-conversion unit
 
   const uint32_t full0 = smem_addr(smem);
   const uint32_t empty0 = full0 + 8u * kMaxStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
   float* wbuf = reinterpret_cast<float*>(smem + kWeightOff) + cw * kWeightStride;
+  // this warp's fp32 token chunk: c[t][r] = w_t * x_t[slab row r] and the B_t
+  // values of its column tile.  B is stored in float4 groups interleaved by
+  // lane: column o of lane column lc sits at t*COLS + (o/4)*LPR*4 + lc*4 + o%4,
+  // so that the eight lanes of a quarter-warp read 128 contiguous bytes.
+  float* cbuf = reinterpret_cast<float*>(smem + kWarpBufOff) + cw * warp_buf_floats(D, N, ES);
+  float* bbuf = cbuf + kTokChunk * SLAB_ROWS;
+  static_assert(VEC % 4 == 0, "B chunk groups");
 
-  const int ct = cw * 32 + lane;
-  const int tc = ct % TC, rg = ct / TC;
-  const bool worker = rg < TR;
-  const int row0 = rg * RPT, col0 = tc * VEC;
+  const int lane_row = lane / LPR, lane_col = lane % LPR;
+  const int slab_row0 = (cw / CT) * SLAB_ROWS;  // first tile row of this warp's slab
+  const int tile_col0 = (cw % CT) * COLS;       // first tile column of this warp's column tile
+  const int rrow = lane_row * RPT;              // this thread's first row inside the slab
+  const int row0 = slab_row0 + rrow;
+  const int ccol = lane_col * VEC;              // this thread's first column inside the column tile
+  const int col0 = tile_col0 + ccol;
+  const bool worker = rrow < SLAB_ROWS;
 
   uint32_t key0 = 0, key1 = 0;
   const bool sr = p.philox_rounds > 0;
@@ -415,7 +427,7 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
       }
       break;
     }
-    const unsigned char* sb = smem + kStageBase + stage * p.stage_bytes;
+    const unsigned char* sb = smem + p.stage0 + stage * p.stage_bytes;
     const ItemDesc* desc = reinterpret_cast<const ItemDesc*>(sb);
     const uint32_t flags = desc->flags;
     if (flags & kFlagEnd) break;
@@ -441,7 +453,7 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
         }
       }
       if constexpr (Q) {
-        for (int r = ct; r < D; r += kConsumerThreads) {
+        for (int r = cw * 32 + lane; r < D; r += kConsumerThreads) {
           const float v = reinterpret_cast<const float*>(sb + p.off_scale)[r];
           if (flags & kFlagScaleAligned) {
             dst_sc[r] = v;
@@ -473,42 +485,101 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
         if (t < k) wbuf[t] = dtv * (excl * carry);
         carry *= __shfl_sync(0xFFFFFFFFu, incl, 0);
       }
-      if (lane == 0) wbuf[kMaxWindow] = carry;
-      __syncwarp();
+      const float P = carry;  // identical in every lane
 
-      // load + dequantize this thread's [RPT, VEC] block of the tile
-      float s[RPT][VEC];
+      // this thread's [RPT rows x VEC columns] of the tile, dequantized, times P
+      float2 acc[RPT][V2];
       if (worker) {
-        const float P = wbuf[kMaxWindow];
+        const float2 P2 = make_float2(P, P);
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
-          const uint4 raw =
-              *reinterpret_cast<const uint4*>(sb + p.off_state + ((row0 + r) * N + col0) * ES);
-          unpack16<SF>(raw, s[r]);
+          const uint4 raw = *reinterpret_cast<const uint4*>(sb + p.off_state + ((row0 + r) * N + col0) * ES);
+          unpack16x2<SF>(raw, acc[r]);
           if constexpr (Q) {
             const float sc = reinterpret_cast<const float*>(sb + p.off_scale)[row0 + r];
+            const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
-            for (int u = 0; u < VEC; ++u) s[r][u] = __fmul_rn(s[r][u], sc);
+            for (int u = 0; u < V2; ++u) acc[r][u] = __fmul2_rn(acc[r][u], sc2);
           }
 #pragma unroll
-          for (int u = 0; u < VEC; ++u) s[r][u] *= P;
+          for (int u = 0; u < V2; ++u) acc[r][u] = __fmul2_rn(acc[r][u], P2);
         }
-        // the whole prefix, one rank-1 update per token
-        const unsigned char* xs = sb + p.off_x;
-        const unsigned char* Bs = sb + p.off_B;
+      }
+      __syncwarp();  // wbuf visible to the whole warp
+
+      // the prefix, kTokChunk tokens at a time: convert this warp's share of
+      // the tokens to fp32 (c = w*x for its rows, B for its columns), then one
+      // rank-1 update per token with packed fp32x2 FMAs
+      const unsigned char* xs = sb + p.off_x;
+      const unsigned char* Bs = sb + p.off_B;
+      for (int t0 = 0; t0 < k; t0 += kTokChunk) {
+        const int tn = min(kTokChunk, k - t0);
+        for (int u = lane; u < tn * (SLAB_ROWS / XW); u += 32) {
+          const int t = u / (SLAB_ROWS / XW), rx = (u % (SLAB_ROWS / XW)) * XW;
+          float xv[XW];
+          load_inputs<IF, XW>(xs + ((t0 + t) * D + slab_row0 + rx) * IE, xv);
+          const float wt = wbuf[t0 + t];
+          float* dst = cbuf + t * SLAB_ROWS + rx;
+          if constexpr (XW == 4) {
+            *reinterpret_cast<float4*>(dst) = make_float4(xv[0] * wt, xv[1] * wt, xv[2] * wt, xv[3] * wt);
+          } else if constexpr (XW == 2) {
+            *reinterpret_cast<float2*>(dst) = make_float2(xv[0] * wt, xv[1] * wt);
+          } else {
+            dst[0] = xv[0] * wt;
+          }
+        }
+        for (int u = lane; u < tn * (COLS / 8); u += 32) {
+          const int t = u / (COLS / 8), j8 = (u % (COLS / 8)) * 8;
+          float bv[8];
+          load_inputs<IF, 8>(Bs + ((t0 + t) * N + tile_col0 + j8) * IE, bv);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int j = j8 + 4 * h, lc = j / VEC, o = j % VEC;  // o is a multiple of 4
+            *reinterpret_cast<float4*>(bbuf + t * COLS + (o / 4) * (LPR * 4) + lc * 4) =
+                make_float4(bv[4 * h], bv[4 * h + 1], bv[4 * h + 2], bv[4 * h + 3]);
+          }
+        }
+        __syncwarp();
+        if (worker) {
 #pragma unroll 2
-        for (int t = 0; t < k; ++t) {
-          const float wt = wbuf[t];
-          float c[RPT], bv[VEC];
-          load_inputs<IF, RPT>(xs + (t * D + row0) * IE, c);
-          load_inputs<IF, VEC>(Bs + (t * N + col0) * IE, bv);
+          for (int t = 0; t < tn; ++t) {
+            float c[RPT];
+            float2 b2[V2];
+            if constexpr (RPT % 4 == 0) {
 #pragma unroll
-          for (int r = 0; r < RPT; ++r) {
-            const float cr = c[r] * wt;
+              for (int r = 0; r < RPT; r += 4) {
+                const float4 v = *reinterpret_cast<const float4*>(cbuf + t * SLAB_ROWS + rrow + r);
+                c[r] = v.x;
+                c[r + 1] = v.y;
+                c[r + 2] = v.z;
+                c[r + 3] = v.w;
+              }
+            } else if constexpr (RPT % 2 == 0) {
 #pragma unroll
-            for (int u = 0; u < VEC; ++u) s[r][u] = fmaf(cr, bv[u], s[r][u]);
+              for (int r = 0; r < RPT; r += 2) {
+                const float2 v = *reinterpret_cast<const float2*>(cbuf + t * SLAB_ROWS + rrow + r);
+                c[r] = v.x;
+                c[r + 1] = v.y;
+              }
+            } else {
+#pragma unroll
+              for (int r = 0; r < RPT; ++r) c[r] = cbuf[t * SLAB_ROWS + rrow + r];
+            }
+#pragma unroll
+            for (int g = 0; g < VEC / 4; ++g) {
+              const float4 v = *reinterpret_cast<const float4*>(bbuf + t * COLS + g * (LPR * 4) + lane_col * 4);
+              b2[2 * g] = make_float2(v.x, v.y);
+              b2[2 * g + 1] = make_float2(v.z, v.w);
+            }
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+              const float2 c2 = make_float2(c[r], c[r]);
+#pragma unroll
+              for (int u = 0; u < V2; ++u) acc[r][u] = __ffma2_rn(c2, b2[u], acc[r][u]);
+            }
           }
         }
+        __syncwarp();  // the chunk buffer is rewritten by the next chunk
       }
 
       // requantize + store
@@ -517,18 +588,19 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
       for (int r = 0; r < RPT; ++r) {
         float scale_out = 0.0f;
         if constexpr (Q) {
-          // symmetric per-(head, row) scale; all threads take part in the shuffles
+          // symmetric per-(head, row) scale; the LPR lanes of a row reduce together
           float amax = 0.0f;
 #pragma unroll
-          for (int u = 0; u < VEC; ++u) amax = fmaxf(amax, fabsf(s[r][u]));
+          for (int u = 0; u < V2; ++u) amax = fmaxf(amax, fmaxf(fabsf(acc[r][u].x), fabsf(acc[r][u].y)));
 #pragma unroll
-          for (int off = TC / 2; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+          for (int off = LPR / 2; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
           constexpr float qmax = SF == RSM_I8 ? 127.0f : 448.0f;
           const float scale = __fdiv_rn(amax, qmax);
           const float inv = __fdiv_rn(qmax, amax);
           const bool zero_row = !(inv <= FLT_MAX);
+          const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-          for (int u = 0; u < VEC; ++u) s[r][u] = zero_row ? 0.0f : __fmul_rn(s[r][u], inv);
+          for (int u = 0; u < V2; ++u) acc[r][u] = zero_row ? make_float2(0.0f, 0.0f) : __fmul2_rn(acc[r][u], inv2);
           scale_out = zero_row ? 0.0f : scale;
         }
         if (!worker) continue;
@@ -539,19 +611,19 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
           uint32_t words[VEC];
           const int64_t e0 = (static_cast<int64_t>(h) * D + row0 + r) * N + col0;
 #pragma unroll
-          for (int q = 0; q < (VEC >= 4 ? VEC / 4 : 1); ++q) {
+          for (int q = 0; q < VEC / 4; ++q) {
             const uint4 rnd = philox4x32(
                 make_uint4(static_cast<uint32_t>((e0 >> 2) + q), static_cast<uint32_t>(desc->dst_slot),
                            static_cast<uint32_t>(desc->layer), 0u),
                 key0, key1, p.philox_rounds);
-            if (4 * q + 0 < VEC) words[4 * q + 0] = rnd.x;
-            if (4 * q + 1 < VEC) words[4 * q + 1] = rnd.y;
-            if (4 * q + 2 < VEC) words[4 * q + 2] = rnd.z;
-            if (4 * q + 3 < VEC) words[4 * q + 3] = rnd.w;
+            words[4 * q + 0] = rnd.x;
+            words[4 * q + 1] = rnd.y;
+            words[4 * q + 2] = rnd.z;
+            words[4 * q + 3] = rnd.w;
           }
-          out = pack16_sr<SF>(s[r], words);
+          out = pack16x2_sr<SF>(acc[r], words);
         } else {
-          out = pack16_rne<SF>(s[r]);
+          out = pack16x2_rne<SF>(acc[r]);
         }
         const uint32_t off = ((row0 + r) * N + col0) * ES;
         if (dst_aligned) {
@@ -562,7 +634,7 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
           for (int q = 0; q < 16; ++q) dst_tile[off + q] = ob[q];
         }
         if constexpr (Q) {
-          if (tc == 0) {
+          if (lane_col == 0) {
             if (flags & kFlagScaleAligned) {
               dst_sc[row0 + r] = scale_out;
             } else {

@@ -17,8 +17,43 @@ constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // 4 s: never reached by a c
 constexpr uint32_t kAbortOff = 2 * 8 * kMaxStages;
 constexpr uint32_t kWeightOff = 512;
 constexpr uint32_t kWeightStride = kMaxWindow + 4;  // floats per consumer warp: w_0..w_63, P
-constexpr uint32_t kStageBase = 3072;
-static_assert(kWeightOff + kConsumerWarps * kWeightStride * 4 <= kStageBase, "smem head overflow");
+constexpr uint32_t kWarpBufOff = 3072;  // per-consumer-warp fp32 token-chunk buffers start here
+static_assert(kWeightOff + kConsumerWarps * kWeightStride * 4 <= kWarpBufOff, "smem head overflow");
+constexpr int kTokChunk = 8;  // tokens converted to fp32 per consumer-warp pass
+
+// How the consumer warps tile a [dim, dstate] state tile.  Each thread owns
+// RPT consecutive rows x VEC consecutive columns (one 16-byte vector per row).
+// Inside a warp, LPR lanes cover one row (LPR*VEC columns), RPW rows side by
+// side; the tile's column span is split into CT column tiles and its rows into
+// SLABS slabs, one (column tile, slab) per warp.
+struct ThreadLayout {
+  int vec, tct, lpr, rpw, ct, slabs, slab_rows, rpt, cols;
+};
+
+__host__ __device__ constexpr ThreadLayout thread_layout(int dim, int dstate, int state_bytes) {
+  const int vec = 16 / state_bytes;
+  const int tct = dstate / vec;
+  const int lpr = tct < 8 ? tct : 8;
+  const int rpw = 32 / lpr;
+  const int ct = tct / lpr;
+  const int slabs = kConsumerWarps / ct;
+  const int slab_rows = dim / slabs;
+  const int rpt = slab_rows >= rpw ? slab_rows / rpw : 1;
+  return ThreadLayout{vec, tct, lpr, rpw, ct, slabs, slab_rows, rpt, lpr * vec};
+}
+
+// fp32 floats in one consumer warp's token-chunk buffer: c = w*x for its
+// slab's rows and B for its column tile, kTokChunk tokens each.
+__host__ __device__ constexpr uint32_t warp_buf_floats(int dim, int dstate, int state_bytes) {
+  return static_cast<uint32_t>(kTokChunk *
+                               (thread_layout(dim, dstate, state_bytes).slab_rows +
+                                thread_layout(dim, dstate, state_bytes).cols));
+}
+
+// Offset of pipeline stage 0: the fixed head plus the consumer warps' buffers.
+__host__ __device__ constexpr uint32_t stage_base(int dim, int dstate, int state_bytes) {
+  return ((kWarpBufOff + kConsumerWarps * warp_buf_floats(dim, dstate, state_bytes) * 4u) + 127u) / 128u * 128u;
+}
 
 struct Params {
   const int64_t* state_ptrs;
@@ -40,8 +75,8 @@ struct Params {
   const int64_t* rand_seed;
   uint32_t* status;
   int32_t L, Bt, H, hpg, W, R, pad, philox_rounds;
-  // shared-memory plan (see make_plan)
-  uint32_t stages, stage_bytes, off_state, off_scale, off_x, off_B, off_dt;
+  // shared-memory plan (see make_plan); stage s starts at stage0 + s*stage_bytes
+  uint32_t stage0, stages, stage_bytes, off_state, off_scale, off_x, off_B, off_dt;
 };
 
 struct Plan {
