@@ -47,6 +47,7 @@ def parse_args():
     p.add_argument("--workload", default="hybrid48_bf16", choices=sorted(wl.SHAPES))
     p.add_argument("--n-active", type=int, default=None, help="active requests per step (default: the workload's)")
     p.add_argument("--batch", type=int, default=None, help="batch size (default: the workload's)")
+    p.add_argument("--prefix", type=int, default=None, help="fixed replay_prefix_len for every request")
     p.add_argument("--no-extras", action="store_true", help="skip the n sweep, empty latency, e2e and CPU baseline")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work for the oracle baseline sample")
     p.add_argument("--e2e-requests", type=int, default=16)
@@ -332,6 +333,8 @@ def main():
         shape = shape.replace(Bt=args.batch, n_active=min(shape.n_active, args.batch))
     if args.n_active is not None:
         shape = shape.replace(n_active=args.n_active)
+    if args.prefix is not None:
+        shape = shape.replace(prefix=("fixed", args.prefix))
     # each rank materializes its own batch (weak scaling: independent shards)
     dw = wl.device_world_random(shape, seed=1000 * rank, device=device)
     active = dw.active.cpu().numpy()

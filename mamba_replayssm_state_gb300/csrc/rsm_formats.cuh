@@ -130,6 +130,16 @@ __device__ __forceinline__ float sr_f16(float y, uint32_t w) { return sr_round<1
 __device__ __forceinline__ float sr_e4m3(float y, uint32_t w) { return sr_round<3, -6, false>(y, w, 448.0f); }
 __device__ __forceinline__ float sr_i8(float y, uint32_t w) { return sr_round<0, 0, true>(y, w, 127.0f); }
 
+// stochastic rounding to the grid of state format F (fp32: identity)
+template <int F>
+__device__ __forceinline__ float sr_fmt(float y, uint32_t w) {
+  if constexpr (F == RSM_BF16) return sr_bf16(y, w);
+  else if constexpr (F == RSM_F16) return sr_f16(y, w);
+  else if constexpr (F == RSM_I8) return sr_i8(y, w);
+  else if constexpr (F == RSM_FP8_E4M3) return sr_e4m3(y, w);
+  else return y;
+}
+
 // ---------------------------------------------------------------------------
 // 16-byte vectors of state elements: VEC = 16 / bytes elements
 // ---------------------------------------------------------------------------
@@ -212,20 +222,6 @@ __device__ __forceinline__ uint4 pack16_rne(const float* v) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// stochastic rounding in place (values become exact grid points), then pack
-template <int F>
-__device__ __forceinline__ uint4 pack16_sr(float* v, const uint32_t* words) {
-  constexpr int n = Vec<F>::N;
-#pragma unroll
-  for (int u = 0; u < n; ++u) {
-    if constexpr (F == RSM_BF16) v[u] = sr_bf16(v[u], words[u]);
-    else if constexpr (F == RSM_F16) v[u] = sr_f16(v[u], words[u]);
-    else if constexpr (F == RSM_I8) v[u] = sr_i8(v[u], words[u]);
-    else if constexpr (F == RSM_FP8_E4M3) v[u] = sr_e4m3(v[u], words[u]);
-  }
-  return pack16_rne<F>(v);  // exact: every value is already representable
-}
-
 // ---------------------------------------------------------------------------
 // the same conversions on float2 pairs (the accumulators of the packed
 // fp32x2 FMA path): element 2u is .x, element 2u+1 is .y
@@ -248,17 +244,6 @@ __device__ __forceinline__ uint4 pack16x2_rne(const float2* v) {
     t[2 * u + 1] = v[u].y;
   }
   return pack16_rne<F>(t);
-}
-
-template <int F>
-__device__ __forceinline__ uint4 pack16x2_sr(const float2* v, const uint32_t* words) {
-  float t[Vec<F>::N];
-#pragma unroll
-  for (int u = 0; u < Vec<F>::N / 2; ++u) {
-    t[2 * u] = v[u].x;
-    t[2 * u + 1] = v[u].y;
-  }
-  return pack16_sr<F>(t, words);
 }
 
 }  // namespace rsm

@@ -241,6 +241,22 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
     const unsigned char* x_slot = x_base + static_cast<int64_t>(src) * x_stride * IE;
     const unsigned char* B_slot = B_base + static_cast<int64_t>(src) * B_stride * IE;
     const float* dt_slot = dt_base + static_cast<int64_t>(src) * dt_stride;
+    const float* src_sc_slot = nullptr;
+    float* dst_sc_slot = nullptr;
+    if constexpr (Q) {
+      src_sc_slot = scale_base + static_cast<int64_t>(src) * scale_stride;
+      dst_sc_slot = scale_base + static_cast<int64_t>(dst) * scale_stride;
+    }
+    // Every tile, row and scale block of the segment starts a whole number of
+    // 16-byte units after its slot base (D*N*ES, D*IE, N*IE and D*4 are
+    // multiples of 16), so alignment is a property of the segment.
+    static_assert((D * IE) % 16 == 0 && (N * IE) % 16 == 0 && (D * 4) % 16 == 0, "row granularity");
+    const bool seg_aligned =
+        ((reinterpret_cast<uintptr_t>(src_slot) | reinterpret_cast<uintptr_t>(x_slot) |
+          reinterpret_cast<uintptr_t>(B_slot) | reinterpret_cast<uintptr_t>(src_sc_slot)) & 15u) == 0u &&
+        ((reinterpret_cast<uintptr_t>(dt_slot) | reinterpret_cast<uintptr_t>(A_base)) & 3u) == 0u;
+    const uint32_t dst_flags = ((reinterpret_cast<uintptr_t>(dst_slot) & 15u) == 0u ? kFlagDstAligned : 0u) |
+                               ((reinterpret_cast<uintptr_t>(dst_sc_slot) & 3u) == 0u ? kFlagScaleAligned : 0u);
 
     for (; w < seg_end; ++w, ++h) {
       if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, kWaitTimeoutNs) || *abort_flag) {
@@ -258,40 +274,18 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
       const float* src_sc = nullptr;
       float* dst_sc = nullptr;
       if constexpr (Q) {
-        src_sc = scale_base + static_cast<int64_t>(src) * scale_stride + static_cast<int64_t>(h) * D;
-        dst_sc = scale_base + static_cast<int64_t>(dst) * scale_stride + static_cast<int64_t>(h) * D;
+        src_sc = src_sc_slot + static_cast<int64_t>(h) * D;
+        dst_sc = dst_sc_slot + static_cast<int64_t>(h) * D;
       }
       const int g = h / p.hpg;
       const float* A_ptr = A_base + h;
-
-      // this lane's tokens: t = lane and t = lane + 32
-      const unsigned char* xrow[2] = {nullptr, nullptr};
-      const unsigned char* brow[2] = {nullptr, nullptr};
-      const float* dtp[2] = {nullptr, nullptr};
-      bool aligned = (reinterpret_cast<uintptr_t>(src_tile) & 15u) == 0u;
-      if constexpr (Q) aligned = aligned && (reinterpret_cast<uintptr_t>(src_sc) & 15u) == 0u;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int t = lane + 32 * q;
-        if (t < k) {
-          const int pr = (rs + t) % p.R;
-          xrow[q] = x_slot + (static_cast<int64_t>(pr) * p.H + h) * D * IE;
-          brow[q] = B_slot + (static_cast<int64_t>(pr) * G + g) * N * IE;
-          dtp[q] = dt_slot + static_cast<int64_t>(pr) * p.H + h;
-          aligned = aligned && (reinterpret_cast<uintptr_t>(xrow[q]) & 15u) == 0u &&
-                    (reinterpret_cast<uintptr_t>(brow[q]) & 15u) == 0u &&
-                    (reinterpret_cast<uintptr_t>(dtp[q]) & 3u) == 0u;
-        }
-      }
-      if (k > 0) aligned = aligned && (reinterpret_cast<uintptr_t>(A_ptr) & 3u) == 0u;
-      aligned = __all_sync(0xFFFFFFFFu, aligned);
+      const bool aligned = seg_aligned;
 
       if (lane == 0) {
         desc->dst_state = reinterpret_cast<unsigned long long>(dst_tile);
         desc->dst_scale = reinterpret_cast<unsigned long long>(dst_sc);
         desc->k = k;
-        desc->flags = ((reinterpret_cast<uintptr_t>(dst_tile) & 15u) == 0u ? kFlagDstAligned : 0u) |
-                      ((reinterpret_cast<uintptr_t>(dst_sc) & 3u) == 0u ? kFlagScaleAligned : 0u);
+        desc->flags = dst_flags;
         desc->layer = l;
         desc->dst_slot = dst;
         desc->head = h;
@@ -307,14 +301,14 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
           if constexpr (Q) bulk_g2s(sba + p.off_scale, src_sc, D * 4u, fullb);
           if (k > 0) cp_async_4(sba + static_cast<uint32_t>(offsetof(ItemDesc, A)), A_ptr);
         }
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int t = lane + 32 * q;
-          if (t < k) {
-            bulk_g2s(sba + p.off_x + static_cast<uint32_t>(t) * D * IE, xrow[q], D * IE, fullb);
-            bulk_g2s(sba + p.off_B + static_cast<uint32_t>(t) * N * IE, brow[q], N * IE, fullb);
-            cp_async_4(sba + p.off_dt + 4u * t, dtp[q]);
-          }
+        // ring rows of this lane's tokens t = lane and t = lane + 32
+        for (int t = lane; t < k; t += 32) {
+          const int pr = (rs + t) % p.R;
+          bulk_g2s(sba + p.off_x + static_cast<uint32_t>(t) * D * IE,
+                   x_slot + (static_cast<int64_t>(pr) * p.H + h) * D * IE, D * IE, fullb);
+          bulk_g2s(sba + p.off_B + static_cast<uint32_t>(t) * N * IE,
+                   B_slot + (static_cast<int64_t>(pr) * G + g) * N * IE, N * IE, fullb);
+          cp_async_4(sba + p.off_dt + 4u * t, dt_slot + static_cast<int64_t>(pr) * p.H + h);
         }
         cp_async_mbar_arrive(fullb);
       } else {
@@ -431,35 +425,57 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
     const ItemDesc* desc = reinterpret_cast<const ItemDesc*>(sb);
     const uint32_t flags = desc->flags;
     if (flags & kFlagEnd) break;
+    // everything the item needs from its descriptor, read before the stage is released
     const int k = desc->k;
     unsigned char* dst_tile = reinterpret_cast<unsigned char*>(desc->dst_state);
     float* dst_sc = reinterpret_cast<float*>(desc->dst_scale);
     const bool dst_aligned = (flags & kFlagDstAligned) != 0u;
+    const int h = desc->head;
+    const uint32_t dst_slot_id = static_cast<uint32_t>(desc->dst_slot);
+    const uint32_t layer_id = static_cast<uint32_t>(desc->layer);
+    // A warp releases the stage as soon as it holds all it still needs (in
+    // registers or in its private chunk buffer), so that the loader refills it
+    // while this warp computes and stores.
+    const uint32_t empty_bar = empty0 + 8u * stage;
+    auto release = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar);
+    };
 
     if (k == 0) {
       // exact copy of the source tile (and scales)
+      uint4 raw[RPT];
+      float scv = 0.0f;
+      if (worker) {
+#pragma unroll
+        for (int r = 0; r < RPT; ++r)
+          raw[r] = *reinterpret_cast<const uint4*>(sb + p.off_state + ((row0 + r) * N + col0) * ES);
+      }
+      const int sr_row = cw * 32 + lane;  // one scale per consumer thread (D <= 256)
+      if constexpr (Q) {
+        if (sr_row < D) scv = reinterpret_cast<const float*>(sb + p.off_scale)[sr_row];
+      }
+      release();
       if (worker) {
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
           const uint32_t off = ((row0 + r) * N + col0) * ES;
-          const uint4 raw = *reinterpret_cast<const uint4*>(sb + p.off_state + off);
           if (dst_aligned) {
-            stg128_stream(dst_tile + off, raw);
+            stg128_stream(dst_tile + off, raw[r]);
           } else {
-            const unsigned char* rb = reinterpret_cast<const unsigned char*>(&raw);
+            const unsigned char* rb = reinterpret_cast<const unsigned char*>(&raw[r]);
 #pragma unroll
             for (int q = 0; q < 16; ++q) dst_tile[off + q] = rb[q];
           }
         }
       }
       if constexpr (Q) {
-        for (int r = cw * 32 + lane; r < D; r += kConsumerThreads) {
-          const float v = reinterpret_cast<const float*>(sb + p.off_scale)[r];
+        if (sr_row < D) {
           if (flags & kFlagScaleAligned) {
-            dst_sc[r] = v;
+            dst_sc[sr_row] = scv;
           } else {
-            const unsigned char* vb = reinterpret_cast<const unsigned char*>(&v);
-            unsigned char* db = reinterpret_cast<unsigned char*>(dst_sc + r);
+            const unsigned char* vb = reinterpret_cast<const unsigned char*>(&scv);
+            unsigned char* db = reinterpret_cast<unsigned char*>(dst_sc + sr_row);
             for (int q = 0; q < 4; ++q) db[q] = vb[q];
           }
         }
@@ -540,6 +556,7 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
           }
         }
         __syncwarp();
+        if (t0 + kTokChunk >= k) release();  // the last chunk: nothing more is read from the stage
         if (worker) {
 #pragma unroll 2
           for (int t = 0; t < tn; ++t) {
@@ -583,7 +600,6 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
       }
 
       // requantize + store
-      const int h = desc->head;
 #pragma unroll
       for (int r = 0; r < RPT; ++r) {
         float scale_out = 0.0f;
@@ -608,20 +624,18 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
         bool use_sr = false;
         if constexpr (SF != RSM_F32) use_sr = sr;
         if (use_sr) {
-          uint32_t words[VEC];
+          // one Philox block per 4 consecutive elements; round, then pack exactly
           const int64_t e0 = (static_cast<int64_t>(h) * D + row0 + r) * N + col0;
 #pragma unroll
           for (int q = 0; q < VEC / 4; ++q) {
             const uint4 rnd = philox4x32(
-                make_uint4(static_cast<uint32_t>((e0 >> 2) + q), static_cast<uint32_t>(desc->dst_slot),
-                           static_cast<uint32_t>(desc->layer), 0u),
-                key0, key1, p.philox_rounds);
-            words[4 * q + 0] = rnd.x;
-            words[4 * q + 1] = rnd.y;
-            words[4 * q + 2] = rnd.z;
-            words[4 * q + 3] = rnd.w;
+                make_uint4(static_cast<uint32_t>((e0 >> 2) + q), dst_slot_id, layer_id, 0u), key0, key1,
+                p.philox_rounds);
+            acc[r][2 * q] = make_float2(sr_fmt<SF>(acc[r][2 * q].x, rnd.x), sr_fmt<SF>(acc[r][2 * q].y, rnd.y));
+            acc[r][2 * q + 1] =
+                make_float2(sr_fmt<SF>(acc[r][2 * q + 1].x, rnd.z), sr_fmt<SF>(acc[r][2 * q + 1].y, rnd.w));
           }
-          out = pack16x2_sr<SF>(acc[r], words);
+          out = pack16x2_rne<SF>(acc[r]);
         } else {
           out = pack16x2_rne<SF>(acc[r]);
         }
@@ -646,8 +660,6 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8u * stage);
     if (++stage == p.stages) {
       stage = 0;
       phase ^= 1u;
