@@ -258,8 +258,24 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
     const uint32_t dst_flags = ((reinterpret_cast<uintptr_t>(dst_slot) & 15u) == 0u ? kFlagDstAligned : 0u) |
                                ((reinterpret_cast<uintptr_t>(dst_sc_slot) & 3u) == 0u ? kFlagScaleAligned : 0u);
 
+    // this lane's ring rows for the whole segment: tokens t = lane and lane + 32
+    // (row p_t = (ring_start + t) mod R, the same for every head of the segment)
+    int64_t x_row[2] = {0, 0}, B_row[2] = {0, 0}, dt_row[2] = {0, 0};
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int t = lane + 32 * q;
+      const int pr = t < k ? (rs + t) % p.R : 0;
+      x_row[q] = static_cast<int64_t>(pr) * p.H * D * IE;
+      B_row[q] = static_cast<int64_t>(pr) * G * N * IE;
+      dt_row[q] = static_cast<int64_t>(pr) * p.H;
+    }
+    int g = h / p.hpg;                     // B group of head h, advanced incrementally
+    int g_left = p.hpg - (h - g * p.hpg);  // heads left in group g, h included
+    const uint4 desc_tail = make_uint4(static_cast<uint32_t>(k), dst_flags, static_cast<uint32_t>(l),
+                                       static_cast<uint32_t>(dst));
+
     for (; w < seg_end; ++w, ++h) {
-      if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, kWaitTimeoutNs) || *abort_flag) {
+      if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, kWaitTimeoutNs)) {
         aborted = true;
         break;
       }
@@ -277,17 +293,16 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
         src_sc = src_sc_slot + static_cast<int64_t>(h) * D;
         dst_sc = dst_sc_slot + static_cast<int64_t>(h) * D;
       }
-      const int g = h / p.hpg;
       const float* A_ptr = A_base + h;
       const bool aligned = seg_aligned;
 
       if (lane == 0) {
-        desc->dst_state = reinterpret_cast<unsigned long long>(dst_tile);
-        desc->dst_scale = reinterpret_cast<unsigned long long>(dst_sc);
-        desc->k = k;
-        desc->flags = dst_flags;
-        desc->layer = l;
-        desc->dst_slot = dst;
+        uint4* d4 = reinterpret_cast<uint4*>(desc);
+        const unsigned long long ds = reinterpret_cast<unsigned long long>(dst_tile);
+        const unsigned long long dc = reinterpret_cast<unsigned long long>(dst_sc);
+        d4[0] = make_uint4(static_cast<uint32_t>(ds), static_cast<uint32_t>(ds >> 32), static_cast<uint32_t>(dc),
+                           static_cast<uint32_t>(dc >> 32));
+        d4[1] = desc_tail;  // k, flags, layer, dst_slot
         desc->head = h;
       }
       if (aligned) {
@@ -302,13 +317,16 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
           if (k > 0) cp_async_4(sba + static_cast<uint32_t>(offsetof(ItemDesc, A)), A_ptr);
         }
         // ring rows of this lane's tokens t = lane and t = lane + 32
-        for (int t = lane; t < k; t += 32) {
-          const int pr = (rs + t) % p.R;
-          bulk_g2s(sba + p.off_x + static_cast<uint32_t>(t) * D * IE,
-                   x_slot + (static_cast<int64_t>(pr) * p.H + h) * D * IE, D * IE, fullb);
-          bulk_g2s(sba + p.off_B + static_cast<uint32_t>(t) * N * IE,
-                   B_slot + (static_cast<int64_t>(pr) * G + g) * N * IE, N * IE, fullb);
-          cp_async_4(sba + p.off_dt + 4u * t, dt_slot + static_cast<int64_t>(pr) * p.H + h);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int t = lane + 32 * q;
+          if (t < k) {
+            bulk_g2s(sba + p.off_x + static_cast<uint32_t>(t) * D * IE,
+                     x_slot + x_row[q] + static_cast<int64_t>(h) * D * IE, D * IE, fullb);
+            bulk_g2s(sba + p.off_B + static_cast<uint32_t>(t) * N * IE,
+                     B_slot + B_row[q] + static_cast<int64_t>(g) * N * IE, N * IE, fullb);
+            cp_async_4(sba + p.off_dt + 4u * t, dt_slot + dt_row[q] + h);
+          }
         }
         cp_async_mbar_arrive(fullb);
       } else {
@@ -332,6 +350,10 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(fullb);
+      if (--g_left == 0) {
+        ++g;
+        g_left = p.hpg;
+      }
       ++fills;
       if (++stage == p.stages) {
         stage = 0;
