@@ -52,6 +52,8 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work for the oracle baseline sample")
     p.add_argument("--e2e-requests", type=int, default=16)
     p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--all-workloads", action="store_true",
+                   help="also measure the other named workloads (added under 'workloads')")
     return p.parse_args()
 
 
@@ -313,6 +315,50 @@ def e2e_measure(torch, rsm, shape, n_req, steps, device):
             "workload": f"{sh.name} with {n_req} active requests, inputs from pinned host memory"}
 
 
+ALU_LANES_PER_SM = 128  # FP32 lanes per SM (Blackwell)
+
+
+def measure_workload(torch, rsm, shape, device, steps, peak_gbs, sms, sm_mhz):
+    """State GB/s, microseconds per active request and roofline fractions of
+    one named workload (its own seeded world, timed with CUDA events)."""
+    import numpy as np
+    dw = wl.device_world_random(shape, seed=5, device=device)
+    active = dw.active.cpu().numpy()
+    prefix = dw.replay_prefix_len.cpu().numpy()
+    src, dst = dw.src_slots.cpu().numpy(), dw.dst_slots.cpu().numpy()
+    state_b, ring_b, n = workload_bytes(shape, active, prefix, src, dst)
+    call = rsm.prepare(**dw.call_kwargs())
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        call(stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    # FP32 lane-FMAs of the replay: one per element per replayed token (+1 for the decay product)
+    nb = int(np.argmax(active == -1)) if (active == -1).any() else len(active)
+    fmas = 0
+    for b in active[:nb]:
+        for l in range(shape.L):
+            if src[l, int(b)] == shape.pad_slot_id or dst[l, int(b)] == shape.pad_slot_id:
+                continue
+            k = int(prefix[int(b)])
+            fmas += shape.H * shape.D * shape.N * (k + 1 if k > 0 else 0)
+    alu_peak = sms * ALU_LANES_PER_SM * sm_mhz * 1e6
+    status = int(dw.status.item())
+    del dw, call
+    torch.cuda.empty_cache()
+    return {"state_dtype": shape.state_dtype, "layers": shape.L, "heads": shape.H, "n_active": n,
+            "prefix": list(shape.prefix), "ms_per_call": ms, "state_gbs": state_b / (ms * 1e-3) / 1e9,
+            "us_per_request": ms * 1e3 / max(n, 1),
+            "hbm_frac": (state_b + ring_b) / (ms * 1e-3) / 1e9 / peak_gbs,
+            "alu_frac": fmas / (ms * 1e-3) / alu_peak, "device_status": status}
+
+
 def main():
     args = parse_args()
     rank, local_rank, world = dist.env()
@@ -451,6 +497,19 @@ def main():
                 out["e2e"] = {"value": None, "error": str(ex)[:200]}
             if world == 1:
                 out["cpu_baseline"] = cpu_baseline_from_device(dw, shape, args.cpu_seconds)
+    if args.all_workloads:
+        del dw, call
+        torch.cuda.empty_cache()
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        mhz = (clock_info or {}).get("sm_mhz") or 2070.0
+        sweep = {}
+        for name in ("mamba2_2p7b_fp32", "hybrid48_int8", "hybrid48_fp8_sr"):
+            sweep[name] = measure_workload(torch, rsm, wl.SHAPES[name], device, 20, peak, sms, mhz)
+        for k in (0, 1, 4, 16, 64):
+            shp = wl.SHAPES["ring_sweep_fp16"].replace(prefix=("fixed", k))
+            sweep[f"ring_sweep_fp16_k{k}"] = measure_workload(torch, rsm, shp, device, 10, peak, sms, mhz)
+        out["workloads"] = sweep
+        out["alu_peak_note"] = f"{sms} SMs x {ALU_LANES_PER_SM} FP32 lanes x {mhz:.0f} MHz lane-FMA/s"
     if rank == 0:
         print(json.dumps(out), flush=True)
     dist.barrier()
