@@ -48,6 +48,8 @@ def parse_args():
     p.add_argument("--n-active", type=int, default=None, help="active requests per step (default: the workload's)")
     p.add_argument("--batch", type=int, default=None, help="batch size (default: the workload's)")
     p.add_argument("--prefix", type=int, default=None, help="fixed replay_prefix_len for every request")
+    p.add_argument("--state-dtype", default=None, choices=sorted(wl.ELEM_SIZE), help="override the state format")
+    p.add_argument("--window", type=int, default=None, help="override max_window (and ring_buffer_len)")
     p.add_argument("--no-extras", action="store_true", help="skip the n sweep, empty latency, e2e and CPU baseline")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work for the oracle baseline sample")
     p.add_argument("--e2e-requests", type=int, default=16)
@@ -381,6 +383,11 @@ def main():
         shape = shape.replace(n_active=args.n_active)
     if args.prefix is not None:
         shape = shape.replace(prefix=("fixed", args.prefix))
+    if args.state_dtype is not None:
+        shape = shape.replace(state_dtype=args.state_dtype)
+    if args.window is not None:
+        shape = shape.replace(W=args.window, R=max(args.window, shape.R),
+                              ring_start=(0, max(args.window, shape.R)))
     # each rank materializes its own batch (weak scaling: independent shards)
     dw = wl.device_world_random(shape, seed=1000 * rank, device=device)
     active = dw.active.cpu().numpy()
@@ -505,6 +512,10 @@ def main():
         sweep = {}
         for name in ("mamba2_2p7b_fp32", "hybrid48_int8", "hybrid48_fp8_sr"):
             sweep[name] = measure_workload(torch, rsm, wl.SHAPES[name], device, 20, peak, sms, mhz)
+        # the fp8 state rounded to nearest even (no Philox), for comparison
+        sweep["hybrid48_fp8_rne"] = measure_workload(
+            torch, rsm, wl.SHAPES["hybrid48_fp8_sr"].replace(name="hybrid48_fp8_rne", philox_rounds=0), device, 20,
+            peak, sms, mhz)
         for k in (0, 1, 4, 16, 64):
             shp = wl.SHAPES["ring_sweep_fp16"].replace(prefix=("fixed", k))
             sweep[f"ring_sweep_fp16_k{k}"] = measure_workload(torch, rsm, shp, device, 10, peak, sms, mhz)

@@ -180,13 +180,13 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   const bool quant = elem_bytes(a->state_dtype) == 1;
   const rsm::Plan plan = rsm::make_plan(a->dim, a->dstate, elem_bytes(a->state_dtype), quant,
                                         elem_bytes(a->input_dtype), a->max_window);
-  // Prefer two CTAs per SM (two loaders in flight) when each still gets >= 3
-  // stages; otherwise one CTA per SM with a deeper ring.
+  // Prefer two CTAs per SM (two loaders in flight) when each still gets >= 4
+  // stages; otherwise one CTA per SM with a deeper ring (long replay windows).
   const int base = static_cast<int>(rsm::stage_base(a->dim, a->dstate, elem_bytes(a->state_dtype)));
   const int two_cta = di.smem_per_sm / 2 - di.smem_reserved - base;
   const int one_cta = di.smem_optin - base;
   int stages = two_cta > 0 ? two_cta / static_cast<int>(plan.stage_bytes) : 0;
-  if (stages < 3) stages = one_cta / static_cast<int>(plan.stage_bytes);
+  if (stages < 4) stages = one_cta / static_cast<int>(plan.stage_bytes);
   if (stages > 8) stages = 8;
   if (stages < 2)
     return fail(RSM_ENOTSUP, "a pipeline stage of %u bytes does not fit twice in shared memory", plan.stage_bytes);

@@ -11,6 +11,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "../../include/replayssm.h"
 
@@ -75,9 +76,11 @@ __device__ __forceinline__ uint4 philox4x32(uint4 c, uint32_t k0, uint32_t k1, i
       k0 += kWeylA;
       k1 += kWeylB;
     }
-    const uint32_t hiA = __umulhi(kMulA, c.x), loA = kMulA * c.x;
-    const uint32_t hiB = __umulhi(kMulB, c.z), loB = kMulB * c.z;
-    c = make_uint4(hiB ^ c.y ^ k0, loB, hiA ^ c.w ^ k1, loA);
+    // one 32x32 -> 64-bit multiply gives both halves of each product
+    const uint64_t pA = static_cast<uint64_t>(kMulA) * c.x;
+    const uint64_t pB = static_cast<uint64_t>(kMulB) * c.z;
+    c = make_uint4(static_cast<uint32_t>(pB >> 32) ^ c.y ^ k0, static_cast<uint32_t>(pB),
+                   static_cast<uint32_t>(pA >> 32) ^ c.w ^ k1, static_cast<uint32_t>(pA));
   }
   return c;
 }
@@ -141,43 +144,66 @@ __device__ __forceinline__ float sr_fmt(float y, uint32_t w) {
 }
 
 // ---------------------------------------------------------------------------
-// 16-byte vectors of state elements: VEC = 16 / bytes elements
+// vectors of state elements: a thread moves one vector per tile row, 16 bytes
+// for 4- and 2-byte formats and 8 bytes (8 codes) for one-byte formats
 // ---------------------------------------------------------------------------
 
 template <int F>
 struct Vec {
-  static constexpr int N = 16 / Fmt<F>::bytes;
+  static constexpr int N = Fmt<F>::bytes == 1 ? 8 : 16 / Fmt<F>::bytes;  // elements
+  static constexpr int BYTES = N * Fmt<F>::bytes;
+  static constexpr int WORDS = BYTES / 4;
+  using Raw = typename std::conditional<BYTES == 16, uint4, uint2>::type;
 };
 
-// raw 16 bytes -> fp32 values (one-byte formats: codes only; the caller scales)
 template <int F>
-__device__ __forceinline__ void unpack16(const uint4 raw, float* v) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+__device__ __forceinline__ void raw_words(const typename Vec<F>::Raw& r, uint32_t* w) {
+  if constexpr (Vec<F>::BYTES == 16) {
+    w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
+  } else {
+    w[0] = r.x; w[1] = r.y;
+  }
+}
+
+template <int F>
+__device__ __forceinline__ typename Vec<F>::Raw words_raw(const uint32_t* w) {
+  if constexpr (Vec<F>::BYTES == 16) return make_uint4(w[0], w[1], w[2], w[3]);
+  else return make_uint2(w[0], w[1]);
+}
+
+// raw words -> fp32 values (one-byte formats: codes only; the caller scales)
+template <int F, int NW>
+__device__ __forceinline__ void unpack_words(const uint32_t* w, float* v) {
   if constexpr (F == RSM_F32) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) v[q] = __uint_as_float(w[q]);
+    for (int q = 0; q < NW; ++q) v[q] = __uint_as_float(w[q]);
   } else if constexpr (F == RSM_BF16) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < NW; ++q) {
       v[2 * q] = bf16lo(w[q]);
       v[2 * q + 1] = bf16hi(w[q]);
     }
   } else if constexpr (F == RSM_F16) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < NW; ++q) {
       const float2 f = f16x2_to_f32(w[q]);
       v[2 * q] = f.x;
       v[2 * q + 1] = f.y;
     }
   } else if constexpr (F == RSM_I8) {
+    // int8 -> fp32 exactly on the integer pipes: flip the sign bit so that each
+    // byte holds code + 128, place it in the mantissa of 2^23 (0x4B0000xx) and
+    // subtract 2^23 + 128.
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < NW; ++q) {
+      const uint32_t u = w[q] ^ 0x80808080u;
 #pragma unroll
-      for (int b = 0; b < 4; ++b) v[4 * q + b] = static_cast<float>(static_cast<int8_t>((w[q] >> (8 * b)) & 0xFF));
+      for (int b = 0; b < 4; ++b)
+        v[4 * q + b] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540u + b)) - 8388736.0f;
     }
   } else {  // FP8 e4m3
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < NW; ++q) {
       const float2 a = e4m3x2_to_f32(w[q] & 0xFFFFu);
       const float2 b = e4m3x2_to_f32(w[q] >> 16);
       v[4 * q + 0] = a.x;
@@ -189,61 +215,59 @@ __device__ __forceinline__ void unpack16(const uint4 raw, float* v) {
 }
 
 // fp32 values (already scaled into code units for one-byte formats) -> raw
-// 16 bytes, round to nearest even (saturating for one-byte formats)
-template <int F>
-__device__ __forceinline__ uint4 pack16_rne(const float* v) {
-  uint32_t w[4];
+// words, round to nearest even (saturating for one-byte formats)
+template <int F, int NW>
+__device__ __forceinline__ void pack_words_rne(const float* v, uint32_t* w) {
   if constexpr (F == RSM_F32) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) w[q] = __float_as_uint(v[q]);
+    for (int q = 0; q < NW; ++q) w[q] = __float_as_uint(v[q]);
   } else if constexpr (F == RSM_BF16) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) w[q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
+    for (int q = 0; q < NW; ++q) w[q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
   } else if constexpr (F == RSM_F16) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) w[q] = pack_f16x2(v[2 * q], v[2 * q + 1]);
+    for (int q = 0; q < NW; ++q) w[q] = pack_f16x2(v[2 * q], v[2 * q + 1]);
   } else if constexpr (F == RSM_I8) {
+    // round to nearest even by adding 1.5 * 2^23: the sum's low byte is the
+    // two's-complement code.  No clamp is needed: |v| <= amax, so
+    // |v * fl(127/amax)| < 127.5 and the code lies in [-127, 127].
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t acc = 0;
+    for (int q = 0; q < NW; ++q) {
+      uint32_t r[4];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        int c = __float2int_rn(v[4 * q + b]);
-        c = c > 127 ? 127 : (c < -127 ? -127 : c);
-        acc |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * b);
-      }
-      w[q] = acc;
+      for (int b = 0; b < 4; ++b) r[b] = __float_as_uint(v[4 * q + b] + 12582912.0f);
+      w[q] = __byte_perm(__byte_perm(r[0], r[1], 0x0040u), __byte_perm(r[2], r[3], 0x0040u), 0x5410u);
     }
   } else {
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
+    for (int q = 0; q < NW; ++q)
       w[q] = f32x2_to_e4m3x2(v[4 * q], v[4 * q + 1]) | (f32x2_to_e4m3x2(v[4 * q + 2], v[4 * q + 3]) << 16);
   }
-  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// ---------------------------------------------------------------------------
-// the same conversions on float2 pairs (the accumulators of the packed
-// fp32x2 FMA path): element 2u is .x, element 2u+1 is .y
-// ---------------------------------------------------------------------------
-
+// one vector <-> float2 pairs (the accumulators of the packed fp32x2 FMA path):
+// element 2u is .x, element 2u+1 is .y
 template <int F>
-__device__ __forceinline__ void unpack16x2(const uint4 raw, float2* v) {
+__device__ __forceinline__ void unpack_vec(const typename Vec<F>::Raw raw, float2* v) {
+  uint32_t w[Vec<F>::WORDS];
+  raw_words<F>(raw, w);
   float t[Vec<F>::N];
-  unpack16<F>(raw, t);
+  unpack_words<F, Vec<F>::WORDS>(w, t);
 #pragma unroll
   for (int u = 0; u < Vec<F>::N / 2; ++u) v[u] = make_float2(t[2 * u], t[2 * u + 1]);
 }
 
 template <int F>
-__device__ __forceinline__ uint4 pack16x2_rne(const float2* v) {
+__device__ __forceinline__ typename Vec<F>::Raw pack_vec_rne(const float2* v) {
   float t[Vec<F>::N];
 #pragma unroll
   for (int u = 0; u < Vec<F>::N / 2; ++u) {
     t[2 * u] = v[u].x;
     t[2 * u + 1] = v[u].y;
   }
-  return pack16_rne<F>(t);
+  uint32_t w[Vec<F>::WORDS];
+  pack_words_rne<F, Vec<F>::WORDS>(t, w);
+  return words_raw<F>(w);
 }
 
 }  // namespace rsm

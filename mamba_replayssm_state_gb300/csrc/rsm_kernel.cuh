@@ -3,9 +3,10 @@
 // persistent work-queue design of FlashInfer PR #4815, Description).
 //
 // Work item = (active request i, layer l, head h): one [dim, dstate] state tile.
-// Items are numbered request-major -> layer -> head and every CTA takes one
-// contiguous range of them, so consecutive items of a CTA share their
-// (request, layer) metadata and stream through contiguous state memory.
+// Items are numbered request-major -> layer -> head; runs of up to 32 heads of
+// one (request, layer) form units dealt to the CTAs round-robin, so that every
+// CTA gets a mix of requests (and of replay lengths) while the items of a unit
+// share their metadata and stream through contiguous state memory.
 //
 // One CTA = 1 loader warp + 8 consumer warps, joined by an S-stage ring in
 // shared memory:
@@ -151,23 +152,30 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
     }
   }
 
-  const int64_t LH = static_cast<int64_t>(p.L) * p.H;
-  const int64_t total = static_cast<int64_t>(n) * LH;
-  const int64_t w_begin = total * blockIdx.x / gridDim.x;
-  const int64_t w_end = total * (blockIdx.x + 1) / gridDim.x;
+  // Work units: (request i, layer l, a run of `chunk` consecutive heads), in
+  // request -> layer -> head order, dealt to the CTAs round-robin.  Each CTA
+  // thus sees every part of the batch (replay lengths differ per request, so
+  // contiguous ranges would leave the CTAs of long-prefix requests last),
+  // while a unit still shares one metadata lookup and a run of B rows.
+  // Smaller batches get shorter runs so that every CTA still has ~16 units.
+  const int64_t total = static_cast<int64_t>(n) * p.L * p.H;
+  int chunk = static_cast<int>(min(static_cast<int64_t>(32),
+                                   max(static_cast<int64_t>(4), total / (16 * static_cast<int64_t>(gridDim.x)))));
+  if (chunk > p.H) chunk = p.H;
+  const int units_per_seg = (p.H + chunk - 1) / chunk;
+  const int64_t total_units = static_cast<int64_t>(n) * p.L * units_per_seg;
   const int G = p.H / p.hpg;
   const uint64_t policy = l2_policy_evict_first();
 
   uint32_t stage = 0, phase = 0, fills = 0;
   bool aborted = false;
   int cur_i = -1, b = 0;
-  int64_t w = w_begin;
-  while (w < w_end && !aborted) {
-    const int i = static_cast<int>(w / LH);
-    const int64_t rem = w - static_cast<int64_t>(i) * LH;
-    const int l = static_cast<int>(rem / p.H);
-    int h = static_cast<int>(rem - static_cast<int64_t>(l) * p.H);
-    const int64_t seg_end = min(w_end, (static_cast<int64_t>(i) * p.L + l + 1) * p.H);
+  for (int64_t u = blockIdx.x; u < total_units && !aborted; u += gridDim.x) {
+    const int64_t seg = u / units_per_seg;
+    const int i = static_cast<int>(seg / p.L);
+    const int l = static_cast<int>(seg - static_cast<int64_t>(i) * p.L);
+    int h = static_cast<int>(u - seg * units_per_seg) * chunk;
+    const int h_end = min(p.H, h + chunk);
 
     // per-layer table entries, one per lane, fetched together
     int64_t tab = 0;
@@ -220,10 +228,7 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
       }
     }
     if (lane == 0) flag_status(p.status, bad);
-    if (!ok) {
-      w = seg_end;
-      continue;
-    }
+    if (!ok) continue;
     const unsigned char* state_base = reinterpret_cast<const unsigned char*>(__shfl_sync(0xFFFFFFFFu, tab, 0));
     const int64_t state_stride = __shfl_sync(0xFFFFFFFFu, tab, 1);
     const unsigned char* x_base = reinterpret_cast<const unsigned char*>(__shfl_sync(0xFFFFFFFFu, tab, 2));
@@ -274,7 +279,7 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
     const uint4 desc_tail = make_uint4(static_cast<uint32_t>(k), dst_flags, static_cast<uint32_t>(l),
                                        static_cast<uint32_t>(dst));
 
-    for (; w < seg_end; ++w, ++h) {
+    for (; h < h_end; ++h) {
       if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, kWaitTimeoutNs)) {
         aborted = true;
         break;
@@ -399,6 +404,8 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
   constexpr int VEC = TL.vec, LPR = TL.lpr, CT = TL.ct, SLAB_ROWS = TL.slab_rows, RPT = TL.rpt, COLS = TL.cols;
   constexpr int V2 = VEC / 2;
   static_assert(VEC == Vec<SF>::N && VEC % 2 == 0, "vector width");
+  using Raw = typename Vec<SF>::Raw;
+  constexpr int VB = Vec<SF>::BYTES;  // bytes per vector
   static_assert(TL.tct % LPR == 0 && kConsumerWarps % CT == 0 && D % TL.slabs == 0, "thread layout");
   static_assert(SLAB_ROWS % TL.rpw == 0 || SLAB_ROWS < TL.rpw, "rows must split evenly");
   static_assert(!Q || SLAB_ROWS >= TL.rpw, "one-byte formats need every consumer lane busy");
@@ -466,12 +473,12 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
 
     if (k == 0) {
       // exact copy of the source tile (and scales)
-      uint4 raw[RPT];
+      Raw raw[RPT];
       float scv = 0.0f;
       if (worker) {
 #pragma unroll
         for (int r = 0; r < RPT; ++r)
-          raw[r] = *reinterpret_cast<const uint4*>(sb + p.off_state + ((row0 + r) * N + col0) * ES);
+          raw[r] = *reinterpret_cast<const Raw*>(sb + p.off_state + ((row0 + r) * N + col0) * ES);
       }
       const int sr_row = cw * 32 + lane;  // one scale per consumer thread (D <= 256)
       if constexpr (Q) {
@@ -483,11 +490,11 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
         for (int r = 0; r < RPT; ++r) {
           const uint32_t off = ((row0 + r) * N + col0) * ES;
           if (dst_aligned) {
-            stg128_stream(dst_tile + off, raw[r]);
+            stg_stream(dst_tile + off, raw[r]);
           } else {
             const unsigned char* rb = reinterpret_cast<const unsigned char*>(&raw[r]);
 #pragma unroll
-            for (int q = 0; q < 16; ++q) dst_tile[off + q] = rb[q];
+            for (int q = 0; q < VB; ++q) dst_tile[off + q] = rb[q];
           }
         }
       }
@@ -531,16 +538,18 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
         const float2 P2 = make_float2(P, P);
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(sb + p.off_state + ((row0 + r) * N + col0) * ES);
-          unpack16x2<SF>(raw, acc[r]);
+          const Raw raw = *reinterpret_cast<const Raw*>(sb + p.off_state + ((row0 + r) * N + col0) * ES);
+          unpack_vec<SF>(raw, acc[r]);
           if constexpr (Q) {
-            const float sc = reinterpret_cast<const float*>(sb + p.off_scale)[row0 + r];
-            const float2 sc2 = make_float2(sc, sc);
+            // code * (scale * P): the row's scale folded into the decay product
+            const float sp = reinterpret_cast<const float*>(sb + p.off_scale)[row0 + r] * P;
+            const float2 sp2 = make_float2(sp, sp);
 #pragma unroll
-            for (int u = 0; u < V2; ++u) acc[r][u] = __fmul2_rn(acc[r][u], sc2);
+            for (int u = 0; u < V2; ++u) acc[r][u] = __fmul2_rn(acc[r][u], sp2);
+          } else {
+#pragma unroll
+            for (int u = 0; u < V2; ++u) acc[r][u] = __fmul2_rn(acc[r][u], P2);
           }
-#pragma unroll
-          for (int u = 0; u < V2; ++u) acc[r][u] = __fmul2_rn(acc[r][u], P2);
         }
       }
       __syncwarp();  // wbuf visible to the whole warp
@@ -622,27 +631,45 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
       }
 
       // requantize + store
+      float scale_own = 0.0f;  // one-byte formats: the scale of row row0 + lane_col (lanes lane_col < RPT)
+      if constexpr (Q) {
+        // symmetric per-(head, row) scale: amax by a butterfly over the LPR lanes
+        // of each row; then each row's scale and inverse are divided once, by
+        // the row's lane lane_col == r, and the inverse is shuffled to the rest
+        static_assert(RPT <= LPR, "one lane per row for the scale division");
+        float amax[RPT];
 #pragma unroll
-      for (int r = 0; r < RPT; ++r) {
-        float scale_out = 0.0f;
-        if constexpr (Q) {
-          // symmetric per-(head, row) scale; the LPR lanes of a row reduce together
-          float amax = 0.0f;
+        for (int r = 0; r < RPT; ++r) {
+          amax[r] = 0.0f;
 #pragma unroll
-          for (int u = 0; u < V2; ++u) amax = fmaxf(amax, fmaxf(fabsf(acc[r][u].x), fabsf(acc[r][u].y)));
+          for (int u = 0; u < V2; ++u) amax[r] = fmaxf(amax[r], fmaxf(fabsf(acc[r][u].x), fabsf(acc[r][u].y)));
+        }
 #pragma unroll
-          for (int off = LPR / 2; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-          constexpr float qmax = SF == RSM_I8 ? 127.0f : 448.0f;
-          const float scale = __fdiv_rn(amax, qmax);
-          const float inv = __fdiv_rn(qmax, amax);
+        for (int off = LPR / 2; off >= 1; off >>= 1) {
+#pragma unroll
+          for (int r = 0; r < RPT; ++r) amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xFFFFFFFFu, amax[r], off));
+        }
+        float am = amax[0];
+#pragma unroll
+        for (int r = 1; r < RPT; ++r) am = lane_col == r ? amax[r] : am;
+        constexpr float qmax = SF == RSM_I8 ? 127.0f : 448.0f;
+        const float inv_own = __fdiv_rn(qmax, am);
+        scale_own = inv_own <= FLT_MAX ? __fdiv_rn(am, qmax) : 0.0f;
+        const int row_lane0 = lane & ~(LPR - 1);
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+          const float inv = __shfl_sync(0xFFFFFFFFu, inv_own, row_lane0 + r);
+          // a row whose qmax/amax is not finite (amax == 0 or tiny) becomes zero codes
           const bool zero_row = !(inv <= FLT_MAX);
           const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
           for (int u = 0; u < V2; ++u) acc[r][u] = zero_row ? make_float2(0.0f, 0.0f) : __fmul2_rn(acc[r][u], inv2);
-          scale_out = zero_row ? 0.0f : scale;
         }
+      }
+#pragma unroll
+      for (int r = 0; r < RPT; ++r) {
         if (!worker) continue;
-        uint4 out;
+        Raw out;
         bool use_sr = false;
         if constexpr (SF != RSM_F32) use_sr = sr;
         if (use_sr) {
@@ -657,27 +684,27 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
             acc[r][2 * q + 1] =
                 make_float2(sr_fmt<SF>(acc[r][2 * q + 1].x, rnd.z), sr_fmt<SF>(acc[r][2 * q + 1].y, rnd.w));
           }
-          out = pack16x2_rne<SF>(acc[r]);
+          out = pack_vec_rne<SF>(acc[r]);
         } else {
-          out = pack16x2_rne<SF>(acc[r]);
+          out = pack_vec_rne<SF>(acc[r]);
         }
         const uint32_t off = ((row0 + r) * N + col0) * ES;
         if (dst_aligned) {
-          stg128_stream(dst_tile + off, out);
+          stg_stream(dst_tile + off, out);
         } else {
           const unsigned char* ob = reinterpret_cast<const unsigned char*>(&out);
 #pragma unroll
-          for (int q = 0; q < 16; ++q) dst_tile[off + q] = ob[q];
+          for (int q = 0; q < VB; ++q) dst_tile[off + q] = ob[q];
         }
-        if constexpr (Q) {
-          if (lane_col == 0) {
-            if (flags & kFlagScaleAligned) {
-              dst_sc[row0 + r] = scale_out;
-            } else {
-              const unsigned char* vb = reinterpret_cast<const unsigned char*>(&scale_out);
-              unsigned char* db = reinterpret_cast<unsigned char*>(dst_sc + row0 + r);
-              for (int q = 0; q < 4; ++q) db[q] = vb[q];
-            }
+      }
+      if constexpr (Q) {
+        if (lane_col < RPT) {
+          if (flags & kFlagScaleAligned) {
+            dst_sc[row0 + lane_col] = scale_own;
+          } else {
+            const unsigned char* vb = reinterpret_cast<const unsigned char*>(&scale_own);
+            unsigned char* db = reinterpret_cast<unsigned char*>(dst_sc + row0 + lane_col);
+            for (int q = 0; q < 4; ++q) db[q] = vb[q];
           }
         }
       }

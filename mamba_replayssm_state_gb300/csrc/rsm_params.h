@@ -22,7 +22,7 @@ static_assert(kWeightOff + kConsumerWarps * kWeightStride * 4 <= kWarpBufOff, "s
 constexpr int kTokChunk = 8;  // tokens converted to fp32 per consumer-warp pass
 
 // How the consumer warps tile a [dim, dstate] state tile.  Each thread owns
-// RPT consecutive rows x VEC consecutive columns (one 16-byte vector per row).
+// RPT consecutive rows x VEC consecutive columns (one vector per row).
 // Inside a warp, LPR lanes cover one row (LPR*VEC columns), RPW rows side by
 // side; the tile's column span is split into CT column tiles and its rows into
 // SLABS slabs, one (column tile, slab) per warp.
@@ -31,9 +31,11 @@ struct ThreadLayout {
 };
 
 __host__ __device__ constexpr ThreadLayout thread_layout(int dim, int dstate, int state_bytes) {
-  const int vec = 16 / state_bytes;
+  // 16-byte vectors, except one-byte formats: 8 codes (8 bytes), with a whole
+  // row inside one warp so that the row's amax is a warp reduction
+  const int vec = state_bytes == 1 ? 8 : 16 / state_bytes;
   const int tct = dstate / vec;
-  const int lpr = tct < 8 ? tct : 8;
+  const int lpr = state_bytes == 1 ? tct : (tct < 8 ? tct : 8);
   const int rpw = 32 / lpr;
   const int ct = tct / lpr;
   const int slabs = kConsumerWarps / ct;

@@ -118,4 +118,11 @@ __device__ __forceinline__ void stg128_stream(void* p, uint4 v) {
                : "memory");
 }
 
+__device__ __forceinline__ void stg64_stream(void* p, uint2 v) {
+  asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void stg_stream(void* p, uint4 v) { stg128_stream(p, v); }
+__device__ __forceinline__ void stg_stream(void* p, uint2 v) { stg64_stream(p, v); }
+
 }  // namespace rsm
