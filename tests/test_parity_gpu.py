@@ -115,6 +115,26 @@ def test_every_instance(sd, idt, D, N):
     check(hw)
 
 
+@pytest.mark.parametrize("sd,idt,D,N", WIDE + BYTE, ids=lambda v: str(v))
+def test_every_instance_long_window(sd, idt, D, N):
+    """A 40-token window: prefixes of up to 40 ring rows span up to three
+    pipeline stages of 16 tokens, the last one ragged, with ring wrap."""
+    shape = wl.Shape("instw", L=2, Bt=6, H=6, hpg=3, D=D, N=N, R=48, W=40, state_dtype=sd, input_dtype=idt,
+                     n_active=5, ring_start=(0, 48), prefix=("uniform", 0, 40))
+    hw = wl.host_world(shape, seed=zlib.crc32(repr(("w", sd, idt, D, N)).encode()) % 1000)
+    hw.replay_prefix_len[int(hw.active[0])] = 40
+    hw.replay_prefix_len[int(hw.active[1])] = 17
+    check(hw)
+
+
+@pytest.mark.parametrize("sd", ["bf16", "i8"])
+def test_stochastic_rounding_long_window(sd):
+    shape = wl.Shape("srw", L=2, Bt=4, H=4, hpg=2, D=64, N=128, R=64, W=64, state_dtype=sd, n_active=4,
+                     ring_start=(0, 64), prefix=("uniform", 17, 64), philox_rounds=10, rand_seed=0xABCDEF)
+    hw = wl.host_world(shape, seed=8)
+    check(hw)
+
+
 @pytest.mark.parametrize("sd", ["bf16", "f16", "i8", "fp8_e4m3"])
 def test_stochastic_rounding_every_format(sd):
     shape = wl.Shape("sr", L=2, Bt=4, H=4, hpg=2, D=64, N=128, R=8, W=8, state_dtype=sd, n_active=4,
@@ -166,6 +186,26 @@ def test_misaligned_state_and_ring_take_the_byte_path():
     dw.x[1] = xv
     dw.tables = wl._tables(dw.state, dw.scale, dw.x, dw.B, dw.dt, dw.A, "cuda")
     assert dw.state[0].data_ptr() % 16 == 2
+    rsm.replayssm_materialize(**dw.call_kwargs())
+    torch.cuda.synchronize()
+    got = hw.copy()
+    got.state = [wl._to_np(t).view(a.dtype) for t, a in zip(dw.state, hw.state)]
+    compare_worlds(got, run_oracle(hw), hw)
+
+
+def test_misaligned_ring_long_window():
+    """Byte-copy path over several stages: misaligned B rows, prefixes up to 48."""
+    shape = wl.Shape("misw", L=1, Bt=4, H=4, hpg=2, D=64, N=128, R=64, W=48, state_dtype="f16", n_active=4,
+                     ring_start=(0, 64), prefix=("uniform", 10, 48))
+    hw = wl.host_world(shape, seed=23)
+    hw.B[0] = _offset_copy(hw.B[0], 1)
+    dw = wl.device_world_from_host(hw)
+    buf = torch.zeros(hw.B[0].size + 1, dtype=torch.int16, device="cuda")
+    bv = buf[1:].view(hw.B[0].shape)
+    bv.copy_(torch.from_numpy(hw.B[0].view(np.int16).copy()))
+    dw.B[0] = bv
+    dw.tables = wl._tables(dw.state, dw.scale, dw.x, dw.B, dw.dt, dw.A, "cuda")
+    assert dw.B[0].data_ptr() % 16 == 2
     rsm.replayssm_materialize(**dw.call_kwargs())
     torch.cuda.synchronize()
     got = hw.copy()
