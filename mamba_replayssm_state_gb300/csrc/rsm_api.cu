@@ -167,6 +167,9 @@ struct Launch {
   rsm::Params params;
 };
 
+constexpr int kSlotsPerSm = 6;  // pipeline slots per SM, over its CTAs
+static_assert(kSlotsPerSm <= rsm::kMaxStages, "slot count");
+
 int plan_launch(const rsm_materialize_args* a, Launch* L) {
   const int inst = validate(a);
   if (inst < 0) return inst;
@@ -178,19 +181,26 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   if (rc != RSM_OK) return rc;
 
   const bool quant = elem_bytes(a->state_dtype) == 1;
-  const rsm::Plan plan = rsm::make_plan(a->dim, a->dstate, elem_bytes(a->state_dtype), quant,
-                                        elem_bytes(a->input_dtype), a->max_window);
-  // Prefer two CTAs per SM (two loaders in flight) when each still gets >= 4
-  // stages; otherwise one CTA per SM with a deeper ring (long replay windows).
-  const int base = static_cast<int>(rsm::stage_base(a->dim, a->dstate, elem_bytes(a->state_dtype)));
+  // Items are packed into a byte arena, each taking its tile (+ scales) and
+  // only its own k ring rows.  Two CTAs per SM (two loaders in flight) when
+  // each arena still holds two items of the longest window; otherwise one CTA
+  // per SM with the whole shared memory.
+  const int sb = elem_bytes(a->state_dtype), ib = elem_bytes(a->input_dtype);
+  const int item_min = static_cast<int>(rsm::item_layout(a->dim, a->dstate, sb, quant, ib, 0).bytes);
+  const int item_max = static_cast<int>(rsm::item_layout(a->dim, a->dstate, sb, quant, ib, a->max_window).bytes);
+  const int base = static_cast<int>(rsm::arena_base(a->dim, a->dstate, sb));
   const int two_cta = di.smem_per_sm / 2 - di.smem_reserved - base;
   const int one_cta = di.smem_optin - base;
-  int stages = two_cta > 0 ? two_cta / static_cast<int>(plan.stage_bytes) : 0;
-  if (stages < 4) stages = one_cta / static_cast<int>(plan.stage_bytes);
-  if (stages > 8) stages = 8;
-  if (stages < 2)
-    return fail(RSM_ENOTSUP, "a pipeline stage of %u bytes does not fit twice in shared memory", plan.stage_bytes);
-  const int smem = base + stages * static_cast<int>(plan.stage_bytes);
+  const bool two = two_cta >= 2 * item_max;
+  const int arena = (two ? two_cta : one_cta) / 128 * 128;
+  if (arena < 2 * item_max)
+    return fail(RSM_ENOTSUP, "two work items of %d bytes do not fit in shared memory", item_max);
+  // Six items in flight per SM (three per CTA at two CTAs per SM): measured
+  // on GB300 against two and four per CTA, it is the fastest with replay at
+  // every window length (four per CTA is 2% slower on the 48-layer bf16 shape).
+  int stages = arena / item_min;
+  if (stages > kSlotsPerSm / (two ? 2 : 1)) stages = kSlotsPerSm / (two ? 2 : 1);
+  const int smem = base + arena;
 
   const void* fn = kInstances[inst].kernel();
   int per_sm = 0;
@@ -239,14 +249,10 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   p.R = a->ring_buffer_len;
   p.pad = a->pad_slot_id;
   p.philox_rounds = a->philox_rounds;
-  p.stage0 = static_cast<uint32_t>(base);
+  p.desc0 = rsm::desc_base(a->dim, a->dstate, sb);
+  p.arena0 = static_cast<uint32_t>(base);
+  p.arena_bytes = static_cast<uint32_t>(arena);
   p.stages = static_cast<uint32_t>(stages);
-  p.stage_bytes = plan.stage_bytes;
-  p.off_state = plan.off_state;
-  p.off_scale = plan.off_scale;
-  p.off_x = plan.off_x;
-  p.off_B = plan.off_B;
-  p.off_dt = plan.off_dt;
 
   L->fn = fn;
   L->grid = di.sms * per_sm;

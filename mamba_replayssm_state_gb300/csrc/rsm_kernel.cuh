@@ -8,8 +8,10 @@
 // CTA gets a mix of requests (and of replay lengths) while the items of a unit
 // share their metadata and stream through contiguous state memory.
 //
-// One CTA = 1 loader warp + 8 consumer warps, joined by an S-stage ring in
-// shared memory:
+// One CTA = 1 loader warp + 8 consumer warps, joined by S pipeline slots (a
+// full/empty mbarrier pair and a descriptor each) and a byte arena in shared
+// memory that holds the slots' data, each item taking only the bytes of its
+// own replay length:
 //   loader   : finds n (the first -1 of the active list), resolves the slot
 //              and pointer tables once per (request, layer), and per item
 //              issues bulk asynchronous copies (cp.async.bulk) of the source
@@ -20,7 +22,7 @@
 //   consumers: wait for "full", compute the decay of every token once per
 //              warp (exp(dt*A) with a shuffle suffix-product scan), apply the
 //              whole prefix to the tile in registers, requantize, store with
-//              16-byte streaming stores, and release the stage ("empty").
+//              16-byte streaming stores, and release the slot ("empty").
 // Every state element is read once and written once; the ring is only read.
 // Every wait is bounded in wall time (a logic error ends the kernel with a
 // status bit instead of hanging).
@@ -50,7 +52,7 @@ struct alignas(16) ItemDesc {
   float A;                       // A[h]; landed by cp.async
   uint32_t unused[2];
 };
-static_assert(sizeof(ItemDesc) == 48, "descriptor size");
+static_assert(sizeof(ItemDesc) == kDescBytes, "descriptor size");
 constexpr uint32_t kFlagEnd = 1u, kFlagDstAligned = 2u, kFlagScaleAligned = 4u;
 
 __device__ __forceinline__ void flag_status(uint32_t* status, uint32_t bits) {
@@ -169,6 +171,60 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
 
   uint32_t stage = 0, phase = 0, fills = 0;
   bool aborted = false;
+
+  // Arena bookkeeping (warp-uniform).  The n_out items not yet released by
+  // the consumers sit in the n_out slots before `stage` and occupy
+  // [tail, head) of the arena, or [tail, wrap point) + [0, head) once
+  // allocation has wrapped.  Releases complete in slot order (every consumer
+  // warp takes the items in order), so freeing is first in, first out.
+  // Placement depends on the item sizes alone (arena_next), so the consumers
+  // follow it without reading it from the descriptor.
+  const uint32_t item_max = item_layout(D, N, ES, Q, IE, p.W).bytes;
+  uint32_t head = 0, tail = 0, n_out = 0;
+  bool wrapped = false;
+  uint32_t slot_start = 0;  // lane s: arena offset of the item in slot s
+  uint32_t oldest = 0, oldest_phase = 0;  // slot of the oldest outstanding item and its lap parity
+
+  // waits until the consumers released the oldest outstanding item, frees it
+  auto free_oldest = [&]() -> bool {
+    if (!mbar_wait(empty0 + 8u * oldest, oldest_phase, kWaitTimeoutNs)) return false;
+    if (++oldest == p.stages) {
+      oldest = 0;
+      oldest_phase ^= 1u;
+    }
+    --n_out;
+    const uint32_t next = __shfl_sync(0xFFFFFFFFu, slot_start, static_cast<int>(oldest));
+    if (n_out == 0) {
+      tail = head;
+      wrapped = false;
+    } else {
+      if (next < tail) wrapped = false;  // the oldest item is now past the wrap point
+      tail = next;
+    }
+    return true;
+  };
+  // the item's place, then a free slot and free bytes [off, off + bytes) there
+  auto alloc = [&](uint32_t bytes, uint32_t& off) -> bool {
+    off = arena_next(head, item_max, p.arena_bytes);
+    for (;;) {
+      if (n_out == 0) break;
+      if (n_out < p.stages) {
+        if (off == head) {
+          if (!wrapped || head + bytes <= tail) break;  // [head, arena end) holds item_max
+        } else if (!wrapped && bytes <= tail) {
+          break;  // wrapping to 0: [0, tail) is free
+        }
+      }
+      if (!free_oldest()) return false;
+    }
+    if (n_out == 0) {
+      tail = off;
+      wrapped = false;
+    } else if (off != head) {
+      wrapped = true;
+    }
+    return true;
+  };
   int cur_i = -1, b = 0;
   for (int64_t u = blockIdx.x; u < total_units && !aborted; u += gridDim.x) {
     const int64_t seg = u / units_per_seg;
@@ -265,29 +321,29 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
 
     // this lane's ring rows for the whole segment: tokens t = lane and lane + 32
     // (row p_t = (ring_start + t) mod R, the same for every head of the segment)
-    int64_t x_row[2] = {0, 0}, B_row[2] = {0, 0}, dt_row[2] = {0, 0};
+    int ring_row[2];
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int t = lane + 32 * q;
-      const int pr = t < k ? (rs + t) % p.R : 0;
-      x_row[q] = static_cast<int64_t>(pr) * p.H * D * IE;
-      B_row[q] = static_cast<int64_t>(pr) * G * N * IE;
-      dt_row[q] = static_cast<int64_t>(pr) * p.H;
+      ring_row[q] = t < k ? (rs + t) % p.R : 0;
     }
     int g = h / p.hpg;                     // B group of head h, advanced incrementally
     int g_left = p.hpg - (h - g * p.hpg);  // heads left in group g, h included
     const uint4 desc_tail = make_uint4(static_cast<uint32_t>(k), dst_flags, static_cast<uint32_t>(l),
                                        static_cast<uint32_t>(dst));
+    const ItemLayout il = item_layout(D, N, ES, Q, IE, k);
 
     for (; h < h_end; ++h) {
-      if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, kWaitTimeoutNs)) {
+      uint32_t off = 0;
+      if (!alloc(il.bytes, off)) {
         aborted = true;
         break;
       }
-      unsigned char* sb = smem + p.stage0 + stage * p.stage_bytes;
+      unsigned char* sb = smem + p.arena0 + off;
       const uint32_t sba = smem_addr(sb);
       const uint32_t fullb = full0 + 8u * stage;
-      ItemDesc* desc = reinterpret_cast<ItemDesc*>(sb);
+      ItemDesc* desc = reinterpret_cast<ItemDesc*>(smem + p.desc0) + stage;
+      const uint32_t desca = smem_addr(desc);
 
       const int64_t tile_off = static_cast<int64_t>(h) * D * N * ES;
       const unsigned char* src_tile = src_slot + tile_off;
@@ -317,40 +373,41 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
         }
         __syncwarp();
         if (lane == 0) {
-          bulk_g2s_hint(sba + p.off_state, src_tile, kTileBytes, fullb, policy);
-          if constexpr (Q) bulk_g2s(sba + p.off_scale, src_sc, D * 4u, fullb);
-          if (k > 0) cp_async_4(sba + static_cast<uint32_t>(offsetof(ItemDesc, A)), A_ptr);
+          bulk_g2s_hint(sba, src_tile, kTileBytes, fullb, policy);
+          if constexpr (Q) bulk_g2s(sba + il.off_scale, src_sc, D * 4u, fullb);
+          if (k > 0) cp_async_4(desca + static_cast<uint32_t>(offsetof(ItemDesc, A)), A_ptr);
         }
         // ring rows of this lane's tokens t = lane and t = lane + 32
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           const int t = lane + 32 * q;
           if (t < k) {
-            bulk_g2s(sba + p.off_x + static_cast<uint32_t>(t) * D * IE,
-                     x_slot + x_row[q] + static_cast<int64_t>(h) * D * IE, D * IE, fullb);
-            bulk_g2s(sba + p.off_B + static_cast<uint32_t>(t) * N * IE,
-                     B_slot + B_row[q] + static_cast<int64_t>(g) * N * IE, N * IE, fullb);
-            cp_async_4(sba + p.off_dt + 4u * t, dt_slot + dt_row[q] + h);
+            const int64_t xr = static_cast<int64_t>(ring_row[q]) * p.H + h;  // x row [p_t, h] and dt [p_t, h]
+            bulk_g2s(sba + il.off_x + static_cast<uint32_t>(t) * D * IE, x_slot + xr * (D * IE), D * IE, fullb);
+            bulk_g2s(sba + il.off_B + static_cast<uint32_t>(t) * N * IE,
+                     B_slot + (static_cast<int64_t>(ring_row[q]) * G + g) * (N * IE), N * IE, fullb);
+            cp_async_4(sba + il.off_dt + 4u * t, dt_slot + xr);
           }
         }
         cp_async_mbar_arrive(fullb);
       } else {
         // any alignment: plain byte copies by the whole warp
-        copy_bytes_warp(sb + p.off_state, src_tile, kTileBytes, lane);
+        copy_bytes_warp(sb, src_tile, kTileBytes, lane);
         if constexpr (Q)
-          copy_bytes_warp(sb + p.off_scale, reinterpret_cast<const unsigned char*>(src_sc), D * 4u, lane);
+          copy_bytes_warp(sb + il.off_scale, reinterpret_cast<const unsigned char*>(src_sc), D * 4u, lane);
         for (int t = 0; t < k; ++t) {
           const int pr = (rs + t) % p.R;
-          copy_bytes_warp(sb + p.off_x + t * D * IE, x_slot + (static_cast<int64_t>(pr) * p.H + h) * D * IE,
+          copy_bytes_warp(sb + il.off_x + t * D * IE, x_slot + (static_cast<int64_t>(pr) * p.H + h) * D * IE,
                           D * IE, lane);
-          copy_bytes_warp(sb + p.off_B + t * N * IE, B_slot + (static_cast<int64_t>(pr) * G + g) * N * IE,
+          copy_bytes_warp(sb + il.off_B + t * N * IE, B_slot + (static_cast<int64_t>(pr) * G + g) * N * IE,
                           N * IE, lane);
-          copy_bytes_warp(sb + p.off_dt + 4 * t,
+          copy_bytes_warp(sb + il.off_dt + 4 * t,
                           reinterpret_cast<const unsigned char*>(dt_slot + static_cast<int64_t>(pr) * p.H + h), 4,
                           lane);
         }
         if (k > 0)
-          copy_bytes_warp(sb + offsetof(ItemDesc, A), reinterpret_cast<const unsigned char*>(A_ptr), 4, lane);
+          copy_bytes_warp(reinterpret_cast<unsigned char*>(desc) + offsetof(ItemDesc, A),
+                          reinterpret_cast<const unsigned char*>(A_ptr), 4, lane);
         __threadfence_block();
       }
       __syncwarp();
@@ -359,6 +416,10 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
         ++g;
         g_left = p.hpg;
       }
+      // the item now occupies [off, off + il.bytes) of the arena, in slot `stage`
+      if (lane == static_cast<int>(stage)) slot_start = off;
+      head = off + il.bytes;
+      ++n_out;
       ++fills;
       if (++stage == p.stages) {
         stage = 0;
@@ -367,22 +428,26 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
     }
   }
 
-  // end marker for the consumers
+  // end marker for the consumers, in the next slot once it is free
   bool ended = false;
-  if (!aborted && mbar_wait(empty0 + 8u * stage, phase ^ 1u, kWaitTimeoutNs)) {
-    if (lane == 0) reinterpret_cast<ItemDesc*>(smem + p.stage0 + stage * p.stage_bytes)->flags = kFlagEnd;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(full0 + 8u * stage);
-    ended = true;
+  if (!aborted) {
+    bool ok = true;
+    while (ok && n_out >= p.stages) ok = free_oldest();
+    if (ok) {
+      if (lane == 0) (reinterpret_cast<ItemDesc*>(smem + p.desc0) + stage)->flags = kFlagEnd;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full0 + 8u * stage);
+      ended = true;
+    }
   }
   if (!ended) {
     if (lane == 0) {
       *abort_flag = 1;
       flag_status(p.status, RSM_STATUS_WAIT_TIMEOUT);
     }
-    // let copies already issued into the ring land before the CTA exits: the
-    // last fill of stage s completed the full-barrier phase of parity `phase`
-    // (s < stage) or `phase ^ 1` (s >= stage, if the ring went round once)
+    // let copies already issued into the arena land before the CTA exits: the
+    // last fill of slot s completed the full-barrier phase of parity `phase`
+    // (s < stage) or `phase ^ 1` (s >= stage, if the slots went round once)
     for (uint32_t s = 0; s < p.stages; ++s) {
       if (s < stage)
         (void)mbar_wait(full0 + 8u * s, phase, 1000000ull);
@@ -441,6 +506,8 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
     key1 = static_cast<uint32_t>(s >> 32);
   }
 
+  const uint32_t item_max = item_layout(D, N, ES, Q, IE, p.W).bytes;
+  uint32_t arena_head = 0;  // where the loader's next item goes (arena_next)
   uint32_t stage = 0, phase = 0;
   for (;;) {
     if (!mbar_wait(full0 + 8u * stage, phase, kWaitTimeoutNs) || *abort_flag) {
@@ -450,12 +517,16 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
       }
       break;
     }
-    const unsigned char* sb = smem + p.stage0 + stage * p.stage_bytes;
-    const ItemDesc* desc = reinterpret_cast<const ItemDesc*>(sb);
+    // the item's data (tile, scales, x rows, B rows, dt), placed as the loader places it
+    const uint32_t off = arena_next(arena_head, item_max, p.arena_bytes);
+    const unsigned char* sb = smem + p.arena0 + off;
+    const ItemDesc* desc = reinterpret_cast<const ItemDesc*>(smem + p.desc0) + stage;
     const uint32_t flags = desc->flags;
     if (flags & kFlagEnd) break;
-    // everything the item needs from its descriptor, read before the stage is released
+    // everything the item needs from its descriptor, read before the slot is released
     const int k = desc->k;
+    const ItemLayout il = item_layout(D, N, ES, Q, IE, k);
+    arena_head = off + il.bytes;
     unsigned char* dst_tile = reinterpret_cast<unsigned char*>(desc->dst_state);
     float* dst_sc = reinterpret_cast<float*>(desc->dst_scale);
     const bool dst_aligned = (flags & kFlagDstAligned) != 0u;
@@ -478,11 +549,11 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
       if (worker) {
 #pragma unroll
         for (int r = 0; r < RPT; ++r)
-          raw[r] = *reinterpret_cast<const Raw*>(sb + p.off_state + ((row0 + r) * N + col0) * ES);
+          raw[r] = *reinterpret_cast<const Raw*>(sb + ((row0 + r) * N + col0) * ES);
       }
       const int sr_row = cw * 32 + lane;  // one scale per consumer thread (D <= 256)
       if constexpr (Q) {
-        if (sr_row < D) scv = reinterpret_cast<const float*>(sb + p.off_scale)[sr_row];
+        if (sr_row < D) scv = reinterpret_cast<const float*>(sb + il.off_scale)[sr_row];
       }
       release();
       if (worker) {
@@ -513,7 +584,7 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
       // decay of each token, once per warp: a_t = exp(dt_t*A), then
       // w_t = dt_t * prod_{s>t} a_s and P = prod_t a_t by a suffix-product scan
       const float A = desc->A;
-      const float* dts = reinterpret_cast<const float*>(sb + p.off_dt);
+      const float* dts = reinterpret_cast<const float*>(sb + il.off_dt);
       float carry = 1.0f;
       for (int c = (k - 1) >> 5; c >= 0; --c) {
         const int t = 32 * c + lane;
@@ -538,11 +609,11 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
         const float2 P2 = make_float2(P, P);
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
-          const Raw raw = *reinterpret_cast<const Raw*>(sb + p.off_state + ((row0 + r) * N + col0) * ES);
+          const Raw raw = *reinterpret_cast<const Raw*>(sb + ((row0 + r) * N + col0) * ES);
           unpack_vec<SF>(raw, acc[r]);
           if constexpr (Q) {
             // code * (scale * P): the row's scale folded into the decay product
-            const float sp = reinterpret_cast<const float*>(sb + p.off_scale)[row0 + r] * P;
+            const float sp = reinterpret_cast<const float*>(sb + il.off_scale)[row0 + r] * P;
             const float2 sp2 = make_float2(sp, sp);
 #pragma unroll
             for (int u = 0; u < V2; ++u) acc[r][u] = __fmul2_rn(acc[r][u], sp2);
@@ -557,8 +628,8 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
       // the prefix, kTokChunk tokens at a time: convert this warp's share of
       // the tokens to fp32 (c = w*x for its rows, B for its columns), then one
       // rank-1 update per token with packed fp32x2 FMAs
-      const unsigned char* xs = sb + p.off_x;
-      const unsigned char* Bs = sb + p.off_B;
+      const unsigned char* xs = sb + il.off_x;
+      const unsigned char* Bs = sb + il.off_B;
       for (int t0 = 0; t0 < k; t0 += kTokChunk) {
         const int tn = min(kTokChunk, k - t0);
         for (int u = lane; u < tn * (SLAB_ROWS / XW); u += 32) {

@@ -12,8 +12,9 @@ constexpr int kMaxWindow = 64;
 constexpr int kMaxStages = 16;
 constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // 4 s: never reached by a correct run
 
-// Shared memory head: [full mbarriers][empty mbarriers] | abort flag | per-warp
-// decay weights | stages...
+// Shared memory: [full mbarriers][empty mbarriers] | abort flag | per-warp
+// decay weights | per-warp token-chunk buffers | item descriptors (one per
+// pipeline slot) | the item arena.
 constexpr uint32_t kAbortOff = 2 * 8 * kMaxStages;
 constexpr uint32_t kWeightOff = 512;
 constexpr uint32_t kWeightStride = kMaxWindow + 4;  // floats per consumer warp: w_0..w_63, P
@@ -52,9 +53,44 @@ __host__ __device__ constexpr uint32_t warp_buf_floats(int dim, int dstate, int 
                                 thread_layout(dim, dstate, state_bytes).cols));
 }
 
-// Offset of pipeline stage 0: the fixed head plus the consumer warps' buffers.
-__host__ __device__ constexpr uint32_t stage_base(int dim, int dstate, int state_bytes) {
-  return ((kWarpBufOff + kConsumerWarps * warp_buf_floats(dim, dstate, state_bytes) * 4u) + 127u) / 128u * 128u;
+__host__ __device__ constexpr uint32_t round_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+constexpr uint32_t kDescBytes = 48;  // sizeof(ItemDesc)
+
+// Offset of the descriptor table: the fixed head plus the consumer warps' buffers.
+__host__ __device__ constexpr uint32_t desc_base(int dim, int dstate, int state_bytes) {
+  return round_up(kWarpBufOff + kConsumerWarps * warp_buf_floats(dim, dstate, state_bytes) * 4u, 128u);
+}
+
+// Offset of the item arena (after one descriptor per pipeline slot).
+__host__ __device__ constexpr uint32_t arena_base(int dim, int dstate, int state_bytes) {
+  return round_up(desc_base(dim, dstate, state_bytes) + kMaxStages * kDescBytes, 128u);
+}
+
+// Byte layout of one work item in the arena: the source tile at offset 0, its
+// scales (one-byte formats), then the item's own k ring rows of x, of B and
+// its k dt values.  Every part starts on a 16-byte boundary (D*N*ES, D*IE and
+// N*IE are multiples of 16); items start on 128-byte boundaries.
+struct ItemLayout {
+  uint32_t off_scale, off_x, off_B, off_dt, bytes;
+};
+
+__host__ __device__ constexpr ItemLayout item_layout(int dim, int dstate, int state_bytes, bool quant, int in_bytes,
+                                                     int k) {
+  const uint32_t off_scale = static_cast<uint32_t>(dim * dstate * state_bytes);
+  const uint32_t off_x = off_scale + (quant ? static_cast<uint32_t>(dim) * 4u : 0u);
+  const uint32_t off_B = off_x + static_cast<uint32_t>(k * dim * in_bytes);
+  const uint32_t off_dt = off_B + static_cast<uint32_t>(k * dstate * in_bytes);
+  return ItemLayout{off_scale, off_x, off_B, off_dt, round_up(off_dt + 4u * static_cast<uint32_t>(k), 128u)};
+}
+
+// Arena offset of the next item, given where the previous one ended (`head`):
+// there if an item of the longest window would still end inside the arena,
+// else at 0.  It depends on the sizes of the items alone, so the loader that
+// places the items and the consumers that read them agree without exchanging
+// offsets.
+__host__ __device__ constexpr uint32_t arena_next(uint32_t head, uint32_t item_max, uint32_t arena_bytes) {
+  return head + item_max <= arena_bytes ? head : 0u;
 }
 
 struct Params {
@@ -77,27 +113,9 @@ struct Params {
   const int64_t* rand_seed;
   uint32_t* status;
   int32_t L, Bt, H, hpg, W, R, pad, philox_rounds;
-  // shared-memory plan (see make_plan); stage s starts at stage0 + s*stage_bytes
-  uint32_t stage0, stages, stage_bytes, off_state, off_scale, off_x, off_B, off_dt;
+  // shared-memory plan: descriptor table at desc0, item arena of arena_bytes at
+  // arena0, `stages` pipeline slots (mbarrier pairs and descriptors)
+  uint32_t desc0, arena0, arena_bytes, stages;
 };
-
-struct Plan {
-  uint32_t stage_bytes, off_state, off_scale, off_x, off_B, off_dt;
-};
-
-__host__ __device__ constexpr uint32_t round_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
-
-// Byte layout of one pipeline stage.
-__host__ __device__ inline Plan make_plan(int dim, int dstate, int state_bytes, bool quant, int in_bytes,
-                                          int max_window) {
-  Plan p{};
-  p.off_state = 128;
-  p.off_scale = round_up(p.off_state + dim * dstate * state_bytes, 128);
-  p.off_x = round_up(p.off_scale + (quant ? dim * 4 : 0), 128);
-  p.off_B = round_up(p.off_x + max_window * dim * in_bytes, 128);
-  p.off_dt = round_up(p.off_B + max_window * dstate * in_bytes, 128);
-  p.stage_bytes = round_up(p.off_dt + max_window * 4, 128);
-  return p;
-}
 
 }  // namespace rsm
