@@ -53,6 +53,19 @@ class OracleArgs(ctypes.Structure):
     ]
 
 
+class GdnArgs(ctypes.Structure):
+    """Mirror of oracle_gdn_args (gdn_commit_oracle.h)."""
+    _fields_ = [
+        ("state", ctypes.c_void_p), ("rawv", ctypes.c_void_p), ("rawk", ctypes.c_void_p),
+        ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p),
+        ("state_indices", _P32), ("accept_lens", _P32),
+        ("track_state_indices", _P32), ("track_steps", _P32),
+        ("layers", ctypes.c_int32), ("slots", ctypes.c_int32), ("hv", ctypes.c_int32), ("h", ctypes.c_int32),
+        ("t", ctypes.c_int32), ("batch", ctypes.c_int32),
+        ("use_qk_l2norm", ctypes.c_int32), ("null_block_id", ctypes.c_int32),
+    ]
+
+
 _lib = None
 
 
@@ -73,6 +86,9 @@ def lib():
         L.oracle_encode.argtypes = [ctypes.c_int, ctypes.c_double]
         L.oracle_encode.restype = ctypes.c_uint32
         L.oracle_args_size.restype = ctypes.c_int
+        L.oracle_gdn_commit.argtypes = [ctypes.POINTER(GdnArgs)]
+        L.oracle_gdn_commit.restype = ctypes.c_int
+        L.oracle_gdn_last_error.restype = ctypes.c_char_p
         if L.oracle_args_size() != ctypes.sizeof(OracleArgs):
             raise RuntimeError("oracle argument struct layout mismatch")
         _lib = L
@@ -168,3 +184,42 @@ def decode(fmt, bits):
 
 def encode(fmt, value):
     return lib().oracle_encode(DTYPE_CODES.get(fmt, fmt), float(value))
+
+
+def gdn_commit(world) -> None:
+    """Runs the gated-delta-rule commit oracle on a host world in place
+    (flashinfer.gdn_decode.gated_delta_rule_replayssm_commit, API page):
+    world.state is updated; track slots are written.  `world` is a
+    workloads.GdnWorld (any object with the same attributes works)."""
+    L = lib()
+    keep = []
+
+    def arr(a, dtype):
+        assert a.dtype == dtype and a.flags["C_CONTIGUOUS"], (a.dtype, dtype)
+        keep.append(a)
+        return a.ctypes.data
+
+    def i32(a):
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a, dtype=np.int32)
+        keep.append(a)
+        return a.ctypes.data_as(_P32)
+
+    L_, SL, HV, T = world.state.shape[0], world.state.shape[1], world.state.shape[2], world.rawv.shape[3]
+    args = GdnArgs()
+    args.state = arr(world.state, np.float32)
+    args.rawv = arr(world.rawv, np.uint16)
+    args.rawk = arr(world.rawk, np.uint16)
+    args.g = arr(world.g, np.float32)
+    args.beta = arr(world.beta, np.float32)
+    args.state_indices = i32(world.state_indices)
+    args.accept_lens = i32(world.accept_lens)
+    args.track_state_indices = i32(world.track_state_indices)
+    args.track_steps = i32(world.track_steps)
+    args.layers, args.slots, args.hv, args.h, args.t = L_, SL, HV, world.rawk.shape[2], T
+    args.batch = len(world.state_indices)
+    args.use_qk_l2norm = int(bool(world.use_qk_l2norm))
+    args.null_block_id = int(world.null_block_id)
+    if L.oracle_gdn_commit(ctypes.byref(args)) != 0:
+        raise ValueError("oracle: " + L.oracle_gdn_last_error().decode())

@@ -8,7 +8,7 @@ import subprocess
 import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-SRC = os.path.join(HERE, "replayssm_oracle.c")
+SRCS = [os.path.join(HERE, "replayssm_oracle.c"), os.path.join(HERE, "gdn_commit_oracle.c")]
 LIB = os.path.join(HERE, "_replayssm_oracle.so")
 
 # -ffp-contract=off: no fused multiply-add, every fp32 step rounds on its own.
@@ -16,12 +16,13 @@ CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-s
 
 
 def build(force: bool = False) -> str:
-    deps = [SRC, os.path.join(HERE, "replayssm_oracle.h"), os.path.abspath(__file__)]
+    deps = SRCS + [os.path.join(HERE, "replayssm_oracle.h"), os.path.join(HERE, "gdn_commit_oracle.h"),
+                   os.path.abspath(__file__)]
     if not force and os.path.exists(LIB):
         if os.path.getmtime(LIB) >= max(os.path.getmtime(p) for p in deps):
             return LIB
     tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = ["gcc", *CFLAGS, SRC, "-o", tmp, "-lm"]
+    cmd = ["gcc", *CFLAGS, *SRCS, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
     return LIB
