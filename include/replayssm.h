@@ -2,10 +2,11 @@
  * replayssm.h -- C ABI of libreplayssm.so: ReplaySSM prefix materialization on
  * GB300 (sm_103a).
  *
- * One entry point, rsm_materialize(), mirrors flashinfer.mamba.replayssm_materialize
- * (API page: signature, Parameters, Notes).  The page's torch.compile
- * dependency anchors (dependency_inputs / dependency_outputs) are torch
- * plumbing and are not part of a C call.
+ * rsm_materialize() mirrors flashinfer.mamba.replayssm_materialize (API page:
+ * signature, Parameters, Notes).  The page's torch.compile dependency anchors
+ * (dependency_inputs / dependency_outputs) are torch plumbing and are not part
+ * of a C call.  rsm_gdn_commit() (declared further down) mirrors
+ * flashinfer.gdn_decode.gated_delta_rule_replayssm_commit.
  *
  * What it computes.  For every request b selected by the -1-terminated
  * active_request_indices and every layer l, read the source state slot
@@ -59,7 +60,7 @@
 extern "C" {
 #endif
 
-#define RSM_ABI_VERSION 1
+#define RSM_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define RSM_API __attribute__((visibility("default")))
@@ -158,6 +159,67 @@ RSM_API int rsm_abi_version(void);
  */
 RSM_API int rsm_launch_config(const rsm_materialize_args *args, int *grid, int *block,
                       int *smem_bytes, int *stages);
+
+/*
+ * ---------------------------------------------------------------------------
+ * Gated-delta-rule commit (flashinfer.gdn_decode.gated_delta_rule_replayssm_commit,
+ * API page: signature, Parameters, Notes).
+ *
+ * What it computes.  For every request b whose slot s = state_indices[b] is
+ * live (s > null_block_id) and whose accepted length n = accept_lens[b] is not
+ * zero, and for every layer l and value head hv, the accepted tokens
+ * t = 0 .. n-1 of the slot's windows are applied in order to the checkpoint
+ * S = checkpoint_state[l, s, hv] (128 value rows x 128 key columns, fp32,
+ * K-last), in place:
+ *     k^ = k_t / sqrt(|k_t|^2 + 1e-6)   (use_qk_l2norm; otherwise k^ = k_t)
+ *     S  = exp(g_t) * S
+ *     S  = S + beta_t * (v_t - S k^) k^T
+ * with k_t = rawk_cache[l, s, hv / (num_v_heads / num_k_heads), t, :] and
+ * v_t = rawv_cache[l, s, hv, t, :].  With tracking, the state right after
+ * token track_steps[b] (zero-based) is also written to
+ * checkpoint_state[l, track_state_indices[b], hv] when that slot is live and
+ * the step lies inside the accepted prefix; otherwise the track slot is left
+ * unchanged.  The windows are only read; nothing is shifted or cleared.
+ *
+ * Memory layout (contiguous, every base 16-byte aligned, as the page requires):
+ *   checkpoint_state [layers, slots, num_v_heads, 128, 128] fp32
+ *   rawv_cache       [layers, slots, num_v_heads, window, 128] bf16
+ *   rawk_cache       [layers, slots, num_k_heads, window, 128] bf16 (before normalisation)
+ *   g_cache          [layers, slots, num_v_heads, window] fp32 log-decay
+ *   beta_cache       [layers, slots, num_v_heads, window] fp32 (sigmoid already applied)
+ *   state_indices, accept_lens, track_state_indices, track_steps: [batch] int32
+ *
+ * Ownership, errors and the status word are as for rsm_materialize: device
+ * pointers, caller-owned, one kernel enqueued on `stream`, no allocation, no
+ * host read of device memory, no synchronization.  The kernel skips a request
+ * whose slot is >= slots (RSM_STATUS_BAD_SLOT) or whose accepted length is
+ * outside [0, window] (RSM_STATUS_BAD_PREFIX_LEN); a track slot >= slots is
+ * ignored and flagged likewise.  Live state slots must be unique and live
+ * track slots distinct and disjoint from them (caller contract, not checked).
+ */
+typedef struct rsm_gdn_commit_args {
+  float *checkpoint_state;
+  const uint16_t *rawv_cache, *rawk_cache; /* bf16 bit patterns */
+  const float *g_cache, *beta_cache;
+  const int32_t *state_indices, *accept_lens;
+  const int32_t *track_state_indices, *track_steps; /* both NULL, or both given */
+  uint32_t *device_status;                         /* optional, RSM_STATUS_* bits */
+  int32_t layers, slots;
+  int32_t num_v_heads, num_k_heads; /* num_k_heads divides num_v_heads */
+  int32_t window;                   /* T: 1 .. 64 */
+  int32_t batch;                    /* >= 0; 0 enqueues nothing */
+  int32_t use_qk_l2norm;            /* nonzero: normalise k with epsilon 1e-6 */
+  int32_t null_block_id;            /* >= -1; slots <= it are ignored */
+} rsm_gdn_commit_args;
+
+/* Enqueue the commit described by *args on `stream`; same return codes as
+ * rsm_materialize.  Host checks: non-NULL tensors, positive sizes, divisibility
+ * of the heads, window range, null_block_id >= -1, track arrays both or
+ * neither, and 16-byte alignment of every tensor base (RSM_EINVAL). */
+RSM_API int rsm_gdn_commit(const rsm_gdn_commit_args *args, void *stream);
+
+/* sizeof(rsm_gdn_commit_args). */
+RSM_API int rsm_gdn_args_size(void);
 
 #ifdef __cplusplus
 }

@@ -16,8 +16,8 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["replayssm_materialize", "prepare", "launch_config", "pointer_table", "stride_table",
-           "library_path", "load_library", "ReplaySSMError", "STATUS_BITS"]
+__all__ = ["replayssm_materialize", "gated_delta_rule_replayssm_commit", "prepare", "launch_config",
+           "pointer_table", "stride_table", "library_path", "load_library", "ReplaySSMError", "STATUS_BITS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libreplayssm.so")
@@ -61,13 +61,26 @@ class RsmArgs(ctypes.Structure):
     ]
 
 
-EXPORTS = ("rsm_materialize", "rsm_last_error", "rsm_args_size", "rsm_abi_version", "rsm_launch_config")
+EXPORTS = ("rsm_materialize", "rsm_last_error", "rsm_args_size", "rsm_abi_version", "rsm_launch_config",
+           "rsm_gdn_commit", "rsm_gdn_args_size")
 
 _lib = None
 
 
 def library_path() -> str:
     return _LIB_PATH
+
+
+class GdnArgs(ctypes.Structure):
+    """Mirror of rsm_gdn_commit_args (include/replayssm.h)."""
+    _fields_ = [
+        ("checkpoint_state", _P), ("rawv_cache", _P), ("rawk_cache", _P), ("g_cache", _P), ("beta_cache", _P),
+        ("state_indices", _P), ("accept_lens", _P), ("track_state_indices", _P), ("track_steps", _P),
+        ("device_status", _P),
+        ("layers", ctypes.c_int32), ("slots", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
+        ("num_k_heads", ctypes.c_int32), ("window", ctypes.c_int32), ("batch", ctypes.c_int32),
+        ("use_qk_l2norm", ctypes.c_int32), ("null_block_id", ctypes.c_int32),
+    ]
 
 
 def load_library(build_if_missing: bool = True):
@@ -90,6 +103,11 @@ def load_library(build_if_missing: bool = True):
     lib.rsm_launch_config.restype = ctypes.c_int
     if lib.rsm_args_size() != ctypes.sizeof(RsmArgs):
         raise OSError("rsm_materialize_args layout mismatch between libreplayssm.so and the binding")
+    lib.rsm_gdn_commit.argtypes = [ctypes.POINTER(GdnArgs), ctypes.c_void_p]
+    lib.rsm_gdn_commit.restype = ctypes.c_int
+    lib.rsm_gdn_args_size.restype = ctypes.c_int
+    if lib.rsm_gdn_args_size() != ctypes.sizeof(GdnArgs):
+        raise OSError("rsm_gdn_commit_args layout mismatch between libreplayssm.so and the binding")
     _lib = lib
     return lib
 
@@ -262,3 +280,72 @@ def stride_table(tensors, device=None):
     import torch
     dev = device or next(t.device for t in tensors if t is not None)
     return torch.tensor([0 if t is None else t.stride(0) for t in tensors], dtype=torch.int64, device=dev)
+
+
+def _gdn_args(checkpoint_state, rawv_cache, rawk_cache, g_cache, beta_cache, state_indices, accept_lens, *,
+              track_state_indices=None, track_steps=None, use_qk_l2norm=True, null_block_id=-1,
+              device_status=None):
+    import torch
+    if checkpoint_state.dim() != 5 or tuple(checkpoint_state.shape[3:]) != (128, 128):
+        raise ValueError("checkpoint_state must be [layers, slots, HV, 128, 128]")
+    L, SL, HV = checkpoint_state.shape[:3]
+    if rawv_cache.dim() != 5 or tuple(rawv_cache.shape[:3]) != (L, SL, HV) or rawv_cache.shape[4] != 128:
+        raise ValueError("rawv_cache must be [layers, slots, HV, T, 128]")
+    T = rawv_cache.shape[3]
+    if rawk_cache.dim() != 5 or tuple(rawk_cache.shape[:2]) != (L, SL) or tuple(rawk_cache.shape[3:]) != (T, 128):
+        raise ValueError("rawk_cache must be [layers, slots, H, T, 128]")
+    for name, t in (("g_cache", g_cache), ("beta_cache", beta_cache)):
+        if tuple(t.shape) != (L, SL, HV, T):
+            raise ValueError(f"{name} must be [layers, slots, HV, T]")
+    if (track_state_indices is None) != (track_steps is None):
+        raise ValueError("track_state_indices and track_steps come together")
+    B = state_indices.numel()
+    for name, t in (("accept_lens", accept_lens), ("track_state_indices", track_state_indices),
+                    ("track_steps", track_steps)):
+        if t is not None and t.numel() != B:
+            raise ValueError(f"{name} must have B={B} entries")
+    a = GdnArgs()
+    a.checkpoint_state = _ptr(checkpoint_state, "checkpoint_state", torch.float32)
+    a.rawv_cache = _ptr(rawv_cache, "rawv_cache", torch.bfloat16)
+    a.rawk_cache = _ptr(rawk_cache, "rawk_cache", torch.bfloat16)
+    a.g_cache = _ptr(g_cache, "g_cache", torch.float32)
+    a.beta_cache = _ptr(beta_cache, "beta_cache", torch.float32)
+    a.state_indices = _ptr(state_indices, "state_indices", torch.int32)
+    a.accept_lens = _ptr(accept_lens, "accept_lens", torch.int32)
+    a.track_state_indices = _ptr(track_state_indices, "track_state_indices", torch.int32, optional=True)
+    a.track_steps = _ptr(track_steps, "track_steps", torch.int32, optional=True)
+    a.device_status = _ptr(device_status, "device_status", optional=True)
+    a.layers, a.slots, a.num_v_heads, a.num_k_heads = int(L), int(SL), int(HV), int(rawk_cache.shape[2])
+    a.window, a.batch = int(T), int(B)
+    a.use_qk_l2norm = int(bool(use_qk_l2norm))
+    a.null_block_id = int(null_block_id)
+    return a
+
+
+def gated_delta_rule_replayssm_commit(checkpoint_state, rawv_cache, rawk_cache, g_cache, beta_cache, state_indices,
+                                      accept_lens, *, track_state_indices=None, track_steps=None,
+                                      use_qk_l2norm=True, null_block_id=-1, backend="auto", device_status=None,
+                                      stream=None) -> None:
+    """Commit accepted ReplaySSM prefixes into every layer's gated-delta-rule
+    checkpoints, in place.
+
+    Same arguments as flashinfer.gdn_decode.gated_delta_rule_replayssm_commit
+    (API page).  There is one kernel, with fp32 contractions on the CUDA cores:
+    `backend` "auto" and "simt" select it; "tcgen05" is not built and raises.
+    `device_status` (optional int32 [1] CUDA tensor) receives RSM_STATUS_* bits
+    for skipped out-of-range metadata.  Asynchronous on `stream` (default:
+    torch's current stream).
+    """
+    import torch
+    if backend not in ("auto", "simt"):
+        raise ValueError(f"backend {backend!r} is not available (this library has the fp32 'simt' kernel only)")
+    lib = load_library()
+    a = _gdn_args(checkpoint_state, rawv_cache, rawk_cache, g_cache, beta_cache, state_indices, accept_lens,
+                  track_state_indices=track_state_indices, track_steps=track_steps, use_qk_l2norm=use_qk_l2norm,
+                  null_block_id=null_block_id, device_status=device_status)
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    rc = lib.rsm_gdn_commit(ctypes.byref(a), ctypes.c_void_p(handle))
+    if rc != 0:
+        raise ReplaySSMError(rc, lib.rsm_last_error().decode())

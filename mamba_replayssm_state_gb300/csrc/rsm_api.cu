@@ -16,6 +16,7 @@
 #include <string>
 
 #include "../../include/replayssm.h"
+#include "gdn_params.h"
 #include "rsm_instances.h"
 #include "rsm_params.h"
 
@@ -261,6 +262,117 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   return RSM_OK;
 }
 
+// ---------------------------------------------------------------------------
+// gated-delta-rule commit (flashinfer.gdn_decode.gated_delta_rule_replayssm_commit,
+// API page: Parameters and Notes give the checks below)
+// ---------------------------------------------------------------------------
+int g_gdn_smem_set[kMaxDevices];
+int g_gdn_occ_smem[kMaxDevices];
+int g_gdn_occ_blocks[kMaxDevices];
+
+int validate_gdn(const rsm_gdn_commit_args* a) {
+  if (a == nullptr) return fail(RSM_EINVAL, "args is NULL");
+  const struct {
+    const void* p;
+    const char* name;
+  } tensors[] = {{a->checkpoint_state, "checkpoint_state"}, {a->rawv_cache, "rawv_cache"},
+                 {a->rawk_cache, "rawk_cache"},             {a->g_cache, "g_cache"},
+                 {a->beta_cache, "beta_cache"},             {a->state_indices, "state_indices"},
+                 {a->accept_lens, "accept_lens"}};
+  for (const auto& t : tensors) {
+    if (t.p == nullptr) return fail(RSM_EINVAL, "%s is NULL", t.name);
+    if (reinterpret_cast<uintptr_t>(t.p) % 16 != 0)
+      return fail(RSM_EINVAL, "%s is not 16-byte aligned", t.name);
+  }
+  if ((a->track_state_indices == nullptr) != (a->track_steps == nullptr))
+    return fail(RSM_EINVAL, "track_state_indices and track_steps must be given together");
+  if (a->track_state_indices != nullptr &&
+      (reinterpret_cast<uintptr_t>(a->track_state_indices) % 16 != 0 ||
+       reinterpret_cast<uintptr_t>(a->track_steps) % 16 != 0))
+    return fail(RSM_EINVAL, "track tensors are not 16-byte aligned");
+  if (a->layers <= 0 || a->slots <= 0 || a->batch < 0)
+    return fail(RSM_EINVAL, "layers and slots must be positive and batch non-negative");
+  if (a->num_v_heads <= 0 || a->num_k_heads <= 0 || a->num_v_heads % a->num_k_heads != 0)
+    return fail(RSM_EINVAL, "num_k_heads (%d) must divide num_v_heads (%d)", a->num_k_heads, a->num_v_heads);
+  if (a->window < 1 || a->window > gdn::kMaxWindow)
+    return fail(RSM_EINVAL, "window %d outside [1, %d]", a->window, gdn::kMaxWindow);
+  if (a->null_block_id < -1) return fail(RSM_EINVAL, "null_block_id must be >= -1");
+  const int64_t heads = static_cast<int64_t>(a->layers) * a->slots * a->num_v_heads;
+  if (heads * gdn::kDV * gdn::kDK >= (int64_t{1} << 62) / 4)
+    return fail(RSM_EINVAL, "checkpoint_state is too large");
+  return RSM_OK;
+}
+
+struct GdnLaunch {
+  int grid, smem;
+  gdn::Params params;
+};
+
+int plan_gdn(const rsm_gdn_commit_args* a, GdnLaunch* L) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(RSM_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  DeviceInfo di;
+  int rc = device_info(dev, &di);
+  if (rc != RSM_OK) return rc;
+  // as for the materialization kernel: two CTAs per SM while each arena holds
+  // two items of the longest window, six pipeline slots per SM
+  const int item_min = static_cast<int>(gdn::item_layout(1).bytes);
+  const int item_max = static_cast<int>(gdn::item_layout(a->window).bytes);
+  const int base = static_cast<int>(gdn::kArenaOff);
+  const int two_cta = di.smem_per_sm / 2 - di.smem_reserved - base;
+  const int one_cta = di.smem_optin - base;
+  const bool two = two_cta >= 2 * item_max;
+  const int arena = (two ? two_cta : one_cta) / 128 * 128;
+  if (arena < 2 * item_max) return fail(RSM_ENOTSUP, "two work items of %d bytes do not fit", item_max);
+  int slots = arena / item_min;
+  if (slots > kSlotsPerSm / (two ? 2 : 1)) slots = kSlotsPerSm / (two ? 2 : 1);
+  const int smem = base + arena;
+  const void* fn = gdn::commit_kernel();
+  int per_sm = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_gdn_smem_set[dev] < smem) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return fail(RSM_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+      g_gdn_smem_set[dev] = smem;
+    }
+    if (g_gdn_occ_smem[dev] == smem) {
+      per_sm = g_gdn_occ_blocks[dev];
+    } else {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, gdn::kThreads, smem);
+      if (e != cudaSuccess) return fail(RSM_ECUDA, "occupancy query: %s", cudaGetErrorString(e));
+      g_gdn_occ_smem[dev] = smem;
+      g_gdn_occ_blocks[dev] = per_sm;
+    }
+  }
+  if (per_sm < 1) return fail(RSM_ENOTSUP, "kernel does not fit on an SM with %d bytes of shared memory", smem);
+  gdn::Params& p = L->params;
+  p.state = a->checkpoint_state;
+  p.rawv = a->rawv_cache;
+  p.rawk = a->rawk_cache;
+  p.g = a->g_cache;
+  p.beta = a->beta_cache;
+  p.state_indices = a->state_indices;
+  p.accept_lens = a->accept_lens;
+  p.track_indices = a->track_state_indices;
+  p.track_steps = a->track_steps;
+  p.status = a->device_status;
+  p.L = a->layers;
+  p.SL = a->slots;
+  p.HV = a->num_v_heads;
+  p.H = a->num_k_heads;
+  p.T = a->window;
+  p.B = a->batch;
+  p.l2norm = a->use_qk_l2norm != 0;
+  p.null_id = a->null_block_id;
+  p.arena_bytes = static_cast<uint32_t>(arena);
+  p.slots = static_cast<uint32_t>(slots);
+  L->grid = di.sms * per_sm;
+  L->smem = smem;
+  return RSM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -291,6 +403,29 @@ int rsm_launch_config(const rsm_materialize_args* args, int* grid, int* block, i
   if (stages) *stages = L.stages;
   return RSM_OK;
 }
+
+int rsm_gdn_commit(const rsm_gdn_commit_args* args, void* stream) {
+  int rc = validate_gdn(args);
+  if (rc != RSM_OK) return rc;
+  if (args->batch == 0) {
+    g_last_error.clear();
+    return RSM_OK;
+  }
+  GdnLaunch L;
+  rc = plan_gdn(args, &L);
+  if (rc != RSM_OK) return rc;
+  if (verbose())
+    std::fprintf(stderr, "[replayssm] gdn commit grid=%d block=%d smem=%d slots=%u\n", L.grid, gdn::kThreads, L.smem,
+                 L.params.slots);
+  void* kargs[] = {&L.params};
+  cudaError_t e = cudaLaunchKernel(gdn::commit_kernel(), dim3(L.grid), dim3(gdn::kThreads), kargs,
+                                   static_cast<size_t>(L.smem), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(RSM_ECUDA, "launch failed: %s", cudaGetErrorString(e));
+  g_last_error.clear();
+  return RSM_OK;
+}
+
+int rsm_gdn_args_size(void) { return static_cast<int>(sizeof(rsm_gdn_commit_args)); }
 
 const char* rsm_last_error(void) { return g_last_error.c_str(); }
 

@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_struct_layout_and_version(lib):
     assert lib.rsm_args_size() == ctypes.sizeof(rsm.RsmArgs)
-    assert lib.rsm_abi_version() == 1
+    assert lib.rsm_abi_version() == 2
 
 
 def test_oracle_library_loads():
@@ -127,3 +127,51 @@ def test_no_oracle_on_the_product_path():
                 txt = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in txt and "from oracle" not in txt, f
                 assert "replayssm_oracle" not in txt, f
+
+
+# ----------------------------------------------------------------------------
+# rsm_gdn_commit: host-side validation (no CUDA call is reached)
+# ----------------------------------------------------------------------------
+
+def good_gdn_args():
+    a = rsm.GdnArgs()
+    for name in ("checkpoint_state", "rawv_cache", "rawk_cache", "g_cache", "beta_cache", "state_indices",
+                 "accept_lens"):
+        setattr(a, name, 0x10000)
+    a.layers, a.slots, a.num_v_heads, a.num_k_heads, a.window, a.batch = 36, 128, 32, 16, 8, 64
+    a.use_qk_l2norm, a.null_block_id = 1, -1
+    return a
+
+
+def test_gdn_struct_layout(lib):
+    assert lib.rsm_gdn_args_size() == ctypes.sizeof(rsm.GdnArgs)
+
+
+@pytest.mark.parametrize("rule", ["null_state", "misaligned", "track_half", "heads", "window_lo", "window_hi",
+                                  "null_id", "layers"])
+def test_gdn_validation_rejects(lib, rule):
+    a = good_gdn_args()
+    if rule == "null_state":
+        a.checkpoint_state = None
+    elif rule == "misaligned":
+        a.rawk_cache = 0x10008
+    elif rule == "track_half":
+        a.track_state_indices = 0x10000
+    elif rule == "heads":
+        a.num_k_heads = 5
+    elif rule == "window_lo":
+        a.window = 0
+    elif rule == "window_hi":
+        a.window = 65
+    elif rule == "null_id":
+        a.null_block_id = -2
+    else:
+        a.layers = 0
+    assert lib.rsm_gdn_commit(ctypes.byref(a), None) == -1
+    assert lib.rsm_last_error()
+
+
+def test_gdn_empty_batch_enqueues_nothing(lib):
+    a = good_gdn_args()
+    a.batch = 0
+    assert lib.rsm_gdn_commit(ctypes.byref(a), None) == 0
