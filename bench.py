@@ -31,6 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from mamba_replayssm_state_gb300 import dist  # noqa: E402
+from mamba_replayssm_state_gb300 import gdn_workloads as gw  # noqa: E402
 from mamba_replayssm_state_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "state GB/s & µs/active request (48L×256H×64×128); empty-active-list µs"
@@ -56,12 +57,14 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--all-workloads", action="store_true",
                    help="also measure the other named workloads (added under 'workloads')")
+    p.add_argument("--gdn", action="store_true",
+                   help="measure only the gated-delta-rule commit (gdn36_hv32_t8; --batch overrides B)")
     return p.parse_args()
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, "mamba_replayssm_state_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -361,6 +364,46 @@ def measure_workload(torch, rsm, shape, device, steps, peak_gbs, sms, sm_mhz):
             "alu_frac": fmas / (ms * 1e-3) / alu_peak, "device_status": status}
 
 
+GDN_SOURCES = ["gdn_kernel.cuh", "gdn_params.h", "rsm_ptx.cuh", "rsm_api.cu"]
+
+
+def measure_gdn(torch, rsm, shape, device, steps, peak_gbs, sms, sm_mhz):
+    """Time of one gated-delta-rule commit call over a seeded full-size world
+    (state updated in place, so every timed call is a fresh commit of the same
+    shape), its algorithmic bytes against the HBM peak, and its FP32 lane
+    operations (per element and accepted token: the dot-product FMA, the decay
+    multiply and the update FMA) against the lane peak."""
+    import numpy as np
+    dw = gw.gdn_device_world_random(shape, seed=5, device=device)
+    kw = dw.call_kwargs()
+    idx, lens = dw.state_indices.cpu().numpy(), dw.accept_lens.cpu().numpy()
+    tidx = None if dw.track_state_indices is None else dw.track_state_indices.cpu().numpy()
+    tst = None if dw.track_steps is None else dw.track_steps.cpu().numpy()
+    nbytes = gw.gdn_bytes(shape, idx, lens, tidx, tst)
+    live = [b for b in range(shape.B) if idx[b] > shape.null_block_id and lens[b] > 0]
+    lane_ops = sum(int(lens[b]) for b in live) * shape.L * shape.HV * gw.DV * gw.DK * 3
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        rsm.gated_delta_rule_replayssm_commit(**kw, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        rsm.gated_delta_rule_replayssm_commit(**kw, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    status = int(dw.status.item())
+    del dw, kw
+    torch.cuda.empty_cache()
+    alu_peak = sms * ALU_LANES_PER_SM * sm_mhz * 1e6
+    return {"kernel": "gdn_commit_kernel", "layers": shape.L, "v_heads": shape.HV, "k_heads": shape.H,
+            "window": shape.T, "batch": shape.B, "live_requests": len(live), "track": shape.track,
+            "accept": list(shape.accept), "ms_per_call": ms, "algorithmic_bytes": nbytes,
+            "gbs": nbytes / (ms * 1e-3) / 1e9, "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peak_gbs,
+            "alu_frac": lane_ops / (ms * 1e-3) / alu_peak, "device_status": status}
+
+
 def main():
     args = parse_args()
     rank, local_rank, world = dist.env()
@@ -375,6 +418,21 @@ def main():
     device = torch.device("cuda", local_rank)
     dist.init("nccl")
     rsm.load_library()
+
+    if args.gdn:
+        gshape = gw.GDN_SHAPES["gdn36_hv32_t8"]
+        if args.batch is not None:
+            gshape = gshape.replace(B=args.batch)
+        if args.prefix is not None:
+            gshape = gshape.replace(accept=("fixed", args.prefix))
+        gpeak, gsrc = measured_peak()
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        res = measure_gdn(torch, rsm, gshape, device, max(args.steps, 1), gpeak, sms, 2070.0)
+        if rank == 0:
+            print(json.dumps({"metric": "gated-delta-rule commit: algorithmic GB/s", "unit": "GB/s",
+                              "value": res["gbs"], "peak_gbs": gpeak, "peak_source": gsrc,
+                              "source_hash": kernel_source_hash(GDN_SOURCES), **res}), flush=True)
+        return 0
 
     shape = wl.SHAPES[args.workload]
     if args.batch is not None:
@@ -519,6 +577,10 @@ def main():
         for k in (0, 1, 4, 16, 64):
             shp = wl.SHAPES["ring_sweep_fp16"].replace(prefix=("fixed", k))
             sweep[f"ring_sweep_fp16_k{k}"] = measure_workload(torch, rsm, shp, device, 10, peak, sms, mhz)
+        gshape = gw.GDN_SHAPES["gdn36_hv32_t8"]
+        sweep["gdn36_hv32_t8"] = measure_gdn(torch, rsm, gshape, device, 20, peak, sms, mhz)
+        sweep["gdn36_hv32_t8_full"] = measure_gdn(torch, rsm, gshape.replace(accept=("fixed", 8)), device, 20,
+                                                  peak, sms, mhz)
         out["workloads"] = sweep
         out["alu_peak_note"] = f"{sms} SMs x {ALU_LANES_PER_SM} FP32 lanes x {mhz:.0f} MHz lane-FMA/s"
     if rank == 0:

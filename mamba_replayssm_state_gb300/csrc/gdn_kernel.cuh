@@ -12,7 +12,8 @@
 // work item is a slab of 32 rows of one head (16 KiB): a row's dot product is
 // a reduction over the 8 lanes that hold it.  The normalisation is folded into
 // two scalars per token (S k^ = r * S k, k^ k^T update = (u r) k), so k is
-// used raw.
+// used raw, and the decay into a running scale of the whole slab, so that each
+// element costs two FMAs per token.
 //
 // One CTA = 1 loader warp + 8 consumer warps joined by pipeline slots (full /
 // empty mbarrier pairs and descriptors) and a byte arena, as in the
@@ -268,13 +269,46 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
     const Item it = item_layout(n);
     arena_head = off + it.bytes;
 
+    // per-token scalars, once per item and warp, four lanes per token:
+    // exp(g), beta, r = 1/sqrt(|k|^2 + 1e-6) (1 without normalisation), exp(-g)
+    float4* tok = reinterpret_cast<float4*>(smem + kTokOff + cw * kTokBytes);
+    for (int t0 = 0; t0 < n; t0 += 8) {
+      const int t = t0 + (lane >> 2), part = lane & 3;
+      float ss = 0.0f;
+      if (t < n && l2norm) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // columns (q*4 + part)*8 .. +7
+          const uint4 w = *reinterpret_cast<const uint4*>(sb + it.off_k + t * kDK * 2 + (q * 4 + part) * 16);
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = bf16lo(ws[e]), hi = bf16hi(ws[e]);
+            ss = fmaf(lo, lo, ss);
+            ss = fmaf(hi, hi, ss);
+          }
+        }
+      }
+      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
+      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
+      if (t < n && part == 0) {
+        const float g = reinterpret_cast<const float*>(sb + it.off_g)[t];
+        tok[t] = make_float4(expf(g), reinterpret_cast<const float*>(sb + it.off_beta)[t],
+                             l2norm ? rsqrtf(ss + 1e-6f) : 1.0f, expf(-g));
+      }
+    }
+    __syncwarp();
+
+    // The decay is kept as a scale: the state is c * S.  Per token, with
+    // ca = c * exp(g): S k^ after the decay is ca * r * (S k), and the update
+    // (u r) k adds (u r / ca) k to S.  Rescaling is exact up to rounding
+    // (it scales every term alike); S is renormalised before c gets small.
     float4 S[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q)
       S[q] = *reinterpret_cast<const float4*>(sb + (row * kDK + q * 32 + lc * 4) * 4);
-
+    float c = 1.0f, inv_c = 1.0f;
     for (int t = 0; t < n; ++t) {
-      // this lane's 16 key values (four groups of four bf16)
+      const float4 tp = tok[t];
       float k[16];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -284,44 +318,52 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
         k[4 * q + 2] = bf16lo(w.y);
         k[4 * q + 3] = bf16hi(w.y);
       }
-      float dot = 0.0f, ss = 0.0f;
+      float dq[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        dot = fmaf(S[q].x, k[4 * q], dot);
-        dot = fmaf(S[q].y, k[4 * q + 1], dot);
-        dot = fmaf(S[q].z, k[4 * q + 2], dot);
-        dot = fmaf(S[q].w, k[4 * q + 3], dot);
+        dq[q] = S[q].x * k[4 * q];
+        dq[q] = fmaf(S[q].y, k[4 * q + 1], dq[q]);
+        dq[q] = fmaf(S[q].z, k[4 * q + 2], dq[q]);
+        dq[q] = fmaf(S[q].w, k[4 * q + 3], dq[q]);
       }
-      if (l2norm) {
+      float dot = (dq[0] + dq[1]) + (dq[2] + dq[3]);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) ss = fmaf(k[e], k[e], ss);
-      }
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) {
-        dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
-        if (l2norm) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-      }
-      const float r = l2norm ? rsqrtf(ss + 1e-6f) : 1.0f;
-      const float alpha = expf(reinterpret_cast<const float*>(sb + it.off_g)[t]);
-      const float beta = reinterpret_cast<const float*>(sb + it.off_beta)[t];
+      for (int o = 1; o < 8; o <<= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
       const float v = __uint_as_float(static_cast<uint32_t>(
                                            reinterpret_cast<const uint16_t*>(sb + it.off_v)[t * kSlabRows + row])
                                        << 16);
-      // S k^ after the decay is alpha * r * (S k); the correction is u k^ = (u r) k
-      const float d = alpha * (r * dot);
-      const float ur = beta * (v - d) * r;
+      const float ca = c * tp.x, inv_ca = inv_c * tp.w;
+      const float u = tp.y * (v - ca * (tp.z * dot));
+      const float w = u * tp.z * inv_ca;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        S[q].x = fmaf(ur, k[4 * q], alpha * S[q].x);
-        S[q].y = fmaf(ur, k[4 * q + 1], alpha * S[q].y);
-        S[q].z = fmaf(ur, k[4 * q + 2], alpha * S[q].z);
-        S[q].w = fmaf(ur, k[4 * q + 3], alpha * S[q].w);
+        S[q].x = fmaf(w, k[4 * q], S[q].x);
+        S[q].y = fmaf(w, k[4 * q + 1], S[q].y);
+        S[q].z = fmaf(w, k[4 * q + 2], S[q].z);
+        S[q].w = fmaf(w, k[4 * q + 3], S[q].w);
+      }
+      c = ca;
+      inv_c = inv_ca;
+      if (c < 0x1p-30f) {  // the same in every lane of the item
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          S[q].x *= c;
+          S[q].y *= c;
+          S[q].z *= c;
+          S[q].w *= c;
+        }
+        c = 1.0f;
+        inv_c = 1.0f;
       }
       if (track != nullptr && t == step) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) __stcs(reinterpret_cast<float4*>(track + row * kDK + q * 32 + lc * 4), S[q]);
+        for (int q = 0; q < 4; ++q)
+          __stcs(reinterpret_cast<float4*>(track + row * kDK + q * 32 + lc * 4),
+                 make_float4(c * S[q].x, c * S[q].y, c * S[q].z, c * S[q].w));
       }
     }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) S[q] = make_float4(c * S[q].x, c * S[q].y, c * S[q].z, c * S[q].w);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8u * stage);  // nothing more is read from the slot
 #pragma unroll

@@ -21,11 +21,14 @@ constexpr int kMaxSlots = 16;
 constexpr uint64_t kWaitTimeoutNs = 4000000000ull;
 static_assert(kConsumerWarps * 4 == kSlabRows, "four rows per consumer warp");
 
-// shared memory: [full mbarriers][empty mbarriers] | abort flag | descriptors | arena
+// shared memory: [full mbarriers][empty mbarriers] | abort flag | descriptors |
+// per-consumer-warp token tables (exp(g), beta, 1/|k|, exp(-g) per token) | arena
 constexpr uint32_t kAbortOff = 2 * 8 * kMaxSlots;
 constexpr uint32_t kDescOff = 512;
 constexpr uint32_t kDescBytes = 32;
-constexpr uint32_t kArenaOff = kDescOff + kMaxSlots * kDescBytes;  // 1024
+constexpr uint32_t kTokOff = kDescOff + kMaxSlots * kDescBytes;      // 1024
+constexpr uint32_t kTokBytes = kMaxWindow * 16;                      // one float4 per token
+constexpr uint32_t kArenaOff = kTokOff + kConsumerWarps * kTokBytes;  // 9216
 
 struct alignas(16) Desc {
   unsigned long long slab;   // global address of the slab (read and written in place)
