@@ -302,31 +302,32 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
     // ca = c * exp(g): S k^ after the decay is ca * r * (S k), and the update
     // (u r) k adds (u r / ca) k to S.  Rescaling is exact up to rounding
     // (it scales every term alike); S is renormalised before c gets small.
-    float4 S[4];
+    // this lane's 16 state values as packed pairs: S2[2q], S2[2q+1] = columns
+    // q*32 + lc*4 + {0,1}, {2,3}
+    float2 S2[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      S[q] = *reinterpret_cast<const float4*>(sb + (row * kDK + q * 32 + lc * 4) * 4);
+    for (int q = 0; q < 4; ++q) {
+      const float4 v4 = *reinterpret_cast<const float4*>(sb + (row * kDK + q * 32 + lc * 4) * 4);
+      S2[2 * q] = make_float2(v4.x, v4.y);
+      S2[2 * q + 1] = make_float2(v4.z, v4.w);
+    }
     float c = 1.0f, inv_c = 1.0f;
     for (int t = 0; t < n; ++t) {
       const float4 tp = tok[t];
-      float k[16];
+      float2 k2[8];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint2 w = *reinterpret_cast<const uint2*>(sb + it.off_k + (t * kDK + q * 32 + lc * 4) * 2);
-        k[4 * q] = bf16lo(w.x);
-        k[4 * q + 1] = bf16hi(w.x);
-        k[4 * q + 2] = bf16lo(w.y);
-        k[4 * q + 3] = bf16hi(w.y);
+        k2[2 * q] = make_float2(bf16lo(w.x), bf16hi(w.x));
+        k2[2 * q + 1] = make_float2(bf16lo(w.y), bf16hi(w.y));
       }
-      float dq[4];
+      float2 d0 = __fmul2_rn(S2[0], k2[0]), d1 = __fmul2_rn(S2[1], k2[1]);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        dq[q] = S[q].x * k[4 * q];
-        dq[q] = fmaf(S[q].y, k[4 * q + 1], dq[q]);
-        dq[q] = fmaf(S[q].z, k[4 * q + 2], dq[q]);
-        dq[q] = fmaf(S[q].w, k[4 * q + 3], dq[q]);
+      for (int e = 2; e < 8; e += 2) {
+        d0 = __ffma2_rn(S2[e], k2[e], d0);
+        d1 = __ffma2_rn(S2[e + 1], k2[e + 1], d1);
       }
-      float dot = (dq[0] + dq[1]) + (dq[2] + dq[3]);
+      float dot = (d0.x + d0.y) + (d1.x + d1.y);
 #pragma unroll
       for (int o = 1; o < 8; o <<= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
       const float v = __uint_as_float(static_cast<uint32_t>(
@@ -335,23 +336,15 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
       const float ca = c * tp.x, inv_ca = inv_c * tp.w;
       const float u = tp.y * (v - ca * (tp.z * dot));
       const float w = u * tp.z * inv_ca;
+      const float2 w2 = make_float2(w, w);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        S[q].x = fmaf(w, k[4 * q], S[q].x);
-        S[q].y = fmaf(w, k[4 * q + 1], S[q].y);
-        S[q].z = fmaf(w, k[4 * q + 2], S[q].z);
-        S[q].w = fmaf(w, k[4 * q + 3], S[q].w);
-      }
+      for (int e = 0; e < 8; ++e) S2[e] = __ffma2_rn(w2, k2[e], S2[e]);
       c = ca;
       inv_c = inv_ca;
       if (c < 0x1p-30f) {  // the same in every lane of the item
+        const float2 c2 = make_float2(c, c);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          S[q].x *= c;
-          S[q].y *= c;
-          S[q].z *= c;
-          S[q].w *= c;
-        }
+        for (int e = 0; e < 8; ++e) S2[e] = __fmul2_rn(S2[e], c2);
         c = 1.0f;
         inv_c = 1.0f;
       }
@@ -359,11 +352,13 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           __stcs(reinterpret_cast<float4*>(track + row * kDK + q * 32 + lc * 4),
-                 make_float4(c * S[q].x, c * S[q].y, c * S[q].z, c * S[q].w));
+                 make_float4(c * S2[2 * q].x, c * S2[2 * q].y, c * S2[2 * q + 1].x, c * S2[2 * q + 1].y));
       }
     }
+    float4 S[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) S[q] = make_float4(c * S[q].x, c * S[q].y, c * S[q].z, c * S[q].w);
+    for (int q = 0; q < 4; ++q)
+      S[q] = make_float4(c * S2[2 * q].x, c * S2[2 * q].y, c * S2[2 * q + 1].x, c * S2[2 * q + 1].y);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8u * stage);  // nothing more is read from the slot
 #pragma unroll
