@@ -77,9 +77,9 @@ constexpr size_t kNumInstances = sizeof(kInstances) / sizeof(kInstances[0]);
 // largest dynamic shared memory size already configured per (device, instance),
 // and the occupancy found for the last size queried (so that calls made while
 // a stream is being captured issue no queries)
-int g_smem_set[kMaxDevices][kNumInstances];
-int g_occ_smem[kMaxDevices][kNumInstances];
-int g_occ_blocks[kMaxDevices][kNumInstances];
+int g_smem_set[kMaxDevices][kNumInstances + 2];  // + the two tensor-core variants
+int g_occ_smem[kMaxDevices][kNumInstances + 2];  // + the two tensor-core variants
+int g_occ_blocks[kMaxDevices][kNumInstances + 2];  // + the two tensor-core variants
 
 int device_info(int dev, DeviceInfo* out) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -189,7 +189,11 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   const int sb = elem_bytes(a->state_dtype), ib = elem_bytes(a->input_dtype);
   const int item_min = static_cast<int>(rsm::item_layout(a->dim, a->dstate, sb, quant, ib, 0).bytes);
   const int item_max = static_cast<int>(rsm::item_layout(a->dim, a->dstate, sb, quant, ib, a->max_window).bytes);
-  const int base = static_cast<int>(rsm::arena_base(a->dim, a->dstate, sb));
+  // 16-bit state with bf16 inputs at 64 x 128 and windows of kTcMinWindow or
+  // more: the tensor-core variant (the prefix as an MMA)
+  const bool use_tc = (a->state_dtype == RSM_BF16 || a->state_dtype == RSM_F16) && a->input_dtype == RSM_BF16 &&
+                a->dim == 64 && a->dstate == 128 && a->max_window >= rsm::kTcMinWindow;
+  const int base = static_cast<int>(use_tc ? rsm::kTcArenaBase : rsm::arena_base(a->dim, a->dstate, sb));
   const int two_cta = di.smem_per_sm / 2 - di.smem_reserved - base;
   const int one_cta = di.smem_optin - base;
   const bool two = two_cta >= 2 * item_max;
@@ -203,24 +207,31 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   if (stages > kSlotsPerSm / (two ? 2 : 1)) stages = kSlotsPerSm / (two ? 2 : 1);
   const int smem = base + arena;
 
-  const void* fn = kInstances[inst].kernel();
+  const void* fn = use_tc ? (a->state_dtype == RSM_BF16 ? rsm::kernel_for_tc<RSM_BF16>() : rsm::kernel_for_tc<RSM_F16>())
+                          : kInstances[inst].kernel();
+  const int ci = use_tc ? static_cast<int>(kNumInstances) + (a->state_dtype == RSM_F16 ? 1 : 0) : inst;
   int per_sm = 0;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_smem_set[dev][inst] < smem) {
+    if (g_smem_set[dev][ci] < smem) {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return fail(RSM_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-      g_smem_set[dev][inst] = smem;
+      g_smem_set[dev][ci] = smem;
     }
-    if (g_occ_smem[dev][inst] == smem) {
-      per_sm = g_occ_blocks[dev][inst];
+    if (g_occ_smem[dev][ci] == smem) {
+      per_sm = g_occ_blocks[dev][ci];
     } else {
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, rsm::kThreads, smem);
       if (e != cudaSuccess) return fail(RSM_ECUDA, "occupancy query: %s", cudaGetErrorString(e));
-      g_occ_smem[dev][inst] = smem;
-      g_occ_blocks[dev][inst] = per_sm;
+      g_occ_smem[dev][ci] = smem;
+      g_occ_blocks[dev][ci] = per_sm;
     }
   }
+  // The occupancy query reports one CTA per SM for the tensor-core kernel
+  // although its shared memory, registers and threads fit two; on GB300 two
+  // run side by side (each allocates 64 of the SM's 512 TMEM columns).  Were
+  // they not co-scheduled, the persistent grid would only take a second wave.
+  if (use_tc && two && per_sm < 2) per_sm = 2;
   if (per_sm < 1) return fail(RSM_ENOTSUP, "kernel does not fit on an SM with %d bytes of shared memory", smem);
 
   rsm::Params& p = L->params;
@@ -250,7 +261,8 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   p.R = a->ring_buffer_len;
   p.pad = a->pad_slot_id;
   p.philox_rounds = a->philox_rounds;
-  p.desc0 = rsm::desc_base(a->dim, a->dstate, sb);
+  p.tc_min_k = rsm::kTcMinK;
+  p.desc0 = use_tc ? rsm::kTcDescBase : rsm::desc_base(a->dim, a->dstate, sb);
   p.arena0 = static_cast<uint32_t>(base);
   p.arena_bytes = static_cast<uint32_t>(arena);
   p.stages = static_cast<uint32_t>(stages);

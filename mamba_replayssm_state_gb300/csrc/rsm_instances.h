@@ -20,4 +20,7 @@ namespace rsm {
 // Defined (explicitly instantiated) in the rsm_inst_*.cu translation units.
 template <int SF, int IF, int D, int N>
 const void* kernel_for();
+// The tensor-core long-window variant (rsm_inst_tc.cu): 16-bit state, bf16 inputs, 64 x 128.
+template <int SF>
+const void* kernel_for_tc();
 }  // namespace rsm

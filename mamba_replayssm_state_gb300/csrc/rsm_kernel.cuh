@@ -460,6 +460,245 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
 // ---------------------------------------------------------------------------
 // consumer warps
 // ---------------------------------------------------------------------------
+// One item with a non-empty prefix on the CUDA cores: the decay scan, the
+// prefix applied to this thread's [RPT rows x VEC columns] of the tile in
+// closed form (the tokens converted kTokChunk at a time into the warp's fp32
+// buffer `cbuf`), requantization and the store.  The slot is released (empty
+// barrier) as soon as the warp holds all it still needs.
+template <int SF, int IF, int D, int N>
+__device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char* sb, const ItemLayout& il,
+                                            const ItemDesc* desc, int k, float* wbuf, float* cbuf, int cw, int lane,
+                                            uint32_t empty_bar, uint32_t key0, uint32_t key1, bool sr) {
+  constexpr int ES = Fmt<SF>::bytes;
+  constexpr int IE = In<IF>::bytes;
+  constexpr bool Q = Fmt<SF>::quant;
+  constexpr ThreadLayout TL = thread_layout(D, N, ES);
+  constexpr int VEC = TL.vec, LPR = TL.lpr, CT = TL.ct, SLAB_ROWS = TL.slab_rows, RPT = TL.rpt, COLS = TL.cols;
+  constexpr int V2 = VEC / 2;
+  using Raw = typename Vec<SF>::Raw;
+  constexpr int VB = Vec<SF>::BYTES;
+  constexpr int XW = SLAB_ROWS % 4 == 0 ? 4 : (SLAB_ROWS % 2 == 0 ? 2 : 1);
+  float* bbuf = cbuf + kTokChunk * SLAB_ROWS;
+  const int lane_row = lane / LPR, lane_col = lane % LPR;
+  const int slab_row0 = (cw / CT) * SLAB_ROWS;
+  const int tile_col0 = (cw % CT) * COLS;
+  const int rrow = lane_row * RPT;
+  const int row0 = slab_row0 + rrow;
+  const int ccol = lane_col * VEC;
+  const int col0 = tile_col0 + ccol;
+  const bool worker = rrow < SLAB_ROWS;
+  (void)ccol;
+  const uint32_t flags = desc->flags;
+  unsigned char* dst_tile = reinterpret_cast<unsigned char*>(desc->dst_state);
+  float* dst_sc = reinterpret_cast<float*>(desc->dst_scale);
+  const bool dst_aligned = (flags & kFlagDstAligned) != 0u;
+  const int h = desc->head;
+  const uint32_t dst_slot_id = static_cast<uint32_t>(desc->dst_slot);
+  const uint32_t layer_id = static_cast<uint32_t>(desc->layer);
+  auto release = [&]() {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar);
+  };
+    // decay of each token, once per warp: a_t = exp(dt_t*A), then
+    // w_t = dt_t * prod_{s>t} a_s and P = prod_t a_t by a suffix-product scan
+    const float A = desc->A;
+    const float* dts = reinterpret_cast<const float*>(sb + il.off_dt);
+    float carry = 1.0f;
+    for (int c = (k - 1) >> 5; c >= 0; --c) {
+      const int t = 32 * c + lane;
+      const float dtv = t < k ? dts[t] : 0.0f;
+      const float a = t < k ? expf(dtv * A) : 1.0f;
+      float incl = a;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float v = __shfl_down_sync(0xFFFFFFFFu, incl, off);
+        if (lane + off < 32) incl *= v;
+      }
+      float excl = __shfl_down_sync(0xFFFFFFFFu, incl, 1);
+      if (lane == 31) excl = 1.0f;
+      if (t < k) wbuf[t] = dtv * (excl * carry);
+      carry *= __shfl_sync(0xFFFFFFFFu, incl, 0);
+    }
+    const float P = carry;  // identical in every lane
+
+    // this thread's [RPT rows x VEC columns] of the tile, dequantized, times P
+    float2 acc[RPT][V2];
+    if (worker) {
+      const float2 P2 = make_float2(P, P);
+#pragma unroll
+      for (int r = 0; r < RPT; ++r) {
+        const Raw raw = *reinterpret_cast<const Raw*>(sb + ((row0 + r) * N + col0) * ES);
+        unpack_vec<SF>(raw, acc[r]);
+        if constexpr (Q) {
+          // code * (scale * P): the row's scale folded into the decay product
+          const float sp = reinterpret_cast<const float*>(sb + il.off_scale)[row0 + r] * P;
+          const float2 sp2 = make_float2(sp, sp);
+#pragma unroll
+          for (int u = 0; u < V2; ++u) acc[r][u] = __fmul2_rn(acc[r][u], sp2);
+        } else {
+#pragma unroll
+          for (int u = 0; u < V2; ++u) acc[r][u] = __fmul2_rn(acc[r][u], P2);
+        }
+      }
+    }
+    __syncwarp();  // wbuf visible to the whole warp
+
+    // the prefix, kTokChunk tokens at a time: convert this warp's share of
+    // the tokens to fp32 (c = w*x for its rows, B for its columns), then one
+    // rank-1 update per token with packed fp32x2 FMAs
+    const unsigned char* xs = sb + il.off_x;
+    const unsigned char* Bs = sb + il.off_B;
+    for (int t0 = 0; t0 < k; t0 += kTokChunk) {
+      const int tn = min(kTokChunk, k - t0);
+      for (int u = lane; u < tn * (SLAB_ROWS / XW); u += 32) {
+        const int t = u / (SLAB_ROWS / XW), rx = (u % (SLAB_ROWS / XW)) * XW;
+        float xv[XW];
+        load_inputs<IF, XW>(xs + ((t0 + t) * D + slab_row0 + rx) * IE, xv);
+        const float wt = wbuf[t0 + t];
+        float* dst = cbuf + t * SLAB_ROWS + rx;
+        if constexpr (XW == 4) {
+          *reinterpret_cast<float4*>(dst) = make_float4(xv[0] * wt, xv[1] * wt, xv[2] * wt, xv[3] * wt);
+        } else if constexpr (XW == 2) {
+          *reinterpret_cast<float2*>(dst) = make_float2(xv[0] * wt, xv[1] * wt);
+        } else {
+          dst[0] = xv[0] * wt;
+        }
+      }
+      for (int u = lane; u < tn * (COLS / 8); u += 32) {
+        const int t = u / (COLS / 8), j8 = (u % (COLS / 8)) * 8;
+        float bv[8];
+        load_inputs<IF, 8>(Bs + ((t0 + t) * N + tile_col0 + j8) * IE, bv);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int j = j8 + 4 * h, lc = j / VEC, o = j % VEC;  // o is a multiple of 4
+          *reinterpret_cast<float4*>(bbuf + t * COLS + (o / 4) * (LPR * 4) + lc * 4) =
+              make_float4(bv[4 * h], bv[4 * h + 1], bv[4 * h + 2], bv[4 * h + 3]);
+        }
+      }
+      __syncwarp();
+      if (t0 + kTokChunk >= k) release();  // the last chunk: nothing more is read from the stage
+      if (worker) {
+#pragma unroll 2
+        for (int t = 0; t < tn; ++t) {
+          float c[RPT];
+          float2 b2[V2];
+          if constexpr (RPT % 4 == 0) {
+#pragma unroll
+            for (int r = 0; r < RPT; r += 4) {
+              const float4 v = *reinterpret_cast<const float4*>(cbuf + t * SLAB_ROWS + rrow + r);
+              c[r] = v.x;
+              c[r + 1] = v.y;
+              c[r + 2] = v.z;
+              c[r + 3] = v.w;
+            }
+          } else if constexpr (RPT % 2 == 0) {
+#pragma unroll
+            for (int r = 0; r < RPT; r += 2) {
+              const float2 v = *reinterpret_cast<const float2*>(cbuf + t * SLAB_ROWS + rrow + r);
+              c[r] = v.x;
+              c[r + 1] = v.y;
+            }
+          } else {
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) c[r] = cbuf[t * SLAB_ROWS + rrow + r];
+          }
+#pragma unroll
+          for (int g = 0; g < VEC / 4; ++g) {
+            const float4 v = *reinterpret_cast<const float4*>(bbuf + t * COLS + g * (LPR * 4) + lane_col * 4);
+            b2[2 * g] = make_float2(v.x, v.y);
+            b2[2 * g + 1] = make_float2(v.z, v.w);
+          }
+#pragma unroll
+          for (int r = 0; r < RPT; ++r) {
+            const float2 c2 = make_float2(c[r], c[r]);
+#pragma unroll
+            for (int u = 0; u < V2; ++u) acc[r][u] = __ffma2_rn(c2, b2[u], acc[r][u]);
+          }
+        }
+      }
+      __syncwarp();  // the chunk buffer is rewritten by the next chunk
+    }
+
+    // requantize + store
+    float scale_own = 0.0f;  // one-byte formats: the scale of row row0 + lane_col (lanes lane_col < RPT)
+    if constexpr (Q) {
+      // symmetric per-(head, row) scale: amax by a butterfly over the LPR lanes
+      // of each row; then each row's scale and inverse are divided once, by
+      // the row's lane lane_col == r, and the inverse is shuffled to the rest
+      static_assert(RPT <= LPR, "one lane per row for the scale division");
+      float amax[RPT];
+#pragma unroll
+      for (int r = 0; r < RPT; ++r) {
+        amax[r] = 0.0f;
+#pragma unroll
+        for (int u = 0; u < V2; ++u) amax[r] = fmaxf(amax[r], fmaxf(fabsf(acc[r][u].x), fabsf(acc[r][u].y)));
+      }
+#pragma unroll
+      for (int off = LPR / 2; off >= 1; off >>= 1) {
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xFFFFFFFFu, amax[r], off));
+      }
+      float am = amax[0];
+#pragma unroll
+      for (int r = 1; r < RPT; ++r) am = lane_col == r ? amax[r] : am;
+      constexpr float qmax = SF == RSM_I8 ? 127.0f : 448.0f;
+      const float inv_own = __fdiv_rn(qmax, am);
+      scale_own = inv_own <= FLT_MAX ? __fdiv_rn(am, qmax) : 0.0f;
+      const int row_lane0 = lane & ~(LPR - 1);
+#pragma unroll
+      for (int r = 0; r < RPT; ++r) {
+        const float inv = __shfl_sync(0xFFFFFFFFu, inv_own, row_lane0 + r);
+        // a row whose qmax/amax is not finite (amax == 0 or tiny) becomes zero codes
+        const bool zero_row = !(inv <= FLT_MAX);
+        const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+        for (int u = 0; u < V2; ++u) acc[r][u] = zero_row ? make_float2(0.0f, 0.0f) : __fmul2_rn(acc[r][u], inv2);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+      if (!worker) continue;
+      Raw out;
+      bool use_sr = false;
+      if constexpr (SF != RSM_F32) use_sr = sr;
+      if (use_sr) {
+        // one Philox block per 4 consecutive elements; round, then pack exactly
+        const int64_t e0 = (static_cast<int64_t>(h) * D + row0 + r) * N + col0;
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+          const uint4 rnd = philox4x32(
+              make_uint4(static_cast<uint32_t>((e0 >> 2) + q), dst_slot_id, layer_id, 0u), key0, key1,
+              p.philox_rounds);
+          acc[r][2 * q] = make_float2(sr_fmt<SF>(acc[r][2 * q].x, rnd.x), sr_fmt<SF>(acc[r][2 * q].y, rnd.y));
+          acc[r][2 * q + 1] =
+              make_float2(sr_fmt<SF>(acc[r][2 * q + 1].x, rnd.z), sr_fmt<SF>(acc[r][2 * q + 1].y, rnd.w));
+        }
+        out = pack_vec_rne<SF>(acc[r]);
+      } else {
+        out = pack_vec_rne<SF>(acc[r]);
+      }
+      const uint32_t off = ((row0 + r) * N + col0) * ES;
+      if (dst_aligned) {
+        stg_stream(dst_tile + off, out);
+      } else {
+        const unsigned char* ob = reinterpret_cast<const unsigned char*>(&out);
+#pragma unroll
+        for (int q = 0; q < VB; ++q) dst_tile[off + q] = ob[q];
+      }
+    }
+    if constexpr (Q) {
+      if (lane_col < RPT) {
+        if (flags & kFlagScaleAligned) {
+          dst_sc[row0 + lane_col] = scale_own;
+        } else {
+          const unsigned char* vb = reinterpret_cast<const unsigned char*>(&scale_own);
+          unsigned char* db = reinterpret_cast<unsigned char*>(dst_sc + row0 + lane_col);
+          for (int q = 0; q < 4; ++q) db[q] = vb[q];
+        }
+      }
+    }
+}
+
 template <int SF, int IF, int D, int N>
 __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* smem, int cw, int lane) {
   constexpr int ES = Fmt<SF>::bytes;
@@ -467,7 +706,6 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
   constexpr bool Q = Fmt<SF>::quant;
   constexpr ThreadLayout TL = thread_layout(D, N, ES);
   constexpr int VEC = TL.vec, LPR = TL.lpr, CT = TL.ct, SLAB_ROWS = TL.slab_rows, RPT = TL.rpt, COLS = TL.cols;
-  constexpr int V2 = VEC / 2;
   static_assert(VEC == Vec<SF>::N && VEC % 2 == 0, "vector width");
   using Raw = typename Vec<SF>::Raw;
   constexpr int VB = Vec<SF>::BYTES;  // bytes per vector
@@ -475,7 +713,6 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
   static_assert(SLAB_ROWS % TL.rpw == 0 || SLAB_ROWS < TL.rpw, "rows must split evenly");
   static_assert(!Q || SLAB_ROWS >= TL.rpw, "one-byte formats need every consumer lane busy");
   static_assert(COLS % 8 == 0, "token-chunk buffer vectors");
-  constexpr int XW = SLAB_ROWS % 4 == 0 ? 4 : (SLAB_ROWS % 2 == 0 ? 2 : 1);  // rows per c-conversion unit
 
   const uint32_t full0 = smem_addr(smem);
   const uint32_t empty0 = full0 + 8u * kMaxStages;
@@ -486,7 +723,6 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
   // lane: column o of lane column lc sits at t*COLS + (o/4)*LPR*4 + lc*4 + o%4,
   // so that the eight lanes of a quarter-warp read 128 contiguous bytes.
   float* cbuf = reinterpret_cast<float*>(smem + kWarpBufOff) + cw * warp_buf_floats(D, N, ES);
-  float* bbuf = cbuf + kTokChunk * SLAB_ROWS;
   static_assert(VEC % 4 == 0, "B chunk groups");
 
   const int lane_row = lane / LPR, lane_col = lane % LPR;
@@ -530,9 +766,6 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
     unsigned char* dst_tile = reinterpret_cast<unsigned char*>(desc->dst_state);
     float* dst_sc = reinterpret_cast<float*>(desc->dst_scale);
     const bool dst_aligned = (flags & kFlagDstAligned) != 0u;
-    const int h = desc->head;
-    const uint32_t dst_slot_id = static_cast<uint32_t>(desc->dst_slot);
-    const uint32_t layer_id = static_cast<uint32_t>(desc->layer);
     // A warp releases the stage as soon as it holds all it still needs (in
     // registers or in its private chunk buffer), so that the loader refills it
     // while this warp computes and stores.
@@ -581,204 +814,7 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
         }
       }
     } else {
-      // decay of each token, once per warp: a_t = exp(dt_t*A), then
-      // w_t = dt_t * prod_{s>t} a_s and P = prod_t a_t by a suffix-product scan
-      const float A = desc->A;
-      const float* dts = reinterpret_cast<const float*>(sb + il.off_dt);
-      float carry = 1.0f;
-      for (int c = (k - 1) >> 5; c >= 0; --c) {
-        const int t = 32 * c + lane;
-        const float dtv = t < k ? dts[t] : 0.0f;
-        const float a = t < k ? expf(dtv * A) : 1.0f;
-        float incl = a;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const float v = __shfl_down_sync(0xFFFFFFFFu, incl, off);
-          if (lane + off < 32) incl *= v;
-        }
-        float excl = __shfl_down_sync(0xFFFFFFFFu, incl, 1);
-        if (lane == 31) excl = 1.0f;
-        if (t < k) wbuf[t] = dtv * (excl * carry);
-        carry *= __shfl_sync(0xFFFFFFFFu, incl, 0);
-      }
-      const float P = carry;  // identical in every lane
-
-      // this thread's [RPT rows x VEC columns] of the tile, dequantized, times P
-      float2 acc[RPT][V2];
-      if (worker) {
-        const float2 P2 = make_float2(P, P);
-#pragma unroll
-        for (int r = 0; r < RPT; ++r) {
-          const Raw raw = *reinterpret_cast<const Raw*>(sb + ((row0 + r) * N + col0) * ES);
-          unpack_vec<SF>(raw, acc[r]);
-          if constexpr (Q) {
-            // code * (scale * P): the row's scale folded into the decay product
-            const float sp = reinterpret_cast<const float*>(sb + il.off_scale)[row0 + r] * P;
-            const float2 sp2 = make_float2(sp, sp);
-#pragma unroll
-            for (int u = 0; u < V2; ++u) acc[r][u] = __fmul2_rn(acc[r][u], sp2);
-          } else {
-#pragma unroll
-            for (int u = 0; u < V2; ++u) acc[r][u] = __fmul2_rn(acc[r][u], P2);
-          }
-        }
-      }
-      __syncwarp();  // wbuf visible to the whole warp
-
-      // the prefix, kTokChunk tokens at a time: convert this warp's share of
-      // the tokens to fp32 (c = w*x for its rows, B for its columns), then one
-      // rank-1 update per token with packed fp32x2 FMAs
-      const unsigned char* xs = sb + il.off_x;
-      const unsigned char* Bs = sb + il.off_B;
-      for (int t0 = 0; t0 < k; t0 += kTokChunk) {
-        const int tn = min(kTokChunk, k - t0);
-        for (int u = lane; u < tn * (SLAB_ROWS / XW); u += 32) {
-          const int t = u / (SLAB_ROWS / XW), rx = (u % (SLAB_ROWS / XW)) * XW;
-          float xv[XW];
-          load_inputs<IF, XW>(xs + ((t0 + t) * D + slab_row0 + rx) * IE, xv);
-          const float wt = wbuf[t0 + t];
-          float* dst = cbuf + t * SLAB_ROWS + rx;
-          if constexpr (XW == 4) {
-            *reinterpret_cast<float4*>(dst) = make_float4(xv[0] * wt, xv[1] * wt, xv[2] * wt, xv[3] * wt);
-          } else if constexpr (XW == 2) {
-            *reinterpret_cast<float2*>(dst) = make_float2(xv[0] * wt, xv[1] * wt);
-          } else {
-            dst[0] = xv[0] * wt;
-          }
-        }
-        for (int u = lane; u < tn * (COLS / 8); u += 32) {
-          const int t = u / (COLS / 8), j8 = (u % (COLS / 8)) * 8;
-          float bv[8];
-          load_inputs<IF, 8>(Bs + ((t0 + t) * N + tile_col0 + j8) * IE, bv);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int j = j8 + 4 * h, lc = j / VEC, o = j % VEC;  // o is a multiple of 4
-            *reinterpret_cast<float4*>(bbuf + t * COLS + (o / 4) * (LPR * 4) + lc * 4) =
-                make_float4(bv[4 * h], bv[4 * h + 1], bv[4 * h + 2], bv[4 * h + 3]);
-          }
-        }
-        __syncwarp();
-        if (t0 + kTokChunk >= k) release();  // the last chunk: nothing more is read from the stage
-        if (worker) {
-#pragma unroll 2
-          for (int t = 0; t < tn; ++t) {
-            float c[RPT];
-            float2 b2[V2];
-            if constexpr (RPT % 4 == 0) {
-#pragma unroll
-              for (int r = 0; r < RPT; r += 4) {
-                const float4 v = *reinterpret_cast<const float4*>(cbuf + t * SLAB_ROWS + rrow + r);
-                c[r] = v.x;
-                c[r + 1] = v.y;
-                c[r + 2] = v.z;
-                c[r + 3] = v.w;
-              }
-            } else if constexpr (RPT % 2 == 0) {
-#pragma unroll
-              for (int r = 0; r < RPT; r += 2) {
-                const float2 v = *reinterpret_cast<const float2*>(cbuf + t * SLAB_ROWS + rrow + r);
-                c[r] = v.x;
-                c[r + 1] = v.y;
-              }
-            } else {
-#pragma unroll
-              for (int r = 0; r < RPT; ++r) c[r] = cbuf[t * SLAB_ROWS + rrow + r];
-            }
-#pragma unroll
-            for (int g = 0; g < VEC / 4; ++g) {
-              const float4 v = *reinterpret_cast<const float4*>(bbuf + t * COLS + g * (LPR * 4) + lane_col * 4);
-              b2[2 * g] = make_float2(v.x, v.y);
-              b2[2 * g + 1] = make_float2(v.z, v.w);
-            }
-#pragma unroll
-            for (int r = 0; r < RPT; ++r) {
-              const float2 c2 = make_float2(c[r], c[r]);
-#pragma unroll
-              for (int u = 0; u < V2; ++u) acc[r][u] = __ffma2_rn(c2, b2[u], acc[r][u]);
-            }
-          }
-        }
-        __syncwarp();  // the chunk buffer is rewritten by the next chunk
-      }
-
-      // requantize + store
-      float scale_own = 0.0f;  // one-byte formats: the scale of row row0 + lane_col (lanes lane_col < RPT)
-      if constexpr (Q) {
-        // symmetric per-(head, row) scale: amax by a butterfly over the LPR lanes
-        // of each row; then each row's scale and inverse are divided once, by
-        // the row's lane lane_col == r, and the inverse is shuffled to the rest
-        static_assert(RPT <= LPR, "one lane per row for the scale division");
-        float amax[RPT];
-#pragma unroll
-        for (int r = 0; r < RPT; ++r) {
-          amax[r] = 0.0f;
-#pragma unroll
-          for (int u = 0; u < V2; ++u) amax[r] = fmaxf(amax[r], fmaxf(fabsf(acc[r][u].x), fabsf(acc[r][u].y)));
-        }
-#pragma unroll
-        for (int off = LPR / 2; off >= 1; off >>= 1) {
-#pragma unroll
-          for (int r = 0; r < RPT; ++r) amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xFFFFFFFFu, amax[r], off));
-        }
-        float am = amax[0];
-#pragma unroll
-        for (int r = 1; r < RPT; ++r) am = lane_col == r ? amax[r] : am;
-        constexpr float qmax = SF == RSM_I8 ? 127.0f : 448.0f;
-        const float inv_own = __fdiv_rn(qmax, am);
-        scale_own = inv_own <= FLT_MAX ? __fdiv_rn(am, qmax) : 0.0f;
-        const int row_lane0 = lane & ~(LPR - 1);
-#pragma unroll
-        for (int r = 0; r < RPT; ++r) {
-          const float inv = __shfl_sync(0xFFFFFFFFu, inv_own, row_lane0 + r);
-          // a row whose qmax/amax is not finite (amax == 0 or tiny) becomes zero codes
-          const bool zero_row = !(inv <= FLT_MAX);
-          const float2 inv2 = make_float2(inv, inv);
-#pragma unroll
-          for (int u = 0; u < V2; ++u) acc[r][u] = zero_row ? make_float2(0.0f, 0.0f) : __fmul2_rn(acc[r][u], inv2);
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < RPT; ++r) {
-        if (!worker) continue;
-        Raw out;
-        bool use_sr = false;
-        if constexpr (SF != RSM_F32) use_sr = sr;
-        if (use_sr) {
-          // one Philox block per 4 consecutive elements; round, then pack exactly
-          const int64_t e0 = (static_cast<int64_t>(h) * D + row0 + r) * N + col0;
-#pragma unroll
-          for (int q = 0; q < VEC / 4; ++q) {
-            const uint4 rnd = philox4x32(
-                make_uint4(static_cast<uint32_t>((e0 >> 2) + q), dst_slot_id, layer_id, 0u), key0, key1,
-                p.philox_rounds);
-            acc[r][2 * q] = make_float2(sr_fmt<SF>(acc[r][2 * q].x, rnd.x), sr_fmt<SF>(acc[r][2 * q].y, rnd.y));
-            acc[r][2 * q + 1] =
-                make_float2(sr_fmt<SF>(acc[r][2 * q + 1].x, rnd.z), sr_fmt<SF>(acc[r][2 * q + 1].y, rnd.w));
-          }
-          out = pack_vec_rne<SF>(acc[r]);
-        } else {
-          out = pack_vec_rne<SF>(acc[r]);
-        }
-        const uint32_t off = ((row0 + r) * N + col0) * ES;
-        if (dst_aligned) {
-          stg_stream(dst_tile + off, out);
-        } else {
-          const unsigned char* ob = reinterpret_cast<const unsigned char*>(&out);
-#pragma unroll
-          for (int q = 0; q < VB; ++q) dst_tile[off + q] = ob[q];
-        }
-      }
-      if constexpr (Q) {
-        if (lane_col < RPT) {
-          if (flags & kFlagScaleAligned) {
-            dst_sc[row0 + lane_col] = scale_own;
-          } else {
-            const unsigned char* vb = reinterpret_cast<const unsigned char*>(&scale_own);
-            unsigned char* db = reinterpret_cast<unsigned char*>(dst_sc + row0 + lane_col);
-            for (int q = 0; q < 4; ++q) db[q] = vb[q];
-          }
-        }
-      }
+      replay_ffma<SF, IF, D, N>(p, sb, il, desc, k, wbuf, cbuf, cw, lane, empty_bar, key0, key1, sr);
     }
     if (++stage == p.stages) {
       stage = 0;
