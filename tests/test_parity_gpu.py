@@ -327,3 +327,38 @@ def test_headline_full_size_sampled():
             compare_slot(got, ref, "bf16", where=f"layer {l} request {b}")
     del dw
     torch.cuda.empty_cache()
+
+
+# ----------------------------------------------------------------------------
+# long windows: the tensor-core path (16-bit state, bf16 inputs, 64 x 128,
+# windows of 16 or more; prefixes of 10 tokens or more go through the MMA)
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("sd", ["bf16", "f16"])
+@pytest.mark.parametrize("k", [9, 10, 15, 17, 31, 33, 63])
+def test_tensor_core_prefix_lengths(sd, k):
+    shape = wl.Shape("tc", L=2, Bt=4, H=8, hpg=4, D=64, N=128, R=64, W=64, state_dtype=sd, n_active=4,
+                     ring_start=(0, 64), prefix=("fixed", k))
+    hw = wl.host_world(shape, seed=300 + k)
+    check(hw)
+
+
+def test_tensor_core_misaligned_destination():
+    """Destination tiles 2 bytes off a 16-byte boundary: the staged tile is
+    written with byte stores."""
+    shape = wl.Shape("tcmis", L=1, Bt=3, H=4, hpg=2, D=64, N=128, R=64, W=64, state_dtype="f16", n_active=3,
+                     ring_start=(0, 64), prefix=("uniform", 10, 64))
+    hw = wl.host_world(shape, seed=24)
+    hw.state[0] = _offset_copy(hw.state[0], 1)
+    dw = wl.device_world_from_host(hw)
+    buf = torch.zeros(hw.state[0].size + 1, dtype=torch.float16, device="cuda")
+    view = buf[1:].view(hw.state[0].shape)
+    view.copy_(torch.from_numpy(hw.state[0]))
+    dw.state[0] = view
+    dw.tables = wl._tables(dw.state, dw.scale, dw.x, dw.B, dw.dt, dw.A, "cuda")
+    assert dw.state[0].data_ptr() % 16 == 2
+    rsm.replayssm_materialize(**dw.call_kwargs())
+    torch.cuda.synchronize()
+    got = hw.copy()
+    got.state = [wl._to_np(t).view(a.dtype) for t, a in zip(dw.state, hw.state)]
+    compare_worlds(got, run_oracle(hw), hw)
