@@ -68,7 +68,24 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
 // Philox-4x32 (Salmon, Moraes, Dror, Shaw, SC'11, section 5.2)
 // ---------------------------------------------------------------------------
 
+// R rounds, unrolled (the key schedule folds into constants)
+template <int R>
+__device__ __forceinline__ uint4 philox4x32_r(uint4 c, uint32_t k0, uint32_t k1) {
+  constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
+  constexpr uint32_t kWeylA = 0x9E3779B9u, kWeylB = 0xBB67AE85u;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    // one 32x32 -> 64-bit multiply gives both halves of each product
+    const uint64_t pA = static_cast<uint64_t>(kMulA) * c.x;
+    const uint64_t pB = static_cast<uint64_t>(kMulB) * c.z;
+    c = make_uint4(static_cast<uint32_t>(pB >> 32) ^ c.y ^ (k0 + r * kWeylA), static_cast<uint32_t>(pB),
+                   static_cast<uint32_t>(pA >> 32) ^ c.w ^ (k1 + r * kWeylB), static_cast<uint32_t>(pA));
+  }
+  return c;
+}
+
 __device__ __forceinline__ uint4 philox4x32(uint4 c, uint32_t k0, uint32_t k1, int rounds) {
+  if (rounds == 10) return philox4x32_r<10>(c, k0, k1);  // the usual round count, unrolled
   constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
   constexpr uint32_t kWeylA = 0x9E3779B9u, kWeylB = 0xBB67AE85u;
   for (int r = 0; r < rounds; ++r) {
@@ -76,7 +93,6 @@ __device__ __forceinline__ uint4 philox4x32(uint4 c, uint32_t k0, uint32_t k1, i
       k0 += kWeylA;
       k1 += kWeylB;
     }
-    // one 32x32 -> 64-bit multiply gives both halves of each product
     const uint64_t pA = static_cast<uint64_t>(kMulA) * c.x;
     const uint64_t pB = static_cast<uint64_t>(kMulB) * c.z;
     c = make_uint4(static_cast<uint32_t>(pB >> 32) ^ c.y ^ k0, static_cast<uint32_t>(pB),
@@ -95,6 +111,18 @@ __device__ __forceinline__ float sr_round(float y, uint32_t word, float maxfin) 
   const uint32_t bits = __float_as_uint(y);
   const uint32_t sign = bits & 0x80000000u;
   const uint32_t ab = bits ^ sign;
+  {
+    // Common case: a normal input whose grid spacing leaves 0 < d < 24 low
+    // bits.  Adding the complement of the d-bit random number r carries into
+    // the next grid point exactly when r < the discarded bits (the rule
+    // below), so the sum truncated to the grid is the rounded value.
+    const int eb = static_cast<int>(ab >> 23);
+    const int d = INTEGER ? 150 - eb : 23 - MANT;
+    if (eb >= (INTEGER ? 127 : EMIN + 127) && eb < 255 && d > 0 && d < 24) {
+      const uint32_t r = (ab + ((~word) >> (32 - d))) & ~((1u << d) - 1u);
+      return __uint_as_float(min(r, __float_as_uint(maxfin)) | sign);
+    }
+  }
   if (ab == 0u) return y;
   if (ab >= 0x7F800000u) return ab == 0x7F800000u ? __uint_as_float(__float_as_uint(maxfin) | sign) : y;
   const int eb = static_cast<int>(ab >> 23);

@@ -460,6 +460,24 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
 // ---------------------------------------------------------------------------
 // consumer warps
 // ---------------------------------------------------------------------------
+// Stochastic rounding of 8 consecutive elements (two Philox blocks, counter
+// (e/4, dst_slot, layer, 0) with e the first element's index), then the exact
+// pack.  Kept out of line, so that the code of the rounding-to-nearest path,
+// which every call without Philox runs, stays compact.
+template <int SF>
+__device__ __noinline__ typename Vec<SF>::Raw sr_pack8(float2 a0, float2 a1, float2 a2, float2 a3, uint32_t blk,
+                                                       uint32_t slot, uint32_t layer, uint32_t key0, uint32_t key1,
+                                                       int rounds) {
+  const uint4 r0 = philox4x32(make_uint4(blk, slot, layer, 0u), key0, key1, rounds);
+  const uint4 r1 = philox4x32(make_uint4(blk + 1u, slot, layer, 0u), key0, key1, rounds);
+  float2 v[4];
+  v[0] = make_float2(sr_fmt<SF>(a0.x, r0.x), sr_fmt<SF>(a0.y, r0.y));
+  v[1] = make_float2(sr_fmt<SF>(a1.x, r0.z), sr_fmt<SF>(a1.y, r0.w));
+  v[2] = make_float2(sr_fmt<SF>(a2.x, r1.x), sr_fmt<SF>(a2.y, r1.y));
+  v[3] = make_float2(sr_fmt<SF>(a3.x, r1.z), sr_fmt<SF>(a3.y, r1.w));
+  return pack_vec_rne<SF>(v);
+}
+
 // One item with a non-empty prefix on the CUDA cores: the decay scan, the
 // prefix applied to this thread's [RPT rows x VEC columns] of the tile in
 // closed form (the tokens converted kTokChunk at a time into the warp's fp32
@@ -662,18 +680,12 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
       bool use_sr = false;
       if constexpr (SF != RSM_F32) use_sr = sr;
       if (use_sr) {
-        // one Philox block per 4 consecutive elements; round, then pack exactly
-        const int64_t e0 = (static_cast<int64_t>(h) * D + row0 + r) * N + col0;
-#pragma unroll
-        for (int q = 0; q < VEC / 4; ++q) {
-          const uint4 rnd = philox4x32(
-              make_uint4(static_cast<uint32_t>((e0 >> 2) + q), dst_slot_id, layer_id, 0u), key0, key1,
-              p.philox_rounds);
-          acc[r][2 * q] = make_float2(sr_fmt<SF>(acc[r][2 * q].x, rnd.x), sr_fmt<SF>(acc[r][2 * q].y, rnd.y));
-          acc[r][2 * q + 1] =
-              make_float2(sr_fmt<SF>(acc[r][2 * q + 1].x, rnd.z), sr_fmt<SF>(acc[r][2 * q + 1].y, rnd.w));
+        if constexpr (SF != RSM_F32) {
+          static_assert(V2 == 4, "stochastic rounding works on 8-element vectors");
+          const int64_t e0 = (static_cast<int64_t>(h) * D + row0 + r) * N + col0;
+          out = sr_pack8<SF>(acc[r][0], acc[r][1], acc[r][2], acc[r][3], static_cast<uint32_t>(e0 >> 2), dst_slot_id,
+                             layer_id, key0, key1, p.philox_rounds);
         }
-        out = pack_vec_rne<SF>(acc[r]);
       } else {
         out = pack_vec_rne<SF>(acc[r]);
       }
