@@ -460,6 +460,17 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
 // ---------------------------------------------------------------------------
 // consumer warps
 // ---------------------------------------------------------------------------
+// Byte-wise store of a vector to a destination that is not 16-byte aligned
+// (out of line: the aligned path is the one every ordinary call runs).
+static __device__ __noinline__ void store_bytes(unsigned char* dst, uint4 v) {
+  const unsigned char* b = reinterpret_cast<const unsigned char*>(&v);
+  for (int q = 0; q < 16; ++q) dst[q] = b[q];
+}
+static __device__ __noinline__ void store_bytes(unsigned char* dst, uint2 v) {
+  const unsigned char* b = reinterpret_cast<const unsigned char*>(&v);
+  for (int q = 0; q < 8; ++q) dst[q] = b[q];
+}
+
 // Stochastic rounding of 8 consecutive elements (two Philox blocks, counter
 // (e/4, dst_slot, layer, 0) with e the first element's index), then the exact
 // pack.  Kept out of line, so that the code of the rounding-to-nearest path,
@@ -494,7 +505,6 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
   constexpr int VEC = TL.vec, LPR = TL.lpr, CT = TL.ct, SLAB_ROWS = TL.slab_rows, RPT = TL.rpt, COLS = TL.cols;
   constexpr int V2 = VEC / 2;
   using Raw = typename Vec<SF>::Raw;
-  constexpr int VB = Vec<SF>::BYTES;
   constexpr int XW = SLAB_ROWS % 4 == 0 ? 4 : (SLAB_ROWS % 2 == 0 ? 2 : 1);
   float* bbuf = cbuf + kTokChunk * SLAB_ROWS;
   const int lane_row = lane / LPR, lane_col = lane % LPR;
@@ -690,13 +700,10 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
         out = pack_vec_rne<SF>(acc[r]);
       }
       const uint32_t off = ((row0 + r) * N + col0) * ES;
-      if (dst_aligned) {
+      if (dst_aligned)
         stg_stream(dst_tile + off, out);
-      } else {
-        const unsigned char* ob = reinterpret_cast<const unsigned char*>(&out);
-#pragma unroll
-        for (int q = 0; q < VB; ++q) dst_tile[off + q] = ob[q];
-      }
+      else
+        store_bytes(dst_tile + off, out);
     }
     if constexpr (Q) {
       if (lane_col < RPT) {
@@ -720,7 +727,6 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
   constexpr int VEC = TL.vec, LPR = TL.lpr, CT = TL.ct, SLAB_ROWS = TL.slab_rows, RPT = TL.rpt, COLS = TL.cols;
   static_assert(VEC == Vec<SF>::N && VEC % 2 == 0, "vector width");
   using Raw = typename Vec<SF>::Raw;
-  constexpr int VB = Vec<SF>::BYTES;  // bytes per vector
   static_assert(TL.tct % LPR == 0 && kConsumerWarps % CT == 0 && D % TL.slabs == 0, "thread layout");
   static_assert(SLAB_ROWS % TL.rpw == 0 || SLAB_ROWS < TL.rpw, "rows must split evenly");
   static_assert(!Q || SLAB_ROWS >= TL.rpw, "one-byte formats need every consumer lane busy");
@@ -805,13 +811,10 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
           const uint32_t off = ((row0 + r) * N + col0) * ES;
-          if (dst_aligned) {
+          if (dst_aligned)
             stg_stream(dst_tile + off, raw[r]);
-          } else {
-            const unsigned char* rb = reinterpret_cast<const unsigned char*>(&raw[r]);
-#pragma unroll
-            for (int q = 0; q < VB; ++q) dst_tile[off + q] = rb[q];
-          }
+          else
+            store_bytes(dst_tile + off, raw[r]);
         }
       }
       if constexpr (Q) {
