@@ -9,8 +9,8 @@
 //   S  = exp(g_t) S
 //   S  = S + beta_t (v_t - S k^) k^T
 // Every value row evolves on its own given k^, its v entry, g and beta, so the
-// work item is a slab of 32 rows of one head (16 KiB): a row's dot product is
-// a reduction over the 8 lanes that hold it.  The normalisation is folded into
+// work item is a slab of 64 rows of one head (32 KiB): a row's dot product is
+// a reduction over the 8 lanes that hold it (each lane holds two rows).  The normalisation is folded into
 // two scalars per token (S k^ = r * S k, k^ k^T update = (u r) k), so k is
 // used raw, and the decay into a running scale of the whole slab, so that each
 // element costs two FMAs per token.
@@ -234,8 +234,9 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
 }
 
 // ---------------------------------------------------------------------------
-// consumer warps: lane (row lr = lane / 8 of the warp's four, column group
-// lc = lane % 8) holds S[row][q*32 + lc*4 + e], q, e = 0..3
+// consumer warps: lane (lr = lane / 8, column group lc = lane % 8) holds
+// S[row][q*32 + lc*4 + e], q, e = 0..3, for its two rows cw*8 + lr and
+// cw*8 + lr + 4 (each key value it loads serves both)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -245,7 +246,7 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
   const uint32_t empty0 = full0 + 8u * kMaxSlots;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
   const int lr = lane >> 3, lc = lane & 7;
-  const int row = cw * 4 + lr;  // row inside the slab
+  const int rowa = cw * 8 + lr, rowb = rowa + 4;  // this lane's rows inside the slab
   const uint32_t item_max = item_layout(p.T).bytes;
   const bool l2norm = p.l2norm != 0;
   uint32_t arena_head = 0;
@@ -302,16 +303,20 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
     // ca = c * exp(g): S k^ after the decay is ca * r * (S k), and the update
     // (u r) k adds (u r / ca) k to S.  Rescaling is exact up to rounding
     // (it scales every term alike); S is renormalised before c gets small.
-    // this lane's 16 state values as packed pairs: S2[2q], S2[2q+1] = columns
-    // q*32 + lc*4 + {0,1}, {2,3}
-    float2 S2[8];
+    // this lane's state values as packed pairs: Sa/Sb[2q], [2q+1] = columns
+    // q*32 + lc*4 + {0,1}, {2,3} of rows rowa / rowb
+    float2 Sa[8], Sb[8];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float4 v4 = *reinterpret_cast<const float4*>(sb + (row * kDK + q * 32 + lc * 4) * 4);
-      S2[2 * q] = make_float2(v4.x, v4.y);
-      S2[2 * q + 1] = make_float2(v4.z, v4.w);
+      const float4 va = *reinterpret_cast<const float4*>(sb + (rowa * kDK + q * 32 + lc * 4) * 4);
+      const float4 vb = *reinterpret_cast<const float4*>(sb + (rowb * kDK + q * 32 + lc * 4) * 4);
+      Sa[2 * q] = make_float2(va.x, va.y);
+      Sa[2 * q + 1] = make_float2(va.z, va.w);
+      Sb[2 * q] = make_float2(vb.x, vb.y);
+      Sb[2 * q + 1] = make_float2(vb.z, vb.w);
     }
     float c = 1.0f, inv_c = 1.0f;
+    const uint16_t* vcol = reinterpret_cast<const uint16_t*>(sb + it.off_v);
     for (int t = 0; t < n; ++t) {
       const float4 tp = tok[t];
       float2 k2[8];
@@ -321,48 +326,61 @@ __device__ __forceinline__ void run_consumer(const Params& p, unsigned char* sme
         k2[2 * q] = make_float2(bf16lo(w.x), bf16hi(w.x));
         k2[2 * q + 1] = make_float2(bf16lo(w.y), bf16hi(w.y));
       }
-      float2 d0 = __fmul2_rn(S2[0], k2[0]), d1 = __fmul2_rn(S2[1], k2[1]);
+      float2 da = __fmul2_rn(Sa[0], k2[0]), db = __fmul2_rn(Sb[0], k2[0]);
 #pragma unroll
-      for (int e = 2; e < 8; e += 2) {
-        d0 = __ffma2_rn(S2[e], k2[e], d0);
-        d1 = __ffma2_rn(S2[e + 1], k2[e + 1], d1);
+      for (int e = 1; e < 8; ++e) {
+        da = __ffma2_rn(Sa[e], k2[e], da);
+        db = __ffma2_rn(Sb[e], k2[e], db);
       }
-      float dot = (d0.x + d0.y) + (d1.x + d1.y);
+      float dota = da.x + da.y, dotb = db.x + db.y;
 #pragma unroll
-      for (int o = 1; o < 8; o <<= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
-      const float v = __uint_as_float(static_cast<uint32_t>(
-                                           reinterpret_cast<const uint16_t*>(sb + it.off_v)[t * kSlabRows + row])
-                                       << 16);
+      for (int o = 1; o < 8; o <<= 1) {
+        dota += __shfl_xor_sync(0xFFFFFFFFu, dota, o);
+        dotb += __shfl_xor_sync(0xFFFFFFFFu, dotb, o);
+      }
+      const float v_a = __uint_as_float(static_cast<uint32_t>(vcol[t * kSlabRows + rowa]) << 16);
+      const float v_b = __uint_as_float(static_cast<uint32_t>(vcol[t * kSlabRows + rowb]) << 16);
       const float ca = c * tp.x, inv_ca = inv_c * tp.w;
-      const float u = tp.y * (v - ca * (tp.z * dot));
-      const float w = u * tp.z * inv_ca;
-      const float2 w2 = make_float2(w, w);
+      const float rs = tp.z * inv_ca;
+      const float wa = tp.y * (v_a - ca * (tp.z * dota)) * rs;
+      const float wb = tp.y * (v_b - ca * (tp.z * dotb)) * rs;
+      const float2 wa2 = make_float2(wa, wa), wb2 = make_float2(wb, wb);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) S2[e] = __ffma2_rn(w2, k2[e], S2[e]);
+      for (int e = 0; e < 8; ++e) {
+        Sa[e] = __ffma2_rn(wa2, k2[e], Sa[e]);
+        Sb[e] = __ffma2_rn(wb2, k2[e], Sb[e]);
+      }
       c = ca;
       inv_c = inv_ca;
       if (c < 0x1p-30f) {  // the same in every lane of the item
         const float2 c2 = make_float2(c, c);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) S2[e] = __fmul2_rn(S2[e], c2);
+        for (int e = 0; e < 8; ++e) {
+          Sa[e] = __fmul2_rn(Sa[e], c2);
+          Sb[e] = __fmul2_rn(Sb[e], c2);
+        }
         c = 1.0f;
         inv_c = 1.0f;
       }
       if (track != nullptr && t == step) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          __stcs(reinterpret_cast<float4*>(track + row * kDK + q * 32 + lc * 4),
-                 make_float4(c * S2[2 * q].x, c * S2[2 * q].y, c * S2[2 * q + 1].x, c * S2[2 * q + 1].y));
+        for (int q = 0; q < 4; ++q) {
+          __stcs(reinterpret_cast<float4*>(track + rowa * kDK + q * 32 + lc * 4),
+                 make_float4(c * Sa[2 * q].x, c * Sa[2 * q].y, c * Sa[2 * q + 1].x, c * Sa[2 * q + 1].y));
+          __stcs(reinterpret_cast<float4*>(track + rowb * kDK + q * 32 + lc * 4),
+                 make_float4(c * Sb[2 * q].x, c * Sb[2 * q].y, c * Sb[2 * q + 1].x, c * Sb[2 * q + 1].y));
+        }
       }
     }
-    float4 S[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      S[q] = make_float4(c * S2[2 * q].x, c * S2[2 * q].y, c * S2[2 * q + 1].x, c * S2[2 * q + 1].y);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8u * stage);  // nothing more is read from the slot
 #pragma unroll
-    for (int q = 0; q < 4; ++q) __stcs(reinterpret_cast<float4*>(slab + row * kDK + q * 32 + lc * 4), S[q]);
+    for (int q = 0; q < 4; ++q) {
+      __stcs(reinterpret_cast<float4*>(slab + rowa * kDK + q * 32 + lc * 4),
+             make_float4(c * Sa[2 * q].x, c * Sa[2 * q].y, c * Sa[2 * q + 1].x, c * Sa[2 * q + 1].y));
+      __stcs(reinterpret_cast<float4*>(slab + rowb * kDK + q * 32 + lc * 4),
+             make_float4(c * Sb[2 * q].x, c * Sb[2 * q].y, c * Sb[2 * q + 1].x, c * Sb[2 * q + 1].y));
+    }
     if (++stage == p.slots) {
       stage = 0;
       phase ^= 1u;

@@ -11,7 +11,7 @@ namespace gdn {
 using rsm::round_up;
 
 constexpr int kDK = 128, kDV = 128;
-constexpr int kSlabRows = 32;
+constexpr int kSlabRows = 64;
 constexpr int kSlabs = kDV / kSlabRows;
 constexpr uint32_t kSlabBytes = kSlabRows * kDK * 4;
 constexpr int kConsumerWarps = 8;
@@ -19,7 +19,7 @@ constexpr int kThreads = 32 * (1 + kConsumerWarps);
 constexpr int kMaxWindow = 64;
 constexpr int kMaxSlots = 16;
 constexpr uint64_t kWaitTimeoutNs = 4000000000ull;
-static_assert(kConsumerWarps * 4 == kSlabRows, "four rows per consumer warp");
+static_assert(kConsumerWarps * 8 == kSlabRows, "eight rows per consumer warp (two per lane)");
 
 // shared memory: [full mbarriers][empty mbarriers] | abort flag | descriptors |
 // per-consumer-warp token tables (exp(g), beta, 1/|k|, exp(-g) per token) | arena
