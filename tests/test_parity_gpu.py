@@ -362,3 +362,50 @@ def test_tensor_core_misaligned_destination():
     got = hw.copy()
     got.state = [wl._to_np(t).view(a.dtype) for t, a in zip(dw.state, hw.state)]
     compare_worlds(got, run_oracle(hw), hw)
+
+
+@pytest.mark.parametrize("bad,bit", [("prefix", 4), ("ring_start", 2), ("active", 1), ("slot", 8)])
+def test_tensor_core_out_of_range_metadata_is_skipped_and_flagged(bad, bit):
+    shape = wl.Shape("tcbad", L=2, Bt=4, H=4, hpg=2, D=64, N=128, R=64, W=64, state_dtype="bf16", n_active=4,
+                     ring_start=(0, 64), prefix=("uniform", 12, 64))
+    hw = wl.host_world(shape, seed=42)
+    victim = int(hw.active[1])
+    if bad == "prefix":
+        hw.replay_prefix_len[victim] = shape.W + 1
+    elif bad == "ring_start":
+        hw.ring_start[victim] = shape.R
+    elif bad == "active":
+        hw.active[1] = shape.Bt + 5
+    else:
+        hw.src_slots[0, victim] = -7
+    got = run_cuda(hw, status_expected=bit)
+    ref_in = hw.copy()
+    if bad == "slot":
+        ref_in.dst_slots[0, victim] = ref_in.pad_slot_id
+        ref_in.src_slots[0, victim] = 0
+    else:
+        keep = [a for i, a in enumerate(hw.active) if i != 1]
+        ref_in.active[:] = keep + [-1]
+        if bad != "active":
+            ref_in.replay_prefix_len[victim] = 0
+            ref_in.ring_start[victim] = 0
+    compare_worlds(got, run_oracle(ref_in), ref_in)
+
+
+@pytest.mark.parametrize("sd", ["bf16", "f16"])
+def test_tensor_core_in_place_commit(sd):
+    shape = wl.Shape("tcinplace", L=2, Bt=5, H=6, hpg=3, D=64, N=128, R=64, W=64, state_dtype=sd, n_active=4,
+                     ring_start=(0, 64), prefix=("uniform", 0, 64))
+    hw = wl.host_world(shape, seed=73)
+    hw.dst_slots[:] = hw.src_slots
+    assert check(hw) >= 4
+
+
+def test_tensor_core_empty_active_list_writes_nothing():
+    shape = wl.Shape("tcempty", L=2, Bt=4, H=4, hpg=2, D=64, N=128, R=64, W=64, state_dtype="bf16", n_active=0,
+                     ring_start=(0, 64), prefix=("uniform", 10, 64))
+    hw = wl.host_world(shape, seed=74)
+    hw.active[:] = -1
+    got = run_cuda(hw)
+    for l in range(hw.L):
+        assert got.state[l].tobytes() == hw.state[l].tobytes()
