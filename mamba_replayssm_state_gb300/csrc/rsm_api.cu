@@ -261,7 +261,7 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   p.R = a->ring_buffer_len;
   p.pad = a->pad_slot_id;
   p.philox_rounds = a->philox_rounds;
-  p.tc_min_k = rsm::kTcMinK;
+  p.tc_min_k = use_tc ? rsm::kTcMinK : 0;
   p.desc0 = use_tc ? rsm::kTcDescBase : rsm::desc_base(a->dim, a->dstate, sb);
   p.arena0 = static_cast<uint32_t>(base);
   p.arena_bytes = static_cast<uint32_t>(arena);

@@ -54,6 +54,10 @@ struct alignas(16) ItemDesc {
 };
 static_assert(sizeof(ItemDesc) == kDescBytes, "descriptor size");
 constexpr uint32_t kFlagEnd = 1u, kFlagDstAligned = 2u, kFlagScaleAligned = 4u;
+// A tensor-core item whose head continues the previous item's B group (same
+// request and layer): its B rows are not copied, the consumers reuse the MMA
+// operand they built from the previous item's.
+constexpr uint32_t kFlagSameB = 8u;
 
 __device__ __forceinline__ void flag_status(uint32_t* status, uint32_t bits) {
   if (status != nullptr && bits != 0u) atomicOr(status, bits);
@@ -331,9 +335,14 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
     int g_left = p.hpg - (h - g * p.hpg);  // heads left in group g, h included
     const uint4 desc_tail = make_uint4(static_cast<uint32_t>(k), dst_flags, static_cast<uint32_t>(l),
                                        static_cast<uint32_t>(dst));
-    const ItemLayout il = item_layout(D, N, ES, Q, IE, k);
+    const ItemLayout il_full = item_layout(D, N, ES, Q, IE, k);
+    const ItemLayout il_noB = item_layout(D, N, ES, Q, IE, k, false);
+    const bool tc_items = p.tc_min_k > 0 && k >= p.tc_min_k;  // the tensor-core kernel's MMA path
+    const int unit_h0 = h;
 
     for (; h < h_end; ++h) {
+      const bool same_B = tc_items && h != unit_h0 && g_left != p.hpg;
+      const ItemLayout il = same_B ? il_noB : il_full;
       uint32_t off = 0;
       if (!alloc(il.bytes, off)) {
         aborted = true;
@@ -363,13 +372,14 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
         const unsigned long long dc = reinterpret_cast<unsigned long long>(dst_sc);
         d4[0] = make_uint4(static_cast<uint32_t>(ds), static_cast<uint32_t>(ds >> 32), static_cast<uint32_t>(dc),
                            static_cast<uint32_t>(dc >> 32));
-        d4[1] = desc_tail;  // k, flags, layer, dst_slot
+        d4[1] = make_uint4(desc_tail.x, desc_tail.y | (same_B ? kFlagSameB : 0u), desc_tail.z,
+                           desc_tail.w);  // k, flags, layer, dst_slot
         desc->head = h;
       }
       if (aligned) {
         if (lane == 0) {
           fence_proxy_async_smem();
-          mbar_expect_tx(fullb, kTileBytes + (Q ? D * 4u : 0u) + static_cast<uint32_t>(k) * (D + N) * IE);
+          mbar_expect_tx(fullb, kTileBytes + (Q ? D * 4u : 0u) + static_cast<uint32_t>(k) * (D + (same_B ? 0 : N)) * IE);
         }
         __syncwarp();
         if (lane == 0) {
@@ -384,8 +394,9 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
           if (t < k) {
             const int64_t xr = static_cast<int64_t>(ring_row[q]) * p.H + h;  // x row [p_t, h] and dt [p_t, h]
             bulk_g2s(sba + il.off_x + static_cast<uint32_t>(t) * D * IE, x_slot + xr * (D * IE), D * IE, fullb);
-            bulk_g2s(sba + il.off_B + static_cast<uint32_t>(t) * N * IE,
-                     B_slot + (static_cast<int64_t>(ring_row[q]) * G + g) * (N * IE), N * IE, fullb);
+            if (!same_B)
+              bulk_g2s(sba + il.off_B + static_cast<uint32_t>(t) * N * IE,
+                       B_slot + (static_cast<int64_t>(ring_row[q]) * G + g) * (N * IE), N * IE, fullb);
             cp_async_4(sba + il.off_dt + 4u * t, dt_slot + xr);
           }
         }
@@ -399,8 +410,9 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
           const int pr = (rs + t) % p.R;
           copy_bytes_warp(sb + il.off_x + t * D * IE, x_slot + (static_cast<int64_t>(pr) * p.H + h) * D * IE,
                           D * IE, lane);
-          copy_bytes_warp(sb + il.off_B + t * N * IE, B_slot + (static_cast<int64_t>(pr) * G + g) * N * IE,
-                          N * IE, lane);
+          if (!same_B)
+            copy_bytes_warp(sb + il.off_B + t * N * IE, B_slot + (static_cast<int64_t>(pr) * G + g) * N * IE,
+                            N * IE, lane);
           copy_bytes_warp(sb + il.off_dt + 4 * t,
                           reinterpret_cast<const unsigned char*>(dt_slot + static_cast<int64_t>(pr) * p.H + h), 4,
                           lane);

@@ -68,19 +68,20 @@ __host__ __device__ constexpr uint32_t arena_base(int dim, int dstate, int state
 }
 
 // Byte layout of one work item in the arena: the source tile at offset 0, its
-// scales (one-byte formats), then the item's own k ring rows of x, of B and
-// its k dt values.  Every part starts on a 16-byte boundary (D*N*ES, D*IE and
+// scales (one-byte formats), then the item's own k ring rows of x, of B (left
+// out for a tensor-core item that reuses the previous item's B) and its k dt
+// values.  Every part starts on a 16-byte boundary (D*N*ES, D*IE and
 // N*IE are multiples of 16); items start on 128-byte boundaries.
 struct ItemLayout {
   uint32_t off_scale, off_x, off_B, off_dt, bytes;
 };
 
 __host__ __device__ constexpr ItemLayout item_layout(int dim, int dstate, int state_bytes, bool quant, int in_bytes,
-                                                     int k) {
+                                                     int k, bool with_B = true) {
   const uint32_t off_scale = static_cast<uint32_t>(dim * dstate * state_bytes);
   const uint32_t off_x = off_scale + (quant ? static_cast<uint32_t>(dim) * 4u : 0u);
   const uint32_t off_B = off_x + static_cast<uint32_t>(k * dim * in_bytes);
-  const uint32_t off_dt = off_B + static_cast<uint32_t>(k * dstate * in_bytes);
+  const uint32_t off_dt = off_B + (with_B ? static_cast<uint32_t>(k * dstate * in_bytes) : 0u);
   return ItemLayout{off_scale, off_x, off_B, off_dt, round_up(off_dt + 4u * static_cast<uint32_t>(k), 128u)};
 }
 
@@ -130,7 +131,7 @@ struct Params {
   const int64_t* rand_seed;
   uint32_t* status;
   int32_t L, Bt, H, hpg, W, R, pad, philox_rounds;
-  int32_t tc_min_k;  // tensor-core variant: prefixes this long or longer go to the MMA
+  int32_t tc_min_k;  // tensor-core variant: prefixes this long or longer go to the MMA (0: no tensor path)
   // shared-memory plan: descriptor table at desc0, item arena of arena_bytes at
   // arena0, `stages` pipeline slots (mbarrier pairs and descriptors)
   uint32_t desc0, arena0, arena_bytes, stages;

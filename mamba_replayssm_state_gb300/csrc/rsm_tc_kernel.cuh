@@ -57,7 +57,6 @@ __device__ __forceinline__ void run_consumer_tc(const Params& p, unsigned char* 
   // short prefixes run on the CUDA cores with per-warp token buffers inside the operand region
   float* cbuf = reinterpret_cast<float*>(smem + kTcAOff) + cw * warp_buf_floats(D, N, ES);
   static_assert(kConsumerWarps * warp_buf_floats(64, 128, 2) * 4 <= kTcDescBase - kTcAOff, "token buffers");
-  const uint32_t xbar4 = mma_bar + 48u;
   const int tid = cw * 32 + lane;       // 0 .. 255 over the consumer warps
   const int quarter = (cw + 1) & 3;     // TMEM lane quarter this warp may access (CTA warp id % 4)
   const int half = cw >> 2;             // which 32 of the 64 accumulator columns
@@ -78,8 +77,8 @@ __device__ __forceinline__ void run_consumer_tc(const Params& p, unsigned char* 
       flag_status(p.status, RSM_STATUS_WAIT_TIMEOUT);
     }
   };
-  uint32_t xpar = 0, mpar = 0, x4par = 0;
-  bool prev_tc = false;  // the last item with a prefix went through the MMA (its tile was staged in aop)
+  uint32_t xpar = 0, x1par = 0, mpar = 0;
+  bool prev_tc = false;  // the last item with a prefix went through the MMA
   // every consumer warp arrives, then all wait (bounded)
   // (every exit decision is taken by the whole warp: the warp-wide tcgen05
   // instructions below must never see a partial warp)
@@ -105,7 +104,8 @@ __device__ __forceinline__ void run_consumer_tc(const Params& p, unsigned char* 
     const uint32_t flags = __shfl_sync(0xFFFFFFFFu, desc->flags, 0);
     if (flags & kFlagEnd) break;
     const int k = __shfl_sync(0xFFFFFFFFu, desc->k, 0);
-    const ItemLayout il = item_layout(D, N, ES, false, IE, k);
+    const bool same_B = (flags & kFlagSameB) != 0u;  // the A operand of the previous item still holds
+    const ItemLayout il = item_layout(D, N, ES, false, IE, k, !same_B);
     arena_head = off + il.bytes;
     unsigned char* dst_tile = reinterpret_cast<unsigned char*>(desc->dst_state);
     const bool dst_aligned = (flags & kFlagDstAligned) != 0u;
@@ -132,17 +132,6 @@ __device__ __forceinline__ void run_consumer_tc(const Params& p, unsigned char* 
         }
       }
     } else if (k < p.tc_min_k) {
-      if (prev_tc) {
-        // every warp has stored the previous item's staged tile before the buffers are reused
-        __syncwarp();
-        if (lane == 0) mbar_arrive(xbar4);
-        const bool ok = mbar_wait(xbar4, x4par, kWaitTimeoutNs) && !*abort_flag;
-        x4par ^= 1u;
-        if (!__all_sync(0xFFFFFFFFu, ok)) {
-          give_up();
-          break;
-        }
-      }
       replay_ffma<SF, RSM_BF16, 64, 128>(p, sb, il, desc, k, wbuf, cbuf, cw, lane, empty_bar, key0, key1, sr);
       prev_tc = false;
     } else {
@@ -176,15 +165,22 @@ __device__ __forceinline__ void run_consumer_tc(const Params& p, unsigned char* 
         s0[c] = static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(sb)[(i0 + 2 * c) * N + j]) |
                 (static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(sb)[(i0 + 2 * c + 1) * N + j]) << 16);
 
-      // the previous item's staged tile has been stored: the operand buffers are free
-      if (!xsync(xbar1)) {
-        give_up();
-        break;
+      // after a CUDA-core item, every warp is done with its token buffer (inside
+      // the operand region) before the operands are written
+      if (!prev_tc) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xbar1);
+        const bool ok = mbar_wait(xbar1, x1par, kWaitTimeoutNs) && !*abort_flag;
+        x1par ^= 1u;
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+          give_up();
+          break;
+        }
       }
       const int kp = (k + 15) & ~15;  // K padded to whole MMAs; tokens k .. kp-1 are zero
       const uint16_t* Brows = reinterpret_cast<const uint16_t*>(sb + il.off_B);
       const uint16_t* xrows = reinterpret_cast<const uint16_t*>(sb + il.off_x);
-      for (int u = tid; u < 128 * (kp / 8); u += 256) {
+      for (int u = same_B ? 128 * (kp / 8) : tid; u < 128 * (kp / 8); u += 256) {  // A = B^T (unless reused)
         const int jj = u & 127, tg = u >> 7;
         uint32_t w[4];
 #pragma unroll
@@ -212,8 +208,6 @@ __device__ __forceinline__ void run_consumer_tc(const Params& p, unsigned char* 
             make_uint4(w[0], w[1], w[2], w[3]);
       }
       fence_proxy_async_smem();  // the operands, written by this thread, before the tensor cores read them
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar);  // nothing more is read from the item
       tc_fence_before();
       if (!xsync(xbar2)) {
         give_up();
@@ -237,7 +231,10 @@ __device__ __forceinline__ void run_consumer_tc(const Params& p, unsigned char* 
       // S = P S_0 + (C B): round and stage [dim row][dstate column] in the A
       // buffer, 16 accumulator columns at a time (the stochastic-rounding loop
       // kept apart, out of the common path)
-      uint16_t* stage_tile = reinterpret_cast<uint16_t*>(aop);
+      // (the staging tile is the item's own source-tile region: every warp has
+      // read its S_0 values before the MMA was issued, and the A operand stays
+      // intact for the next head of the same B group)
+      uint16_t* stage_tile = reinterpret_cast<uint16_t*>(const_cast<unsigned char*>(sb));
       const uint32_t taddr =
           tmem + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(i0);
 #pragma unroll
@@ -273,7 +270,7 @@ __device__ __forceinline__ void run_consumer_tc(const Params& p, unsigned char* 
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const uint32_t o = static_cast<uint32_t>(tid + 256 * r) * 16u;
-        const uint4 v = *reinterpret_cast<const uint4*>(aop + o);
+        const uint4 v = *reinterpret_cast<const uint4*>(sb + o);
         if (dst_aligned) {
           stg128_stream(dst_tile + o, v);
         } else {
@@ -281,6 +278,8 @@ __device__ __forceinline__ void run_consumer_tc(const Params& p, unsigned char* 
           for (int q = 0; q < 16; ++q) dst_tile[o + q] = b[q];
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar);  // the item's region is free again
       xpar ^= 1u;
       prev_tc = true;
     }
@@ -309,7 +308,6 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_tc_kernel(const __gri
     }
     mbar_init(sbase + kTcBarOff, 1u);  // MMA completion
     for (uint32_t b = 1; b <= 4; ++b) mbar_init(sbase + kTcBarOff + 8u * b, kConsumerWarps);  // x1, x2, x3, exit
-    mbar_init(sbase + kTcBarOff + 48u, kConsumerWarps);                                      // x4
     *reinterpret_cast<volatile int*>(smem + kAbortOff) = 0;
     fence_mbar_init();
   }
