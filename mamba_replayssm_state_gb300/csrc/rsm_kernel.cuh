@@ -472,6 +472,46 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
 // ---------------------------------------------------------------------------
 // consumer warps
 // ---------------------------------------------------------------------------
+// Decay of a prefix of k <= 64 tokens, once per warp: a_t = exp(dt_t*A),
+// w_t = dt_t * prod_{s>t} a_s into wbuf, and P = prod_t a_t returned (the same
+// in every lane).  Suffix products by shuffles over 32-token chunks; the two
+// chunks of a longer prefix are scanned side by side, the first one's weights
+// then scaled by the second one's product.
+__device__ __forceinline__ float decay_scan(const float* dts, float A, int k, int lane, float* wbuf) {
+  const float dt0 = lane < k ? dts[lane] : 0.0f;
+  float i0 = lane < k ? expf(dt0 * A) : 1.0f;
+  if (k <= 32) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float v0 = __shfl_down_sync(0xFFFFFFFFu, i0, off);
+      if (lane + off < 32) i0 *= v0;
+    }
+    float e0 = __shfl_down_sync(0xFFFFFFFFu, i0, 1);
+    if (lane == 31) e0 = 1.0f;
+    if (lane < k) wbuf[lane] = dt0 * e0;
+    return __shfl_sync(0xFFFFFFFFu, i0, 0);
+  }
+  const int t1 = 32 + lane;
+  const float dt1 = t1 < k ? dts[t1] : 0.0f;
+  float i1 = t1 < k ? expf(dt1 * A) : 1.0f;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float v0 = __shfl_down_sync(0xFFFFFFFFu, i0, off);
+    const float v1 = __shfl_down_sync(0xFFFFFFFFu, i1, off);
+    if (lane + off < 32) {
+      i0 *= v0;
+      i1 *= v1;
+    }
+  }
+  float e0 = __shfl_down_sync(0xFFFFFFFFu, i0, 1);
+  float e1 = __shfl_down_sync(0xFFFFFFFFu, i1, 1);
+  if (lane == 31) e0 = e1 = 1.0f;
+  const float p1 = __shfl_sync(0xFFFFFFFFu, i1, 0);  // product of the second chunk
+  if (t1 < k) wbuf[t1] = dt1 * e1;
+  if (lane < k) wbuf[lane] = dt0 * (e0 * p1);
+  return p1 * __shfl_sync(0xFFFFFFFFu, i0, 0);
+}
+
 // Byte-wise store of a vector to a destination that is not 16-byte aligned
 // (out of line: the aligned path is the one every ordinary call runs).
 static __device__ __noinline__ void store_bytes(unsigned char* dst, uint4 v) {
@@ -541,25 +581,7 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
   };
     // decay of each token, once per warp: a_t = exp(dt_t*A), then
     // w_t = dt_t * prod_{s>t} a_s and P = prod_t a_t by a suffix-product scan
-    const float A = desc->A;
-    const float* dts = reinterpret_cast<const float*>(sb + il.off_dt);
-    float carry = 1.0f;
-    for (int c = (k - 1) >> 5; c >= 0; --c) {
-      const int t = 32 * c + lane;
-      const float dtv = t < k ? dts[t] : 0.0f;
-      const float a = t < k ? expf(dtv * A) : 1.0f;
-      float incl = a;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float v = __shfl_down_sync(0xFFFFFFFFu, incl, off);
-        if (lane + off < 32) incl *= v;
-      }
-      float excl = __shfl_down_sync(0xFFFFFFFFu, incl, 1);
-      if (lane == 31) excl = 1.0f;
-      if (t < k) wbuf[t] = dtv * (excl * carry);
-      carry *= __shfl_sync(0xFFFFFFFFu, incl, 0);
-    }
-    const float P = carry;  // identical in every lane
+    const float P = decay_scan(reinterpret_cast<const float*>(sb + il.off_dt), desc->A, k, lane, wbuf);
 
     // this thread's [RPT rows x VEC columns] of the tile, dequantized, times P
     float2 acc[RPT][V2];

@@ -136,25 +136,7 @@ __device__ __forceinline__ void run_consumer_tc(const Params& p, unsigned char* 
       prev_tc = false;
     } else {
       // decay of each token, once per warp (as in the materialization kernel)
-      const float A = desc->A;
-      const float* dts = reinterpret_cast<const float*>(sb + il.off_dt);
-      float carry = 1.0f;
-      for (int c = (k - 1) >> 5; c >= 0; --c) {
-        const int t = 32 * c + lane;
-        const float dtv = t < k ? dts[t] : 0.0f;
-        const float a = t < k ? expf(dtv * A) : 1.0f;
-        float incl = a;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float v = __shfl_down_sync(0xFFFFFFFFu, incl, o);
-          if (lane + o < 32) incl *= v;
-        }
-        float excl = __shfl_down_sync(0xFFFFFFFFu, incl, 1);
-        if (lane == 31) excl = 1.0f;
-        if (t < k) wbuf[t] = dtv * (excl * carry);
-        carry *= __shfl_sync(0xFFFFFFFFu, incl, 0);
-      }
-      const float P = carry;
+      const float P = decay_scan(reinterpret_cast<const float*>(sb + il.off_dt), desc->A, k, lane, wbuf);
       __syncwarp();  // wbuf visible to the whole warp
 
       // S_0 at this thread's (dim rows i0 .. i0+31, dstate column j), kept as
