@@ -295,6 +295,30 @@ def time_graph(torch, fn_list, reps=3):
     return e0.elapsed_time(e1) / (reps * len(fn_list))
 
 
+def bind_to_gpu_numa_node(torch, device):
+    """Runs this process on the CPUs of the NUMA node closest to `device` (so
+    that pinned host buffers allocated next are local to the GPU's CPU link);
+    returns that node, or None when the topology cannot be read."""
+    try:
+        prop = torch.cuda.get_device_properties(device)
+        bus = f"{prop.pci_domain_id:04x}:{prop.pci_bus_id:02x}:{prop.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{bus}/numa_node") as f:
+            node = int(f.read().strip())
+        if node < 0:
+            return None
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            lo, _, hi = part.partition("-")
+            cpus.update(range(int(lo), int(hi or lo) + 1))
+        if cpus:
+            os.sched_setaffinity(0, cpus)
+        return node
+    except (OSError, ValueError, AttributeError):
+        return None
+
+
 def e2e_measure(torch, rsm, shape, n_req, steps, device, groups=8):
     """End to end through the public API: every step copies the inputs of n_req
     requests (their source state slots, rings and the call's metadata) from
@@ -303,6 +327,8 @@ def e2e_measure(torch, rsm, shape, n_req, steps, device, groups=8):
     streams: group g's inputs go up while group g-1 computes and group g-2's
     results come back (host-to-device and device-to-host copies overlap)."""
     import numpy as np
+    saved_affinity = os.sched_getaffinity(0)
+    node = bind_to_gpu_numa_node(torch, device)
     sh = shape.replace(Bt=n_req, n_active=n_req)
     meta = wl.draw_metadata(sh, np.random.default_rng(77))
     # contiguous source block (slots 0..n-1) and destination block (n..2n-1) per layer
@@ -377,8 +403,9 @@ def e2e_measure(torch, rsm, shape, n_req, steps, device, groups=8):
                                    meta["dst_slots"])
     del dw, h_state, h_x, h_B, h_dt, h_out, calls
     torch.cuda.empty_cache()
+    os.sched_setaffinity(0, saved_affinity)
     return {"value": state_b / sec / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": sec * 1e3,
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": sec * 1e3, "host_numa_node": node,
             "workload": f"{sh.name} with {n_req} active requests, inputs from pinned host memory, "
                         f"{ng} layer groups streamed through the public call (copies in, compute and copies out "
                         f"overlapped on three streams)"}
