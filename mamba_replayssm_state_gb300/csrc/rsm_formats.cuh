@@ -221,13 +221,19 @@ __device__ __forceinline__ void unpack_words(const uint32_t* w, float* v) {
   } else if constexpr (F == RSM_I8) {
     // int8 -> fp32 exactly on the integer pipes: flip the sign bit so that each
     // byte holds code + 128, place it in the mantissa of 2^23 (0x4B0000xx) and
-    // subtract 2^23 + 128.
+    // subtract 2^23 + 128 (two values per packed add).
+    const float2 bias = make_float2(-8388736.0f, -8388736.0f);
 #pragma unroll
     for (int q = 0; q < NW; ++q) {
       const uint32_t u = w[q] ^ 0x80808080u;
 #pragma unroll
-      for (int b = 0; b < 4; ++b)
-        v[4 * q + b] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540u + b)) - 8388736.0f;
+      for (int b = 0; b < 4; b += 2) {
+        const float2 d = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540u + b)),
+                                                __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541u + b))),
+                                    bias);
+        v[4 * q + b] = d.x;
+        v[4 * q + b + 1] = d.y;
+      }
     }
   } else {  // FP8 e4m3
 #pragma unroll
@@ -259,12 +265,13 @@ __device__ __forceinline__ void pack_words_rne(const float* v, uint32_t* w) {
     // round to nearest even by adding 1.5 * 2^23: the sum's low byte is the
     // two's-complement code.  No clamp is needed: |v| <= amax, so
     // |v * fl(127/amax)| < 127.5 and the code lies in [-127, 127].
+    const float2 magic = make_float2(12582912.0f, 12582912.0f);
 #pragma unroll
     for (int q = 0; q < NW; ++q) {
-      uint32_t r[4];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) r[b] = __float_as_uint(v[4 * q + b] + 12582912.0f);
-      w[q] = __byte_perm(__byte_perm(r[0], r[1], 0x0040u), __byte_perm(r[2], r[3], 0x0040u), 0x5410u);
+      const float2 r01 = __fadd2_rn(make_float2(v[4 * q], v[4 * q + 1]), magic);
+      const float2 r23 = __fadd2_rn(make_float2(v[4 * q + 2], v[4 * q + 3]), magic);
+      w[q] = __byte_perm(__byte_perm(__float_as_uint(r01.x), __float_as_uint(r01.y), 0x0040u),
+                         __byte_perm(__float_as_uint(r23.x), __float_as_uint(r23.y), 0x0040u), 0x5410u);
     }
   } else {
 #pragma unroll

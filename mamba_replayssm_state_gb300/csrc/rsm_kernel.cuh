@@ -481,8 +481,12 @@ __device__ __forceinline__ float decay_scan(const float* dts, float A, int k, in
   const float dt0 = lane < k ? dts[lane] : 0.0f;
   float i0 = lane < k ? expf(dt0 * A) : 1.0f;
   if (k <= 32) {
+    // after the level with offset `off` lane t holds the product over
+    // [t, t + 2*off); levels past the prefix would only multiply by the 1.0
+    // of lanes >= k, so they are skipped (k is warp-uniform)
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
+      if (off >= k) break;
       const float v0 = __shfl_down_sync(0xFFFFFFFFu, i0, off);
       if (lane + off < 32) i0 *= v0;
     }
@@ -682,12 +686,21 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
     }
 
     // requantize + store
-    float scale_own = 0.0f;  // one-byte formats: the scale of row row0 + lane_col (lanes lane_col < RPT)
+    // one-byte formats: lanes with lane_col % RSPAN == 0 own row row0 + lane_col / RSPAN
+    constexpr int RSPAN = LPR / RPT;
+    float scale_own = 0.0f;
+    bool zero_rows[RPT];
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) zero_rows[r] = false;
     if constexpr (Q) {
-      // symmetric per-(head, row) scale: amax by a butterfly over the LPR lanes
-      // of each row; then each row's scale and inverse are divided once, by
-      // the row's lane lane_col == r, and the inverse is shuffled to the rest
-      static_assert(RPT <= LPR, "one lane per row for the scale division");
+      // symmetric per-(head, row) scale.  The row amax is a transpose
+      // reduction over the LPR lanes of the row group: at each of the first
+      // log2(RPT) levels a lane keeps half of its rows and trades the other
+      // half with its partner, so that afterwards each lane holds one row,
+      // row lane_col / RSPAN, reduced over a RSPAN-lane span; the remaining
+      // levels reduce that span.  Each lane divides its row's inverse and
+      // scale once, and the inverses are shuffled to the rest.
+      static_assert(RPT <= LPR && (RPT & (RPT - 1)) == 0 && (LPR & (LPR - 1)) == 0, "row reduction shape");
       float amax[RPT];
 #pragma unroll
       for (int r = 0; r < RPT; ++r) {
@@ -696,25 +709,33 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
         for (int u = 0; u < V2; ++u) amax[r] = fmaxf(amax[r], fmaxf(fabsf(acc[r][u].x), fabsf(acc[r][u].y)));
       }
 #pragma unroll
-      for (int off = LPR / 2; off >= 1; off >>= 1) {
+      for (int s = 0; (RPT >> s) > 1; ++s) {
+        const int half = (RPT >> s) / 2, off = LPR >> (s + 1);
+        const bool upper = (lane & off) != 0;
 #pragma unroll
-        for (int r = 0; r < RPT; ++r) amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xFFFFFFFFu, amax[r], off));
+        for (int i = 0; i < half; ++i) {
+          const float send = upper ? amax[i] : amax[i + half];
+          const float keep = upper ? amax[i + half] : amax[i];
+          amax[i] = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, off));
+        }
       }
       float am = amax[0];
 #pragma unroll
-      for (int r = 1; r < RPT; ++r) am = lane_col == r ? amax[r] : am;
+      for (int off = RSPAN / 2; off >= 1; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, off));
       constexpr float qmax = SF == RSM_I8 ? 127.0f : 448.0f;
       const float inv_own = __fdiv_rn(qmax, am);
       scale_own = inv_own <= FLT_MAX ? __fdiv_rn(am, qmax) : 0.0f;
       const int row_lane0 = lane & ~(LPR - 1);
 #pragma unroll
       for (int r = 0; r < RPT; ++r) {
-        const float inv = __shfl_sync(0xFFFFFFFFu, inv_own, row_lane0 + r);
-        // a row whose qmax/amax is not finite (amax == 0 or tiny) becomes zero codes
-        const bool zero_row = !(inv <= FLT_MAX);
+        const float inv = __shfl_sync(0xFFFFFFFFu, inv_own, row_lane0 + r * RSPAN);
+        // a row whose qmax/amax is not finite (amax == 0 or tiny) becomes zero
+        // codes: its packed words are cleared after the (then meaningless)
+        // scaling and rounding
+        zero_rows[r] = !(inv <= FLT_MAX);
         const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-        for (int u = 0; u < V2; ++u) acc[r][u] = zero_row ? make_float2(0.0f, 0.0f) : __fmul2_rn(acc[r][u], inv2);
+        for (int u = 0; u < V2; ++u) acc[r][u] = __fmul2_rn(acc[r][u], inv2);
       }
     }
 #pragma unroll
@@ -733,6 +754,9 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
       } else {
         out = pack_vec_rne<SF>(acc[r]);
       }
+      if constexpr (Q) {
+        if (zero_rows[r]) out = Raw{};
+      }
       const uint32_t off = ((row0 + r) * N + col0) * ES;
       if (dst_aligned)
         stg_stream(dst_tile + off, out);
@@ -740,12 +764,13 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
         store_bytes(dst_tile + off, out);
     }
     if constexpr (Q) {
-      if (lane_col < RPT) {
+      if (lane_col % RSPAN == 0) {
+        const int srow = row0 + lane_col / RSPAN;
         if (flags & kFlagScaleAligned) {
-          dst_sc[row0 + lane_col] = scale_own;
+          dst_sc[srow] = scale_own;
         } else {
           const unsigned char* vb = reinterpret_cast<const unsigned char*>(&scale_own);
-          unsigned char* db = reinterpret_cast<unsigned char*>(dst_sc + row0 + lane_col);
+          unsigned char* db = reinterpret_cast<unsigned char*>(dst_sc + srow);
           for (int q = 0; q < 4; ++q) db[q] = vb[q];
         }
       }
