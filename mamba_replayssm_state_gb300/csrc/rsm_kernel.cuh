@@ -545,6 +545,41 @@ __device__ __noinline__ typename Vec<SF>::Raw sr_pack8(float2 a0, float2 a1, flo
   return pack_vec_rne<SF>(v);
 }
 
+// The same for two rows of 8 elements (blocks blk_a, blk_a + 1 and blk_b,
+// blk_b + 1): four independent Philox chains side by side.
+template <int SF>
+struct RawPair {
+  typename Vec<SF>::Raw a, b;
+};
+
+template <int SF>
+__device__ __noinline__ RawPair<SF> sr_pack8x2(float2 a0, float2 a1, float2 a2, float2 a3, float2 b0, float2 b1,
+                                               float2 b2, float2 b3, uint32_t blk_a, uint32_t blk_b, uint32_t slot,
+                                               uint32_t layer, uint32_t key0, uint32_t key1, int rounds) {
+  uint4 r0, r1, r2, r3;
+  if (rounds == 10) {
+    r0 = philox4x32_r<10>(make_uint4(blk_a, slot, layer, 0u), key0, key1);
+    r1 = philox4x32_r<10>(make_uint4(blk_a + 1u, slot, layer, 0u), key0, key1);
+    r2 = philox4x32_r<10>(make_uint4(blk_b, slot, layer, 0u), key0, key1);
+    r3 = philox4x32_r<10>(make_uint4(blk_b + 1u, slot, layer, 0u), key0, key1);
+  } else {
+    r0 = philox4x32(make_uint4(blk_a, slot, layer, 0u), key0, key1, rounds);
+    r1 = philox4x32(make_uint4(blk_a + 1u, slot, layer, 0u), key0, key1, rounds);
+    r2 = philox4x32(make_uint4(blk_b, slot, layer, 0u), key0, key1, rounds);
+    r3 = philox4x32(make_uint4(blk_b + 1u, slot, layer, 0u), key0, key1, rounds);
+  }
+  float2 v[4], w[4];
+  v[0] = make_float2(sr_fmt<SF>(a0.x, r0.x), sr_fmt<SF>(a0.y, r0.y));
+  v[1] = make_float2(sr_fmt<SF>(a1.x, r0.z), sr_fmt<SF>(a1.y, r0.w));
+  v[2] = make_float2(sr_fmt<SF>(a2.x, r1.x), sr_fmt<SF>(a2.y, r1.y));
+  v[3] = make_float2(sr_fmt<SF>(a3.x, r1.z), sr_fmt<SF>(a3.y, r1.w));
+  w[0] = make_float2(sr_fmt<SF>(b0.x, r2.x), sr_fmt<SF>(b0.y, r2.y));
+  w[1] = make_float2(sr_fmt<SF>(b1.x, r2.z), sr_fmt<SF>(b1.y, r2.w));
+  w[2] = make_float2(sr_fmt<SF>(b2.x, r3.x), sr_fmt<SF>(b2.y, r3.y));
+  w[3] = make_float2(sr_fmt<SF>(b3.x, r3.z), sr_fmt<SF>(b3.y, r3.w));
+  return RawPair<SF>{pack_vec_rne<SF>(v), pack_vec_rne<SF>(w)};
+}
+
 // One item with a non-empty prefix on the CUDA cores: the decay scan, the
 // prefix applied to this thread's [RPT rows x VEC columns] of the tile in
 // closed form (the tokens converted kTokChunk at a time into the warp's fp32
@@ -738,22 +773,7 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
         for (int u = 0; u < V2; ++u) acc[r][u] = __fmul2_rn(acc[r][u], inv2);
       }
     }
-#pragma unroll
-    for (int r = 0; r < RPT; ++r) {
-      if (!worker) continue;
-      Raw out;
-      bool use_sr = false;
-      if constexpr (SF != RSM_F32) use_sr = sr;
-      if (use_sr) {
-        if constexpr (SF != RSM_F32) {
-          static_assert(V2 == 4, "stochastic rounding works on 8-element vectors");
-          const int64_t e0 = (static_cast<int64_t>(h) * D + row0 + r) * N + col0;
-          out = sr_pack8<SF>(acc[r][0], acc[r][1], acc[r][2], acc[r][3], static_cast<uint32_t>(e0 >> 2), dst_slot_id,
-                             layer_id, key0, key1, p.philox_rounds);
-        }
-      } else {
-        out = pack_vec_rne<SF>(acc[r]);
-      }
+    auto store_row = [&](int r, Raw out) {
       if constexpr (Q) {
         if (zero_rows[r]) out = Raw{};
       }
@@ -762,6 +782,38 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
         stg_stream(dst_tile + off, out);
       else
         store_bytes(dst_tile + off, out);
+    };
+    bool use_sr = false;
+    if constexpr (SF != RSM_F32) use_sr = sr;
+    if (worker) {
+      if (use_sr) {
+        if constexpr (SF != RSM_F32) {
+          // Philox counter of element e: (e / 4, dst_slot, layer, 0); a row's
+          // 8 elements start on a multiple of 8
+          static_assert(V2 == 4, "stochastic rounding works on 8-element vectors");
+          const uint32_t blk0 = static_cast<uint32_t>(((static_cast<int64_t>(h) * D + row0) * N + col0) >> 2);
+          constexpr uint32_t kRowBlocks = N / 4;
+          if constexpr (RPT % 2 == 0) {
+#pragma unroll
+            for (int r = 0; r < RPT; r += 2) {
+              const RawPair<SF> o = sr_pack8x2<SF>(acc[r][0], acc[r][1], acc[r][2], acc[r][3], acc[r + 1][0],
+                                                   acc[r + 1][1], acc[r + 1][2], acc[r + 1][3], blk0 + r * kRowBlocks,
+                                                   blk0 + (r + 1) * kRowBlocks, dst_slot_id, layer_id, key0, key1,
+                                                   p.philox_rounds);
+              store_row(r, o.a);
+              store_row(r + 1, o.b);
+            }
+          } else {
+#pragma unroll
+            for (int r = 0; r < RPT; ++r)
+              store_row(r, sr_pack8<SF>(acc[r][0], acc[r][1], acc[r][2], acc[r][3], blk0 + r * kRowBlocks,
+                                        dst_slot_id, layer_id, key0, key1, p.philox_rounds));
+          }
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) store_row(r, pack_vec_rne<SF>(acc[r]));
+      }
     }
     if constexpr (Q) {
       if (lane_col % RSPAN == 0) {
