@@ -132,7 +132,7 @@ __device__ __forceinline__ void run_consumer_tc(const Params& p, unsigned char* 
         }
       }
     } else if (k < p.tc_min_k) {
-      replay_ffma<SF, RSM_BF16, 64, 128>(p, sb, il, desc, k, wbuf, cbuf, cw, lane, empty_bar, key0, key1, sr);
+      replay_ffma<SF, RSM_BF16, 64, 128, true>(p, sb, il, desc, k, wbuf, cbuf, cw, lane, empty_bar, key0, key1, sr);
       prev_tc = false;
     } else {
       // decay of each token, once per warp (as in the materialization kernel)
