@@ -343,6 +343,22 @@ def test_tensor_core_prefix_lengths(sd, k):
     check(hw)
 
 
+@pytest.mark.parametrize("sd", ["bf16", "f16"])
+def test_tensor_core_mixed_prefixes_many_units_per_cta(sd):
+    """Prefixes U[0,64] over ~3 (request, layer, head-run) units per CTA:
+    copies, CUDA-core items and tensor-core items follow one another inside a
+    CTA, the tensor-core items alternate between the two consumer groups, and
+    B^T is reused across groups within a B group."""
+    shape = wl.Shape("tcmix", L=2, Bt=64, H=32, hpg=8, D=64, N=128, R=64, W=64, state_dtype=sd, n_active=60,
+                     ring_start=(0, 64), prefix=("uniform", 0, 64), pad_frac=0.05)
+    hw = wl.host_world(shape, seed=91)
+    for i in (3, 17):  # two exact copies among them
+        hw.replay_prefix_len[int(hw.active[i])] = 0
+    k = np.asarray(hw.replay_prefix_len)[np.asarray(hw.active)[:60]]
+    assert (k == 0).any() and ((k > 0) & (k < 10)).any() and (k >= 10).any()
+    assert check(hw) >= 100
+
+
 def test_tensor_core_misaligned_destination():
     """Destination tiles 2 bytes off a 16-byte boundary: the staged tile is
     written with byte stores."""
