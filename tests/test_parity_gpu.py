@@ -156,6 +156,32 @@ def test_requantization_is_bit_exact_when_state_is_unchanged(sd, rounds):
     check(hw, exact=True)
 
 
+@pytest.mark.parametrize("sd", ["i8", "fp8_e4m3"])
+@pytest.mark.parametrize("rounds", [0, 10])
+def test_one_byte_rows_without_a_finite_scale_become_zero(sd, rounds):
+    """A row that replays to exact zeros (zero codes, zero x) and a row that
+    replays to fp32 subnormals (zero codes, x ~ 1e-38): qmax/amax is not finite
+    for both, so both are written as zero codes (+0 for fp8) with scale 0, on
+    either rounding path; the other rows of the tile are ordinary."""
+    shape = wl.Shape("zrow", L=1, Bt=4, H=4, hpg=2, D=64, N=128, R=8, W=8, state_dtype=sd, n_active=4,
+                     prefix=("fixed", 5), philox_rounds=rounds, rand_seed=0x5EED)
+    hw = wl.host_world(shape, seed=61)
+    b = int(hw.active[0])
+    src, dst = int(hw.src_slots[0, b]), int(hw.dst_slots[0, b])
+    h, zero_row, tiny_row = 1, 5, 9
+    hw.state[0][src, h, zero_row, :] = 0
+    hw.state[0][src, h, tiny_row, :] = 0
+    hw.x[0][src, :, h, zero_row] = 0
+    hw.x[0][src, :, h, tiny_row] = wl.bf16_bits_from_f32(np.full(shape.R, 1e-38, np.float32))
+    got, ref = run_cuda(hw), run_oracle(hw)
+    for w in (got, ref):
+        for r in (zero_row, tiny_row):
+            assert not w.state[0][dst, h, r].any(), f"row {r}: codes not zero"
+            assert w.scale[0][dst, h, r] == 0.0, f"row {r}: scale not zero"
+        assert w.state[0][dst, h, 0].any()
+    compare_worlds(got, ref, hw)
+
+
 # ----------------------------------------------------------------------------
 # edge cases
 # ----------------------------------------------------------------------------
