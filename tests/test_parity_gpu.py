@@ -355,6 +355,64 @@ def test_headline_full_size_sampled():
     torch.cuda.empty_cache()
 
 
+FULL = [
+    ("hybrid48_int8", {}),
+    ("hybrid48_int8", {"state_dtype": "fp8_e4m3"}),
+    ("mamba2_2p7b_fp32", {}),
+    ("ring_sweep_fp16", {"prefix": ("fixed", 16)}),
+    ("ring_sweep_fp16", {"prefix": ("fixed", 64)}),
+]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,over", FULL, ids=["int8", "fp8_rne", "mamba2_fp32", "ring_k16", "ring_k64"])
+def test_named_workload_full_size_sampled(name, over):
+    """The benchmark's other workloads at full size and in its launch
+    configuration (one-byte state, fp32 state with ring wrap, the 64-token
+    window on the tensor cores), checked on sampled (layer, request) outputs
+    that the oracle recomputes one by one, and on the bytes of pads."""
+    shape = wl.SHAPES[name].replace(**over)
+    assert shape.philox_rounds == 0
+    dw = wl.device_world_random(shape, seed=3)
+    rsm.replayssm_materialize(**dw.call_kwargs())
+    torch.cuda.synchronize()
+    assert int(dw.status.item()) == 0
+    n = shape.n_active
+    live = dw.active.cpu().numpy()[:n]
+    prefix = dw.replay_prefix_len.cpu().numpy()
+    src = dw.src_slots.cpu().numpy()
+    dst = dw.dst_slots.cpu().numpy()
+    pad = shape.pad_slot_id
+    sd = shape.state_dtype
+    rng = np.random.default_rng(7)
+    picks = [(int(rng.integers(shape.L)), int(live[int(rng.integers(n))])) for _ in range(6)]
+    picks.append((shape.L - 1, int(live[-1])))
+    checked = 0
+    for l, b in picks:
+        if src[l, b] == pad or dst[l, b] == pad:
+            continue
+        sub = wl.host_subworld(dw, l, b)
+        oracle.materialize(sub)
+        got = wl._to_np(dw.state[l][dst[l, b]])
+        ref = sub.state[0][1]
+        gs = None if dw.scale[l] is None else wl._to_np(dw.scale[l][dst[l, b]])
+        rs = None if sub.scale[0] is None else sub.scale[0][1]
+        if prefix[b] == 0:
+            assert got.tobytes() == ref.tobytes()
+            assert gs is None or gs.tobytes() == rs.tobytes()
+        else:
+            compare_slot(got, ref, sd, gs, rs, where=f"{name} layer {l} request {b}")
+        checked += 1
+    assert checked >= 4
+    # a destination whose (layer, request) is padded on the source side stays as it was (0xFF)
+    for l in range(shape.L):
+        for b in live[:16]:
+            if src[l, b] == pad and dst[l, b] != pad:
+                assert bool((dw.state[l][dst[l, b]].view(torch.uint8) == 0xFF).all())
+    del dw
+    torch.cuda.empty_cache()
+
+
 # ----------------------------------------------------------------------------
 # long windows: the tensor-core path (16-bit state, bf16 inputs, 64 x 128,
 # windows of 16 or more; prefixes of 10 tokens or more go through the MMA)
