@@ -54,7 +54,7 @@ def parse_args():
     p.add_argument("--no-extras", action="store_true", help="skip the n sweep, empty latency, e2e and CPU baseline")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work for the oracle baseline sample")
     p.add_argument("--e2e-requests", type=int, default=16)
-    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--all-workloads", action="store_true",
                    help="also measure the other named workloads (added under 'workloads')")
     p.add_argument("--gdn", action="store_true",
@@ -391,7 +391,7 @@ def e2e_measure(torch, rsm, shape, n_req, steps, device, groups=8):
                 ev_out[g].record(s_out)
         first[0] = False
 
-    for _ in range(2):
+    for _ in range(3):
         one_step()
     torch.cuda.synchronize()
     t0 = time.perf_counter()

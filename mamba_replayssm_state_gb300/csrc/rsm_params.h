@@ -95,12 +95,12 @@ __host__ __device__ constexpr uint32_t arena_next(uint32_t head, uint32_t item_m
 }
 
 // Shared memory of the tensor-core (long-window) variant: the same head up to
-// kWarpBufOff, then its mbarriers (MMA completion, three consumer-wide
-// barriers, exit) and the TMEM address word, the two MMA operands, the
+// kWarpBufOff, then its mbarriers (MMA completion, two consumer-wide
+// barriers and a spare, exit) and the TMEM address word, the two MMA operands, the
 // descriptor table and the arena.
 constexpr int kTcMinWindow = 16;                  // tensor path for max_window >= this (16-bit state)
 constexpr int kTcKMax = kMaxWindow;               // tokens one item's MMA covers at most
-constexpr uint32_t kTcBarOff = kWarpBufOff;       // mma, x1, x2, x3, done mbarriers (+0 .. +39), x4 (+48)
+constexpr uint32_t kTcBarOff = kWarpBufOff;       // mma, x1, x2, (spare), exit mbarriers (+0 .. +39)
 constexpr uint32_t kTcTmemSlot = kTcBarOff + 40;  // TMEM base address written by tcgen05.alloc
 constexpr uint32_t kTcAOff = kTcBarOff + 128;     // A = B^T: [128 dstate rows][kTcKMax tokens] bf16 core matrices
 constexpr uint32_t kTcBOff = kTcAOff + 128 * kTcKMax * 2;  // C^T: [64 dim rows][kTcKMax tokens] bf16
@@ -108,7 +108,6 @@ constexpr uint32_t kTcSbo = (kTcKMax / 8) * 128;  // bytes between 8-row groups 
 constexpr uint32_t kTcTmemCols = 64;              // fp32 accumulator: 128 lanes x 64 columns
 constexpr uint32_t kTcDescBase = round_up(kTcBOff + 64 * kTcKMax * 2, 128u);
 constexpr uint32_t kTcArenaBase = round_up(kTcDescBase + kMaxStages * kDescBytes, 128u);
-static_assert(128 * kTcKMax * 2 >= 64 * 128 * 2, "the A operand doubles as the output staging tile");
 constexpr int kTcMinK = 10;  // shorter prefixes are applied on the CUDA cores (measured crossover)
 
 struct Params {

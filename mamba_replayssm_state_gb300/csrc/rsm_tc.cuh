@@ -100,4 +100,10 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(r[c]);
 }
 
+// Streaming 2-byte store: one element of a 16-bit state tile (a warp's 32
+// lanes write 64 contiguous bytes of a tile row).
+__device__ __forceinline__ void stg16_stream(void* p, uint16_t v) {
+  asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p), "h"(v) : "memory");
+}
+
 }  // namespace rsm
