@@ -316,6 +316,32 @@ def test_repeated_calls_are_identical():
         assert a.scale[l].tobytes() == b.scale[l].tobytes()
 
 
+def test_prepared_call_replays_from_a_cuda_graph():
+    """The call enqueues one kernel and nothing else (no allocation, no copy,
+    no host sync), so a prepared call can be captured in a CUDA graph: the
+    capture writes nothing, and a replay writes what the oracle writes."""
+    shape = wl.Shape("graph", L=2, Bt=5, H=6, hpg=3, D=64, N=128, R=8, W=8, state_dtype="bf16", n_active=4,
+                     prefix=("uniform", 0, 8))
+    hw = wl.host_world(shape, seed=123)
+    warm = wl.device_world_from_host(hw)  # the host-side launch plan is set up outside the capture
+    rsm.prepare(**warm.call_kwargs())()
+    torch.cuda.synchronize()
+    dw = wl.device_world_from_host(hw)
+    call = rsm.prepare(**dw.call_kwargs())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    torch.cuda.synchronize()
+    for l in range(hw.L):
+        assert wl._to_np(dw.state[l]).tobytes() == hw.state[l].tobytes(), "capture must not run the kernel"
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(dw.status.item()) == 0
+    got = hw.copy()
+    got.state = [wl._to_np(t).view(a.dtype) for t, a in zip(dw.state, hw.state)]
+    compare_worlds(got, run_oracle(hw), hw)
+
+
 # ----------------------------------------------------------------------------
 # full size: the 48-layer x 256-head x 64x128 bf16 call that the benchmark times
 # ----------------------------------------------------------------------------
