@@ -50,6 +50,7 @@ class OracleArgs(ctypes.Structure):
         ("heads_per_group", ctypes.c_int32), ("max_window", ctypes.c_int32),
         ("ring_buffer_len", ctypes.c_int32), ("pad_slot_id", ctypes.c_int32),
         ("philox_rounds", ctypes.c_int32),
+        ("sr_counter_slots", _P32), ("sr_counter_layers", _P32),
     ]
 
 
@@ -161,6 +162,12 @@ def materialize(world) -> None:
     args.ring_buffer_len = world.R
     args.pad_slot_id = world.pad_slot_id
     args.philox_rounds = world.philox_rounds
+    # a one-request copy of a larger call (workloads.host_subworld) names the
+    # destination slot and layer of that call: the Philox counter uses them
+    meta = getattr(world, "meta", None) or {}
+    if "dst_slot_in_call" in meta:
+        args.sr_counter_slots = tab32(np.full((world.L, world.Bt), meta["dst_slot_in_call"], np.int32))
+        args.sr_counter_layers = tab32(np.full(world.L, meta["layer_in_call"], np.int32))
     rc = L.oracle_materialize(ctypes.byref(args))
     if rc != 0:
         raise ValueError("oracle: " + L.oracle_last_error().decode())

@@ -368,7 +368,8 @@ static double load_input(const void *base, int64_t idx, int fmt) {
   return oracle_decode(fmt, load_bits(base, idx, fmt));
 }
 
-/* Writes one head's [dim, dstate] fp64 state S to the destination tile. */
+/* Writes one head's [dim, dstate] fp64 state S to the destination tile;
+ * (layer, dst) are the Philox counter's layer and slot words. */
 static void write_head(const oracle_args *a, int layer, int32_t dst, int64_t h,
                        const double *S, void *dst_state, float *dst_scale) {
   const int fmt = a->state_dtype;
@@ -431,6 +432,9 @@ int oracle_materialize(const oracle_args *a) {
     for (int32_t l = 0; l < a->num_layers; ++l) {
       const int32_t src = a->src_slots[(int64_t)l * a->batch + b];
       const int32_t dst = a->dst_slots[(int64_t)l * a->batch + b];
+      /* the Philox counter's slot and layer words (reading 11) */
+      const int32_t ctr_slot = a->sr_counter_slots ? a->sr_counter_slots[(int64_t)l * a->batch + b] : dst;
+      const int ctr_layer = a->sr_counter_layers ? a->sr_counter_layers[l] : l;
       if (src == a->pad_slot_id || dst == a->pad_slot_id) continue;
 
       unsigned char *state = (unsigned char *)(intptr_t)a->state_ptrs[l];
@@ -489,7 +493,7 @@ int oracle_materialize(const oracle_args *a) {
             }
           }
         }
-        write_head(a, l, dst, h, S, dst_state, dst_scale);
+        write_head(a, ctr_layer, ctr_slot, h, S, dst_state, dst_scale);
       }
     }
   }

@@ -50,6 +50,12 @@ typedef struct oracle_args {
   int64_t num_heads;
   int32_t heads_per_group, max_window, ring_buffer_len, pad_slot_id;
   int32_t philox_rounds;
+  /* Optional, NULL when unused: the slot and layer words of the Philox
+   * counter are taken from these tables ([L, batch] and [L]) instead of the
+   * destination slot and the layer index of this call.  A one-request copy of
+   * a larger call then draws the random words that call draws. */
+  const int32_t *sr_counter_slots;
+  const int32_t *sr_counter_layers;
 } oracle_args;
 
 /* 0 on success; <0 when an argument or a metadata value is out of contract

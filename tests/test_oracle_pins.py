@@ -509,6 +509,30 @@ def test_stochastic_rounding_is_unbiased(fmt, y):
 # Philox
 # ----------------------------------------------------------------------------
 
+@pytest.mark.parametrize("sd", ["bf16", "fp8_e4m3"])
+def test_one_request_copy_draws_the_calls_philox_words(sd):
+    """With the counter's slot and layer taken from the original call, the
+    oracle on a one-request copy of (layer, request) writes the same bytes as
+    the oracle on the whole call (stochastic rounding on)."""
+    shape = wl.Shape("srsub", L=3, Bt=5, H=4, hpg=2, D=16, N=16, R=8, W=8, state_dtype=sd, n_active=4,
+                     philox_rounds=10, rand_seed=0x5EED, prefix=("uniform", 1, 8))
+    hw = wl.host_world(shape, seed=17)
+    full = hw.copy()
+    oracle.materialize(full)
+    dw = wl.device_world_from_host(hw, device="cpu")
+    for l, i in ((2, 0), (1, 3)):
+        b = int(hw.active[i])
+        sub = wl.host_subworld(dw, l, b)
+        oracle.materialize(sub)
+        dst = int(hw.dst_slots[l, b])
+        assert sub.state[0][1].tobytes() == full.state[l][dst].tobytes()
+        # without the remap the words differ, and so do some rounded values
+        plain = wl.host_subworld(dw, l, b)
+        plain.meta = {}
+        oracle.materialize(plain)
+        assert plain.state[0][1].tobytes() != full.state[l][dst].tobytes()
+
+
 def test_philox_known_answer_vectors():
     kat = json.load(open(os.path.join(GOLDEN, "philox4x32_kat.json")))
     for v in kat["vectors"]:
