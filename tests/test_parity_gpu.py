@@ -143,6 +143,36 @@ def test_stochastic_rounding_every_format(sd):
     check(hw)
 
 
+def test_stochastic_rounding_is_unbiased_over_seeds():
+    """Over 48 seeds the bf16 outputs average to the unrounded result: the
+    summed error, over 4096 elements and all seeds, is within 5 standard
+    deviations of zero (each element's variance frac*(1-frac)*spacing^2)."""
+    shape = wl.Shape("srstat", L=1, Bt=4, H=4, hpg=2, D=16, N=16, R=8, W=8, state_dtype="bf16", n_active=4,
+                     prefix=("fixed", 4), philox_rounds=10, rand_seed=1)
+    hw = wl.host_world(shape, seed=5)
+    as_f32 = lambda bits: (bits.astype(np.uint32) << 16).view(np.float32)
+    # the unrounded result: the same call with the bf16 source decoded into an fp32 state
+    hw32 = hw.copy()
+    hw32.shape = shape.replace(state_dtype="f32", philox_rounds=0)
+    hw32.state = [as_f32(a) for a in hw.state]
+    oracle.materialize(hw32)
+    dsts = [int(hw.dst_slots[0, b]) for b in hw.active if b >= 0]
+    ref = np.stack([hw32.state[0][d] for d in dsts]).astype(np.float64)
+    mag = np.abs(ref)
+    spacing = np.exp2(np.floor(np.log2(np.where(mag > 0, mag, 1.0))) - 7)
+    frac = mag / spacing - np.floor(mag / spacing)
+    var = frac * (1 - frac) * spacing ** 2
+    seeds = 48
+    err = np.zeros_like(ref)
+    for s in range(seeds):
+        w = hw.copy()
+        w.rand_seed = 1000 + s
+        got = run_cuda(w)
+        err += np.stack([as_f32(got.state[0][d]) for d in dsts]).astype(np.float64) - ref
+    z = err.sum() / np.sqrt(seeds * var.sum())
+    assert abs(z) < 5.0, z
+
+
 @pytest.mark.parametrize("sd", ["bf16", "f16", "i8", "fp8_e4m3"])
 @pytest.mark.parametrize("rounds", [0, 10])
 def test_requantization_is_bit_exact_when_state_is_unchanged(sd, rounds):
