@@ -108,7 +108,7 @@ constexpr uint32_t kTcSbo = (kTcKMax / 8) * 128;  // bytes between 8-row groups 
 constexpr uint32_t kTcTmemCols = 64;              // fp32 accumulator: 128 lanes x 64 columns
 constexpr uint32_t kTcDescBase = round_up(kTcBOff + 64 * kTcKMax * 2, 128u);
 constexpr uint32_t kTcArenaBase = round_up(kTcDescBase + kMaxStages * kDescBytes, 128u);
-constexpr int kTcMinK = 10;  // shorter prefixes are applied on the CUDA cores (measured crossover)
+constexpr int kTcMinK = 7;  // shorter prefixes are applied on the CUDA cores (measured crossover)
 
 struct Params {
   const int64_t* state_ptrs;

@@ -473,11 +473,11 @@ def test_named_workload_full_size_sampled(name, over):
 
 # ----------------------------------------------------------------------------
 # long windows: the tensor-core path (16-bit state, bf16 inputs, 64 x 128,
-# windows of 16 or more; prefixes of 10 tokens or more go through the MMA)
+# windows of 16 or more; prefixes of 7 tokens or more go through the MMA)
 # ----------------------------------------------------------------------------
 
 @pytest.mark.parametrize("sd", ["bf16", "f16"])
-@pytest.mark.parametrize("k", [9, 10, 15, 17, 31, 33, 63])
+@pytest.mark.parametrize("k", [6, 7, 9, 10, 15, 17, 31, 33, 63])
 def test_tensor_core_prefix_lengths(sd, k):
     shape = wl.Shape("tc", L=2, Bt=4, H=8, hpg=4, D=64, N=128, R=64, W=64, state_dtype=sd, n_active=4,
                      ring_start=(0, 64), prefix=("fixed", k))
@@ -497,7 +497,7 @@ def test_tensor_core_mixed_prefixes_many_units_per_cta(sd):
     for i in (3, 17):  # two exact copies among them
         hw.replay_prefix_len[int(hw.active[i])] = 0
     k = np.asarray(hw.replay_prefix_len)[np.asarray(hw.active)[:60]]
-    assert (k == 0).any() and ((k > 0) & (k < 10)).any() and (k >= 10).any()
+    assert (k == 0).any() and ((k > 0) & (k < 7)).any() and (k >= 7).any()
     assert check(hw) >= 100
 
 
