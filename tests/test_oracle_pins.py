@@ -408,6 +408,21 @@ def test_zero_row_gets_zero_scale():
     assert np.all(w1.state[0][dst, 0, 5] == 0)
 
 
+@pytest.mark.parametrize("sd", ["i8", "fp8_e4m3"])
+def test_subnormal_row_gets_zero_scale(sd):
+    """A row that replays to fp32 subnormals (zero codes, x ~ 1e-38) has a
+    finite non-zero amax, but qmax/amax overflows fp32: zero codes (+0), scale 0."""
+    w0 = single_request_world(seed=54, state_dtype=sd, input_dtype="bf16", D=64, N=128, H=1, hpg=1)
+    w0.state[0][0, 0, 7, :] = 0
+    w0.x[0][0, :, 0, 7] = wl.bf16_bits_from_f32(np.full(w0.x[0].shape[1], 1e-38, np.float32))
+    w0.replay_prefix_len[0] = 3
+    w1 = run(w0)
+    dst = int(w0.dst_slots[0, 0])
+    assert w1.scale[0][dst, 0, 7] == 0.0
+    assert not w1.state[0][dst, 0, 7].any()
+    assert w1.scale[0][dst, 0, 6] > 0.0
+
+
 # ----------------------------------------------------------------------------
 # element formats and rounding, against library casts
 # ----------------------------------------------------------------------------
