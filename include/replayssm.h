@@ -133,8 +133,11 @@ typedef struct rsm_materialize_args {
  *
  * Rounding of the written state: fp32 as is; bf16/fp16 round to nearest even;
  * one-byte state rewrites each (head, dim-row) with scale = amax/qmax and
- * codes = round(value * (qmax/amax)) (qmax 127 or 448, saturating), a row whose
- * qmax/amax is not finite becoming zero codes with scale 0.  With
+ * codes = round(value / scale) (qmax 127 or 448, saturating), a row whose
+ * qmax/amax is not finite becoming zero codes with scale 0.  The kernel forms
+ * the quotient as value * (qmax/amax), so a code can sit one step from the
+ * rounded quotient when the quotient lies within an fp32 ulp of a rounding
+ * boundary.  With
  * philox_rounds > 0 every non-fp32 format rounds stochastically instead: the
  * magnitude goes up with probability equal to its distance from the lower
  * neighbour over the grid spacing, driven by Philox-4x32 (philox_rounds

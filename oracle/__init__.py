@@ -11,10 +11,11 @@ The operation follows the flashinfer.mamba.replayssm_materialize API page
 listed at the top of replayssm_oracle.c.
 
 Parity status: every function here is pinned by tests/test_oracle_pins.py
-(closed form, copy, composition, ring wrap, pad/-1 skipping, brute force over
-ring_start x prefix, format conversions against numpy/torch, Philox against
-the published known-answer vectors).  The Philox counter layout itself is this
-build's own convention and has no external vector.
+and tests/test_oracle_gdn_pins.py (closed form, copy, composition, ring wrap,
+pad/-1 skipping, brute force over ring_start x prefix, format conversions
+against numpy/torch, Philox against the published known-answer vectors, the
+stochastic-rounding counter layout and the one-byte quotient through stored
+bytes predicted from their written statements, the GDN epsilon placement).
 """
 import ctypes
 import os

@@ -29,8 +29,9 @@
  *    the delta correction against the decayed state);
  *  - value heads map to key heads in contiguous groups: h = hv / (HV/H);
  *  - window position t holds accepted token t (the cache is not shifted);
- *  - the epsilon of the K normalisation sits inside the square root (parity
- *    unpinned: no pin tells this from other placements of the epsilon);
+ *  - the epsilon of the K normalisation sits inside the square root (pinned
+ *    by a key of squared norm 2^-20, where the other placements of the
+ *    epsilon give results 30% or more apart);
  *  - evaluation in fp64, each stored value rounded once to fp32.
  */
 #include "gdn_commit_oracle.h"

@@ -31,9 +31,10 @@
  *  - head h uses B group h / heads_per_group;
  *  - dt in the cache is the final fp32 step size, A the final (negative) value;
  *  - one-byte state is symmetric, one fp32 scale per (head, dim-row):
- *    scale = amax/qmax, codes = round(v * (qmax/amax)), qmax 127 (int8) or
- *    448 (fp8 e4m3fn); a row whose qmax/amax is not finite (amax == 0 or
- *    tiny) is stored as zero codes with scale 0;
+ *    scale = amax/qmax and codes = round(v / scale), the plain quotient, both
+ *    fp32 operations, with qmax 127 (int8) or 448 (fp8 e4m3fn); a row whose
+ *    qmax/amax is not finite (amax == 0, or so small that the scale cannot
+ *    be inverted in fp32) is stored as zero codes with scale 0;
  *  - stochastic rounding: Philox-4x32 with philox_rounds rounds,
  *    key = (lo32(seed), hi32(seed)), counter = (e>>2, dst_slot, layer, 0) with
  *    e = (h*dim + i)*dstate + j, word e&3; round the magnitude up iff
@@ -394,15 +395,14 @@ static void write_head(const oracle_args *a, int layer, int32_t dst, int64_t h,
         amax = fmaxf(amax, fabsf(v));
       }
       float scale = amax / qmax;
-      float inv = qmax / amax;
-      if (!(inv <= FLT_MAX)) { /* amax == 0 or so small that qmax/amax overflows */
+      if (!(qmax / amax <= FLT_MAX)) { /* amax == 0 or so small that qmax/amax overflows */
         for (int j = 0; j < N; ++j) store_bits(dst_state, row + j, fmt, 0u);
         dst_scale[h * D + i] = 0.0f;
         continue;
       }
       for (int j = 0; j < N; ++j) {
         float v = (float)S[i * N + j];
-        float y = v * inv;
+        float y = v / scale; /* the code in units of the scale, one fp32 division */
         uint32_t w = sr ? sr_word(a, layer, dst, row + j) : 0u;
         store_bits(dst_state, row + j, fmt, oracle_encode(fmt, oracle_round(fmt, y, sr, w)));
       }

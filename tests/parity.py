@@ -7,6 +7,12 @@ Tolerances (the |gpu - ref| <= tol + tol*|ref| form):
                    within the fp32 tolerance
 Slots that are not written (pads, entries after the first -1, untouched pool
 slots) and prefix-0 copies must be bit-identical.
+
+One-byte codes: the oracle rounds the plain quotient v / scale, the kernel the
+product v * (qmax / amax); the two differ by an fp32 ulp at most, which moves a
+code by one step only when the quotient sits next to a rounding boundary.  So
+even where the state itself is exact (compare_worlds(exact=True)), codes are
+compared within one step, and at most 0.1% of them may differ at all.
 """
 import numpy as np
 
@@ -79,6 +85,12 @@ def compare_worlds(got, ref, before, exact=False):
             key = (l, slot)
             if key in written and written[key][1] > 0 and not exact:
                 compare_slot(g, r, sd, gs, rs, where=f"layer {l} slot {slot}")
+                n_written += 1
+            elif key in written and written[key][1] > 0 and sd in ("i8", "fp8_e4m3"):
+                dist = np.abs(_ordered_code(g, sd) - _ordered_code(r, sd))
+                assert dist.max() <= 1, f"layer {l} slot {slot}: code distance {dist.max()}"
+                assert (dist > 0).mean() <= 1e-3, f"layer {l} slot {slot}: {(dist > 0).mean():.2e} of codes differ"
+                assert gs.tobytes() == rs.tobytes(), f"layer {l} slot {slot}: scale bytes differ"
                 n_written += 1
             else:
                 assert g.tobytes() == r.tobytes(), f"layer {l} slot {slot}: bytes differ (copy/untouched)"

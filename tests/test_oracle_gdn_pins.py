@@ -200,3 +200,28 @@ def test_value_head_inputs_reach_only_their_head(which):
     out, base = run(pert), run(w)
     changed = [hv for hv in range(4) if not np.array_equal(out.state[0, s, hv], base.state[0, s, hv])]
     assert changed == [1]
+
+
+def test_epsilon_sits_inside_the_square_root():
+    """GDN page, Parameters, use_qk_l2norm: K is normalised with epsilon 1e-6.
+    The reading fixed here is k^ = k / sqrt(|k|^2 + 1e-6).  With S0 = 0 and
+    g = 0, one token leaves S1 = beta v k^T, so column c of S1 over beta v is
+    k^'s entry c.  With |k|^2 = 2^-20 (about the epsilon) the placements differ
+    by a factor near sqrt(2): inside the root 2^-10 / sqrt(2^-20 + 1e-6) = 0.716,
+    added to the norm 2^-10 / (2^-10 + 1e-6) = 0.999, left out 1."""
+    w = one_head_world(seed=15)
+    s = int(w.state_indices[0])
+    w.state[0, s, 0] = 0.0
+    w.g[0, s, 0, 0] = 0.0
+    k = np.zeros(DK, np.float32)
+    k[5] = 2.0 ** -10                           # exact in bf16; |k|^2 = 2^-20
+    w.rawk[0, s, 0, 0] = bf16(k)
+    v = f(w.rawv[0, s, 0, 0])
+    beta = np.float64(w.beta[0, s, 0, 0])
+    S1 = run(w).state[0, s, 0].astype(np.float64)
+    inside = 2.0 ** -10 / np.sqrt(2.0 ** -20 + 1e-6)
+    np.testing.assert_allclose(S1[:, 5], beta * v * inside, rtol=1e-6, atol=1e-30)
+    assert not np.any(np.delete(S1, 5, axis=1))
+    # the other placements are far outside that tolerance
+    for other in (2.0 ** -10 / (2.0 ** -10 + 1e-6), 1.0):
+        assert abs(other / inside - 1.0) > 0.3

@@ -391,10 +391,70 @@ def test_requantization_error_bound(sd):
     s1 = w1.scale[0][dst]
     assert np.array_equal(s1, (amax / np.float32(qmax)).astype(np.float32))
     assert np.all(np.abs(c1).max(axis=-1) == qmax)
-    # exact y = v/scale; the stored y was formed as fp32 v * fp32(qmax/amax), which is
-    # within a few fp32 ulps (relative 2^-22) of it
+    # exact y = v/scale; the stored code rounds the fp32 quotient, which is within
+    # half an fp32 ulp (relative 2^-24) of it
     y = v / s1[..., None].astype(np.float64)
-    assert np.all(np.abs(c1 - y) <= _grid_half_ulp(sd, y) + 2.0 ** -21 * np.abs(y) + 1e-9)
+    assert np.all(np.abs(c1 - y) <= _grid_half_ulp(sd, y) + 2.0 ** -23 * np.abs(y))
+
+
+def _rne_fraction_on_grid(q, grid):
+    """Round the exact rational q to the nearest value of the sorted finite grid
+    (non-negative values, mirrored for negatives), ties to the even grid index."""
+    from fractions import Fraction
+    sign = -1 if q < 0 else 1
+    a = abs(q)
+    vals = [Fraction(v) for v in grid]
+    if a >= vals[-1]:
+        return sign * vals[-1]
+    hi = next(i for i, v in enumerate(vals) if v >= a)
+    if vals[hi] == a:
+        return sign * vals[hi]
+    lo = hi - 1
+    dlo, dhi = a - vals[lo], vals[hi] - a
+    pick = lo if dlo < dhi else hi if dhi < dlo else (lo if lo % 2 == 0 else hi)
+    return sign * vals[pick]
+
+
+@pytest.mark.parametrize("sd,row", [("i8", (1.125, 0.5625)), ("fp8_e4m3", (1.53125, 0.79296875))])
+def test_code_is_the_rounded_quotient_by_the_stored_scale(sd, row):
+    """One-byte state: code = round(v / scale) with scale = amax / qmax, the plain
+    quotient (reading 9).  The row below is one where that quotient lies within
+    an fp32 ulp of a rounding boundary, so the inverse-scale product v * (qmax/amax)
+    lands on the other side; the expected code is the exact rational v / scale
+    rounded to the format's grid (ties to even)."""
+    import torch
+    from fractions import Fraction
+    w0 = single_request_world(seed=55, state_dtype=sd, input_dtype="bf16", H=1, hpg=1, D=16, N=16)
+    h, i = 0, 3
+    w0.A[0][:] = 0.0                      # decay exactly 1
+    w0.dt[0][:] = 0.0625                  # S_1 = S_0 + x B^T / 16, exact
+    w0.state[0][0, h, i, :] = 0           # the row starts at zero codes
+    w0.x[0][0, 0, h, i] = wl.bf16_bits_from_f32(np.float32([1.0]))[0]
+    brow = np.zeros(16, np.float32)
+    brow[0], brow[1] = row
+    w0.B[0][0, 0, 0] = wl.bf16_bits_from_f32(brow)
+    w0.ring_start[0] = 0
+    w0.replay_prefix_len[0] = 1
+    w1 = run(w0)
+    dst = int(w0.dst_slots[0, 0])
+    qmax = 127.0 if sd == "i8" else 448.0
+    v = [Fraction(float(b)) / 16 for b in brow]
+    amax = max(abs(x) for x in v)
+    scale = np.float32(np.float32(float(amax)) / np.float32(qmax))
+    assert w1.scale[0][dst, h, i] == scale
+    if sd == "i8":
+        grid = list(range(128))
+        got = [Fraction(int(c)) for c in w1.state[0][dst, h, i]]
+    else:
+        vals = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+        grid = sorted(set(float(x) for x in vals))
+        dec = torch.from_numpy(w1.state[0][dst, h, i].copy()).view(torch.float8_e4m3fn).double().numpy()
+        got = [Fraction(float(c)) for c in dec]
+    want = [_rne_fraction_on_grid(x / Fraction(float(scale)), grid) for x in v]
+    assert got == want
+    # the inverse-scale product would have rounded element 1 to the neighbouring code
+    inv_prod = np.float32(np.float32(float(v[1])) * np.float32(np.float32(qmax) / np.float32(float(amax))))
+    assert _rne_fraction_on_grid(Fraction(float(inv_prod)), grid) != want[1]
 
 
 def test_zero_row_gets_zero_scale():
@@ -546,6 +606,133 @@ def test_one_request_copy_draws_the_calls_philox_words(sd):
         plain.meta = {}
         oracle.materialize(plain)
         assert plain.state[0][1].tobytes() != full.state[l][dst].tobytes()
+
+
+# The counter layout of stochastic rounding is this library's own convention
+# (API page, Parameters: rand_seed, philox_rounds): Philox-4x32 with
+# philox_rounds rounds, key = (lo32(seed), hi32(seed)), counter =
+# (e >> 2, dst_slot, layer, 0) with e = (h*dim + i)*dstate + j, and element e
+# takes word e & 3.  The pins below predict every stored byte of a call from
+# that statement, the known-answer-pinned Philox and the bit-level rounding
+# rule, without the oracle's materialization code.
+
+SR_SEED = 0x0123_4567_89AB_CDEF   # hi32 != lo32, so a dropped or swapped key word shows
+
+
+def _sr_world(sd):
+    """Three layers, one request: layer l reads slot l and writes slot 7 - l (slot
+    and layer words differ), one token with A = 0 (decay exactly 1) and dt = 1/16,
+    so that S_1 = S_0 + x B^T / 16 is exact in fp64 and its fp32 rounding is
+    known without the oracle."""
+    L = 3
+    shape = wl.Shape("srpin", L=L, Bt=1, H=2, hpg=1, D=16, N=16, R=4, W=4, state_dtype=sd, input_dtype="bf16",
+                     n_active=1, pool=8, philox_rounds=10, rand_seed=SR_SEED)
+    meta = dict(src_slots=np.arange(L, dtype=np.int32)[:, None], dst_slots=(7 - np.arange(L, dtype=np.int32))[:, None],
+                ring_start=np.array([2], np.int32), replay_prefix_len=np.array([1], np.int32),
+                active=np.array([0], np.int32), pool=8)
+    w = wl.host_world(shape, seed=101, metadata=meta)
+    for l in range(L):
+        w.A[l][:] = 0.0
+        w.dt[l][:] = 0.0625
+    return w
+
+
+def _exact_f32_result(w, l):
+    """fp32 rounding of S_1 = S_0 + dt x B^T for (layer l, its one request), [H, D, N]."""
+    src = int(w.src_slots[l, 0])
+    if w.state_dtype == "bf16":
+        S0 = decode_state(w, l, src)
+    else:  # one-byte: code * scale as an fp32 product
+        import torch
+        codes = torch.from_numpy(w.state[l][src].copy()).view(torch.float8_e4m3fn).float().numpy()
+        S0 = (codes * w.scale[l][src][..., None]).astype(np.float32).astype(np.float64)
+    x = decode_input(w, w.x[l][src, 2])            # [H, D]
+    B = decode_input(w, w.B[l][src, 2])            # [G, N], G = H here
+    S1 = S0 + (0.0625 * x)[:, :, None] * B[:, None, :]
+    return S1.astype(np.float32)
+
+
+def _words(w, l, layout="reading"):
+    """The stochastic-rounding word of every element of (layer l, dst slot), [H*D*N]."""
+    H, D, N = w.H, w.D, w.N
+    dst = int(w.dst_slots[l, 0])
+    lo, hi = SR_SEED & 0xFFFFFFFF, SR_SEED >> 32
+    out = np.zeros(H * D * N, np.uint64)
+    for blk in range(H * D * N // 4):
+        if layout in ("reading", "word_shifted"):
+            ctr, key = (blk, dst, l, 0), (lo, hi)
+        elif layout == "swap_counter_words":
+            ctr, key = (dst, blk, l, 0), (lo, hi)
+        elif layout == "slot_and_layer_swapped":
+            ctr, key = (blk, l, dst, 0), (lo, hi)
+        elif layout == "hi32_dropped":
+            ctr, key = (blk, dst, l, 0), (lo, 0)
+        else:
+            raise ValueError(layout)
+        r = oracle.philox4x32(ctr, key, 10)
+        for q in range(4):
+            idx = 4 * blk + (q if layout != "word_shifted" else (q + 1) % 4)
+            out[idx] = r[q]
+    return out
+
+
+def _predict_bf16(y32, words):
+    """Stochastic rounding to bf16 on the bit pattern: the 16 discarded bits are
+    compared with the word's top 16 bits (up iff word * 2^-16 ulp-units < them)."""
+    bits = y32.reshape(-1).view(np.uint32).astype(np.uint64)
+    sign, mag = bits >> 31, bits & 0x7FFFFFFF
+    up = (words >> 16) < (mag & 0xFFFF)
+    return (((mag >> 16) + up.astype(np.uint64)) | (sign << 15)).astype(np.uint16)
+
+
+def _predict_e4m3(q32, words):
+    """Stochastic rounding to fp8 e4m3fn where |q| >= 2^-6 (normal grid: the 20
+    discarded bits against the word's top 20 bits), saturated at 448; None
+    below 2^-6 (the subnormal grid, not predicted here)."""
+    import torch
+    bits = q32.reshape(-1).view(np.uint32).astype(np.uint64)
+    sign, mag = bits >> 31, bits & 0x7FFFFFFF
+    up = (words >> 12) < (mag & 0xFFFFF)
+    r = (((mag >> 20) + up.astype(np.uint64)) << 20).astype(np.uint32).view(np.float32)
+    r = np.minimum(r, np.float32(448.0)) * np.where(sign == 1, -1, 1).astype(np.float32)
+    codes = torch.from_numpy(r.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    normal = np.abs(q32.reshape(-1)) >= 2.0 ** -6
+    return codes, normal
+
+
+def test_philox_counter_layout_predicts_every_bf16_byte():
+    w = _sr_world("bf16")
+    out = run(w)
+    for l in range(w.L):
+        dst = int(w.dst_slots[l, 0])
+        y32 = _exact_f32_result(w, l)
+        got = out.state[l][dst].reshape(-1)
+        assert np.array_equal(_predict_bf16(y32, _words(w, l)), got), f"layer {l}"
+        # each planted mistake in the layout moves a good share of the bytes
+        for bad in ("swap_counter_words", "slot_and_layer_swapped", "hi32_dropped", "word_shifted"):
+            wrong = _predict_bf16(y32, _words(w, l, bad))
+            assert (wrong != got).mean() > 0.2, (l, bad)
+
+
+def test_philox_counter_layout_predicts_every_fp8_byte():
+    w = _sr_world("fp8_e4m3")
+    out = run(w)
+    predicted = 0
+    for l in range(w.L):
+        dst = int(w.dst_slots[l, 0])
+        y32 = _exact_f32_result(w, l)
+        amax = np.abs(y32).max(axis=-1)                          # [H, D]
+        scale = (amax / np.float32(448.0)).astype(np.float32)   # fp32 division
+        assert out.scale[l][dst].tobytes() == scale.tobytes(), f"layer {l}: scales"
+        q32 = (y32 / scale[..., None]).astype(np.float32)       # the plain fp32 quotient
+        codes, normal = _predict_e4m3(q32, _words(w, l))
+        got = out.state[l][dst].reshape(-1)
+        assert np.array_equal(codes[normal], got[normal]), f"layer {l}"
+        predicted += int(normal.sum())
+        for bad in ("swap_counter_words", "slot_and_layer_swapped", "hi32_dropped", "word_shifted"):
+            wrong, _ = _predict_e4m3(q32, _words(w, l, bad))
+            assert (wrong[normal] != got[normal]).mean() > 0.2, (l, bad)
+    assert predicted >= 0.95 * w.L * w.H * w.D * w.N
 
 
 def test_philox_known_answer_vectors():

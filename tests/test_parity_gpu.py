@@ -177,7 +177,9 @@ def test_stochastic_rounding_is_unbiased_over_seeds():
 @pytest.mark.parametrize("rounds", [0, 10])
 def test_requantization_is_bit_exact_when_state_is_unchanged(sd, rounds):
     """dt = 0 makes the replay an identity in any precision, so the rewrite of the
-    source state (RNE or stochastic: same words, same decisions) is bit-exact."""
+    source state (RNE or stochastic: same words, same decisions) is bit-exact for
+    16-bit state and for one-byte scales; one-byte codes are within one step, the
+    one-code tolerance of one-byte state (tests/parity.py says why they may differ)."""
     shape = wl.Shape("dt0", L=2, Bt=4, H=4, hpg=2, D=64, N=128, R=8, W=8, state_dtype=sd, n_active=4,
                      prefix=("uniform", 1, 8), philox_rounds=rounds, rand_seed=0x5EED)
     hw = wl.host_world(shape, seed=9)
