@@ -41,9 +41,13 @@
  * rsm_last_error() (thread-local) describes it.  Device-resident metadata is
  * not read on the host: out-of-contract values there are undefined behaviour
  * as on the API page, except that the kernel skips any (layer, request) whose
- * active index, ring_start, replay_prefix_len or slot is out of range instead
- * of touching memory for it, and ORs an RSM_STATUS_* bit into *device_status
- * when that optional word is given.
+ * active index, ring_start or replay_prefix_len is out of range, or whose slot
+ * is negative (and not pad_slot_id), instead of touching memory for it, and
+ * ORs an RSM_STATUS_* bit into *device_status when that optional word is
+ * given.  Slots past the end of a pool are caught the same way only when the
+ * caller states the pool size in num_slots; with num_slots = 0 a slot at or
+ * past the end of the pool is undefined behaviour (the kernel would read and
+ * write outside the caller's buffers).
  *
  * Aliasing.  Destination slots must be distinct and must not be a source slot
  * that another (layer, request) of the same call reads; otherwise the result
@@ -60,7 +64,7 @@
 extern "C" {
 #endif
 
-#define RSM_ABI_VERSION 2
+#define RSM_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define RSM_API __attribute__((visibility("default")))
@@ -78,7 +82,7 @@ extern "C" {
 #define RSM_STATUS_BAD_ACTIVE_INDEX 1u /* an active entry outside [0, batch) */
 #define RSM_STATUS_BAD_RING_START 2u   /* ring_start outside [0, ring_buffer_len) */
 #define RSM_STATUS_BAD_PREFIX_LEN 4u   /* replay_prefix_len outside [0, max_window] */
-#define RSM_STATUS_BAD_SLOT 8u         /* a negative slot that is not pad_slot_id */
+#define RSM_STATUS_BAD_SLOT 8u         /* a negative slot that is not pad_slot_id, or one >= num_slots */
 #define RSM_STATUS_WAIT_TIMEOUT 16u    /* an internal pipeline wait gave up (never expected) */
 
 typedef enum rsm_dtype {
@@ -119,6 +123,12 @@ typedef struct rsm_materialize_args {
   int32_t ring_buffer_len;  /* >= 1 */
   int32_t pad_slot_id;      /* slot sentinel to skip (the API page's default is -1) */
   int32_t philox_rounds;    /* 0 = round to nearest even; > 0 = Philox stochastic rounding */
+  /* slots in every layer's state pool (and in its scale and cache pools): a
+   * (layer, request) whose source or destination slot is >= num_slots is
+   * skipped and flagged RSM_STATUS_BAD_SLOT.  0 = the pool size is not stated
+   * and only negative slots are caught.  Not on the API page, whose tensors
+   * carry their sizes; a C call has only pointers. */
+  int32_t num_slots;
 } rsm_materialize_args;
 
 /*

@@ -58,6 +58,7 @@ class RsmArgs(ctypes.Structure):
         ("heads_per_group", ctypes.c_int32), ("max_window", ctypes.c_int32),
         ("ring_buffer_len", ctypes.c_int32), ("pad_slot_id", ctypes.c_int32),
         ("philox_rounds", ctypes.c_int32),
+        ("num_slots", ctypes.c_int32),
     ]
 
 
@@ -147,7 +148,7 @@ def _build_args(state_ptrs, state_slot_strides, x_cache_ptrs, x_cache_slot_strid
                 state_scale_slot_strides, src_slots, dst_slots, ring_start, replay_prefix_len,
                 active_request_indices, *, state_dtype, input_dtype, matrixA_dtype, dim, dstate, num_heads,
                 heads_per_group, max_window, ring_buffer_len, pad_slot_id=-1, rand_seed=None, philox_rounds=0,
-                device_status=None):
+                device_status=None, num_slots=0):
     import torch
     i64, i32 = torch.int64, torch.int32
     a = RsmArgs()
@@ -190,6 +191,7 @@ def _build_args(state_ptrs, state_slot_strides, x_cache_ptrs, x_cache_slot_strid
     a.ring_buffer_len = int(ring_buffer_len)
     a.pad_slot_id = int(pad_slot_id)
     a.philox_rounds = int(philox_rounds)
+    a.num_slots = int(num_slots or 0)
     return a
 
 
@@ -199,14 +201,16 @@ def replayssm_materialize(state_ptrs, state_slot_strides, x_cache_ptrs, x_cache_
                           active_request_indices, *, state_dtype, input_dtype, matrixA_dtype, dim, dstate,
                           num_heads, heads_per_group, max_window, ring_buffer_len, pad_slot_id=-1, rand_seed=None,
                           philox_rounds=0, dependency_inputs=None, dependency_outputs=None, device_status=None,
-                          stream=None) -> None:
+                          num_slots=0, stream=None) -> None:
     """Materialize SSM states at selected tokens from older states plus their replay rings.
 
     Same arguments as flashinfer.mamba.replayssm_materialize; all tensors live
     on the current CUDA device.  `device_status` (optional uint32/int32 [1]
     CUDA tensor) receives RSM_STATUS_* bits for skipped out-of-range metadata.
-    `stream` defaults to torch's current stream.  Asynchronous: returns once the
-    kernel is enqueued.
+    `num_slots` (optional) states the slot count of every layer's pools, so that
+    a slot at or past it is skipped and flagged instead of addressed; 0 leaves
+    it unchecked.  `stream` defaults to torch's current stream.  Asynchronous:
+    returns once the kernel is enqueued.
     """
     import torch
     lib = load_library()
@@ -217,7 +221,7 @@ def replayssm_materialize(state_ptrs, state_slot_strides, x_cache_ptrs, x_cache_
                     matrixA_dtype=matrixA_dtype, dim=dim, dstate=dstate, num_heads=num_heads,
                     heads_per_group=heads_per_group, max_window=max_window, ring_buffer_len=ring_buffer_len,
                     pad_slot_id=pad_slot_id, rand_seed=rand_seed, philox_rounds=philox_rounds,
-                    device_status=device_status)
+                    device_status=device_status, num_slots=num_slots)
     if stream is None:
         stream = torch.cuda.current_stream()
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)

@@ -151,6 +151,7 @@ int validate(const rsm_materialize_args* a) {
   if (quant && (a->state_scale_ptrs == nullptr || a->state_scale_slot_strides == nullptr))
     return fail(RSM_EINVAL, "one-byte state needs state_scale_ptrs and state_scale_slot_strides");
   if (a->philox_rounds < 0) return fail(RSM_EINVAL, "philox_rounds must be >= 0 (got %d)", a->philox_rounds);
+  if (a->num_slots < 0) return fail(RSM_EINVAL, "num_slots must be >= 0 (got %d)", a->num_slots);
   if (a->philox_rounds > 0 && a->rand_seed == nullptr)
     return fail(RSM_EINVAL, "rand_seed is required when philox_rounds > 0");
   for (size_t i = 0; i < sizeof(kInstances) / sizeof(kInstances[0]); ++i) {
@@ -261,6 +262,7 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   p.R = a->ring_buffer_len;
   p.pad = a->pad_slot_id;
   p.philox_rounds = a->philox_rounds;
+  p.num_slots = a->num_slots;
   p.tc_min_k = use_tc ? rsm::kTcMinK : 0;
   p.desc0 = use_tc ? rsm::kTcDescBase : rsm::desc_base(a->dim, a->dstate, sb);
   p.arena0 = static_cast<uint32_t>(base);

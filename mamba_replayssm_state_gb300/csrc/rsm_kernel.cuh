@@ -282,7 +282,7 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
       }
       if (src == p.pad || dst == p.pad) {
         ok = false;
-      } else if (src < 0 || dst < 0) {
+      } else if (src < 0 || dst < 0 || (p.num_slots > 0 && (src >= p.num_slots || dst >= p.num_slots))) {
         bad |= RSM_STATUS_BAD_SLOT;
         ok = false;
       }

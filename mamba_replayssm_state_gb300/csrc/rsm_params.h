@@ -130,6 +130,7 @@ struct Params {
   const int64_t* rand_seed;
   uint32_t* status;
   int32_t L, Bt, H, hpg, W, R, pad, philox_rounds;
+  int32_t num_slots;  // slots per pool; a slot >= num_slots is skipped (0: not checked)
   int32_t tc_min_k;  // tensor-core variant: prefixes this long or longer go to the MMA (0: no tensor path)
   // shared-memory plan: descriptor table at desc0, item arena of arena_bytes at
   // arena0, `stages` pipeline slots (mbarrier pairs and descriptors)

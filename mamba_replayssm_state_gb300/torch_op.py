@@ -33,7 +33,7 @@ def _materialize(state_ptrs: torch.Tensor, state_slot_strides: torch.Tensor, x_c
                  rand_seed: Optional[torch.Tensor], dependency_inputs: List[torch.Tensor],
                  dependency_outputs: List[torch.Tensor], state_dtype: int, input_dtype: int, matrixA_dtype: int,
                  dim: int, dstate: int, num_heads: int, heads_per_group: int, max_window: int,
-                 ring_buffer_len: int, pad_slot_id: int, philox_rounds: int) -> None:
+                 ring_buffer_len: int, pad_slot_id: int, philox_rounds: int, num_slots: int = 0) -> None:
     replayssm_materialize(state_ptrs, state_slot_strides, x_cache_ptrs, x_cache_slot_strides, B_cache_ptrs,
                           B_cache_slot_strides, dt_cache_ptrs, dt_cache_slot_strides, A_ptrs, state_scale_ptrs,
                           state_scale_slot_strides, src_slots, dst_slots, ring_start, replay_prefix_len,
@@ -41,7 +41,7 @@ def _materialize(state_ptrs: torch.Tensor, state_slot_strides: torch.Tensor, x_c
                           matrixA_dtype=matrixA_dtype, dim=dim, dstate=dstate, num_heads=num_heads,
                           heads_per_group=heads_per_group, max_window=max_window,
                           ring_buffer_len=ring_buffer_len, pad_slot_id=pad_slot_id, rand_seed=rand_seed,
-                          philox_rounds=philox_rounds)
+                          philox_rounds=philox_rounds, num_slots=num_slots)
 
 
 @_materialize.register_fake
@@ -50,7 +50,7 @@ def _materialize_fake(state_ptrs, state_slot_strides, x_cache_ptrs, x_cache_slot
                       state_scale_slot_strides, src_slots, dst_slots, ring_start, replay_prefix_len,
                       active_request_indices, rand_seed, dependency_inputs, dependency_outputs, state_dtype,
                       input_dtype, matrixA_dtype, dim, dstate, num_heads, heads_per_group, max_window,
-                      ring_buffer_len, pad_slot_id, philox_rounds) -> None:
+                      ring_buffer_len, pad_slot_id, philox_rounds, num_slots=0) -> None:
     return None
 
 
@@ -62,7 +62,7 @@ def materialize(state_ptrs, state_slot_strides, x_cache_ptrs, x_cache_slot_strid
                 state_scale_slot_strides, src_slots, dst_slots, ring_start, replay_prefix_len,
                 active_request_indices, *, state_dtype, input_dtype, matrixA_dtype, dim, dstate, num_heads,
                 heads_per_group, max_window, ring_buffer_len, pad_slot_id=-1, rand_seed=None, philox_rounds=0,
-                dependency_inputs=None, dependency_outputs=None) -> None:
+                dependency_inputs=None, dependency_outputs=None, num_slots=0) -> None:
     """replayssm_materialize's arguments (dtypes as torch dtypes, names or
     codes), through the custom op so that torch.compile can trace it."""
     OP(state_ptrs, state_slot_strides, x_cache_ptrs, x_cache_slot_strides, B_cache_ptrs, B_cache_slot_strides,
@@ -70,4 +70,4 @@ def materialize(state_ptrs, state_slot_strides, x_cache_ptrs, x_cache_slot_strid
        dst_slots, ring_start, replay_prefix_len, active_request_indices, rand_seed, list(dependency_inputs or []),
        list(dependency_outputs or []), _dtype_code(state_dtype), _dtype_code(input_dtype),
        _dtype_code(matrixA_dtype), int(dim), int(dstate), int(num_heads), int(heads_per_group), int(max_window),
-       int(ring_buffer_len), int(pad_slot_id), int(philox_rounds))
+       int(ring_buffer_len), int(pad_slot_id), int(philox_rounds), int(num_slots or 0))

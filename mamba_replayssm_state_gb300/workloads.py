@@ -292,7 +292,7 @@ class DeviceWorld:
             state_dtype=s.state_dtype, input_dtype=s.input_dtype, matrixA_dtype=s.A_dtype, dim=s.D,
             dstate=s.N, num_heads=s.H, heads_per_group=s.hpg, max_window=s.W, ring_buffer_len=s.R,
             pad_slot_id=s.pad_slot_id, rand_seed=self.rand_seed, philox_rounds=s.philox_rounds,
-            device_status=self.status)
+            device_status=self.status, num_slots=self.pool)
 
     def set_active(self, active_np) -> None:
         import torch

@@ -52,6 +52,7 @@ class OracleArgs(ctypes.Structure):
         ("ring_buffer_len", ctypes.c_int32), ("pad_slot_id", ctypes.c_int32),
         ("philox_rounds", ctypes.c_int32),
         ("sr_counter_slots", _P32), ("sr_counter_layers", _P32),
+        ("num_slots", ctypes.c_int32),
     ]
 
 
@@ -163,6 +164,7 @@ def materialize(world) -> None:
     args.ring_buffer_len = world.R
     args.pad_slot_id = world.pad_slot_id
     args.philox_rounds = world.philox_rounds
+    args.num_slots = min(int(a.shape[0]) for a in world.state)
     # a one-request copy of a larger call (workloads.host_subworld) names the
     # destination slot and layer of that call: the Philox counter uses them
     meta = getattr(world, "meta", None) or {}

@@ -352,6 +352,8 @@ static int check_aliasing(const oracle_args *a, int32_t n) {
       int32_t d = a->dst_slots[(int64_t)l * a->batch + b];
       if (s == a->pad_slot_id || d == a->pad_slot_id) continue;
       if (s < 0 || d < 0) return fail("negative slot that is not pad_slot_id", s < 0 ? s : d);
+      if (a->num_slots > 0 && (s >= a->num_slots || d >= a->num_slots))
+        return fail("slot past the end of the pool", s >= a->num_slots ? s : d);
       for (int32_t q = 0; q < n; ++q) {
         int32_t b2 = a->active_request_indices[q];
         int32_t s2 = a->src_slots[(int64_t)l * a->batch + b2];

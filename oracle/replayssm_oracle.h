@@ -56,6 +56,9 @@ typedef struct oracle_args {
    * a larger call then draws the random words that call draws. */
   const int32_t *sr_counter_slots;
   const int32_t *sr_counter_layers;
+  /* Slots in every layer's pool; a selected (layer, request) whose slot is
+   * at or past it is refused.  0 = not checked. */
+  int32_t num_slots;
 } oracle_args;
 
 /* 0 on success; <0 when an argument or a metadata value is out of contract

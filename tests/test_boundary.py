@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_struct_layout_and_version(lib):
     assert lib.rsm_args_size() == ctypes.sizeof(rsm.RsmArgs)
-    assert lib.rsm_abi_version() == 2
+    assert lib.rsm_abi_version() == 3
 
 
 def test_oracle_library_loads():
@@ -78,6 +78,7 @@ BAD_CASES = [
     ("input fp16", lambda a: setattr(a, "input_dtype", rsm.RSM_F16), "input_dtype"),
     ("A bf16", lambda a: setattr(a, "matrixA_dtype", rsm.RSM_BF16), "matrixA_dtype"),
     ("state dtype", lambda a: setattr(a, "state_dtype", 9), "state_dtype"),
+    ("num_slots", lambda a: setattr(a, "num_slots", -1), "num_slots"),
     ("int8 shape", lambda a: (setattr(a, "state_dtype", rsm.RSM_I8), setattr(a, "dstate", 64)), "one-byte"),
     ("int8 scales", lambda a: setattr(a, "state_dtype", rsm.RSM_I8), "scale"),
     ("seed", lambda a: setattr(a, "philox_rounds", 10), "rand_seed"),

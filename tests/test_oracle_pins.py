@@ -796,6 +796,8 @@ def test_philox_words_are_uniform():
     (lambda w: w.replay_prefix_len.__setitem__(0, 9), "replay_prefix_len"),
     (lambda w: w.ring_start.__setitem__(0, 8), "ring_start"),
     (lambda w: w.active.__setitem__(0, 5), "active index"),
+    (lambda w: w.dst_slots.__setitem__((0, 0), w.state[0].shape[0]), "past the end of the pool"),
+    (lambda w: w.src_slots.__setitem__((0, 0), w.state[0].shape[0] + 3), "past the end of the pool"),
 ])
 def test_oracle_rejects_out_of_contract_metadata(mutate, msg):
     w = single_request_world(seed=59, R=8, W=8)

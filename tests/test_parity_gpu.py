@@ -326,6 +326,40 @@ def test_out_of_range_metadata_is_skipped_and_flagged(bad, bit):
     compare_worlds(got, run_oracle(ref_in), ref_in)
 
 
+@pytest.mark.parametrize("side", ["dst", "src"])
+@pytest.mark.parametrize("window", [8, 64], ids=["cuda_cores", "tensor_cores"])
+def test_slot_past_the_stated_pool_is_skipped_and_flagged(side, window):
+    """With num_slots stated, a slot at or past it is skipped and flagged
+    (RSM_STATUS_BAD_SLOT) instead of addressed.  The call states a pool one slot
+    shorter than the allocation and uses that last, unused slot, so that nothing
+    outside the buffers could be touched even if the check were missing."""
+    shape = wl.Shape("pastpool", L=2, Bt=4, H=4, hpg=2, D=64, N=128, R=window, W=window, state_dtype="bf16",
+                     n_active=4, pool=10, ring_start=(0, window), prefix=("uniform", 1, window))
+    hw = wl.host_world(shape, seed=43)
+    last = hw.state[0].shape[0] - 1
+    used = list(hw.dst_slots[0])
+    if last in used:  # free the last slot: hand its request the destination slot nobody uses
+        spare = next(d for d in range(hw.state[0].shape[0] // 2, last) if d not in used)
+        hw.dst_slots[0, used.index(last)] = spare
+    victim = int(hw.active[1])
+    if side == "dst":
+        hw.dst_slots[0, victim] = last
+    else:
+        hw.src_slots[0, victim] = last
+    dw = wl.device_world_from_host(hw)
+    kw = dw.call_kwargs()
+    kw["num_slots"] = last
+    rsm.replayssm_materialize(**kw)
+    torch.cuda.synchronize()
+    assert int(dw.status.item()) == 8
+    got = hw.copy()
+    got.state = [wl._to_np(t).view(a.dtype) for t, a in zip(dw.state, hw.state)]
+    ref_in = hw.copy()
+    ref_in.dst_slots[0, victim] = ref_in.pad_slot_id
+    compare_worlds(got, run_oracle(ref_in), ref_in)
+    assert bool((wl._to_np(dw.state[0][last]).view(np.uint8) == 0xFF).all())
+
+
 @pytest.mark.parametrize("sd", ["f32", "bf16", "fp8_e4m3"])
 def test_in_place_commit(sd):
     """dst_slots == src_slots: the prefix is committed into the source slots."""
