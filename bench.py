@@ -36,7 +36,20 @@ from mamba_replayssm_state_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "state GB/s & µs/active request (48L×256H×64×128); empty-active-list µs"
 KERNEL_NAME = "materialize_kernel"
-KERNEL_SOURCES = ["rsm_kernel.cuh", "rsm_formats.cuh", "rsm_ptx.cuh", "rsm_params.h", "rsm_api.cu"]
+SPEC_HBM_GBS = 8000.0  # the GB300's nominal HBM3e bandwidth, the denominator the target is stated against
+_CSRC = "mamba_replayssm_state_gb300/csrc/"
+_SHARED_SOURCES = ["include/replayssm.h", _CSRC + "rsm_api.cu", _CSRC + "rsm_ptx.cuh", _CSRC + "rsm_params.h",
+                   _CSRC + "rsm_instances.h"]
+# every source file whose edit can change a kernel's code, per kernel: a profile
+# summary is valid only for the hash of the files it was taken on
+KERNEL_SOURCES = {
+    "materialize_kernel": _SHARED_SOURCES + [_CSRC + f for f in (
+        "rsm_kernel.cuh", "rsm_formats.cuh", "rsm_inst_f32.cu", "rsm_inst_bf16.cu", "rsm_inst_f16.cu",
+        "rsm_inst_q8.cu")],
+    "materialize_tc_kernel": _SHARED_SOURCES + [_CSRC + f for f in (
+        "rsm_kernel.cuh", "rsm_formats.cuh", "rsm_tc_kernel.cuh", "rsm_tc.cuh", "rsm_inst_tc.cu")],
+    "gdn_commit_kernel": _SHARED_SOURCES + [_CSRC + f for f in ("gdn_kernel.cuh", "gdn_params.h", "gdn_inst.cu")],
+}
 
 
 def parse_args():
@@ -56,16 +69,19 @@ def parse_args():
     p.add_argument("--e2e-requests", type=int, default=16)
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--all-workloads", action="store_true",
-                   help="also measure the other named workloads (added under 'workloads')")
+                   help="measure the other named workloads even with --no-extras")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the other named workloads (measured by default, under 'workloads')")
     p.add_argument("--gdn", action="store_true",
                    help="measure only the gated-delta-rule commit (gdn36_hv32_t8; --batch overrides B)")
     return p.parse_args()
 
 
-def kernel_source_hash(sources=None) -> str:
+def kernel_source_hash(kernel: str = KERNEL_NAME) -> str:
+    """SHA-256 prefix of every source file that builds `kernel`."""
     h = hashlib.sha256()
-    for f in sources or KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "mamba_replayssm_state_gb300", "csrc", f), "rb") as fh:
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -142,10 +158,10 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(power) if power else None}
 
 
-def profile_traffic(workload: str, src_hash: str):
+def profile_traffic(workload: str, src_hash: str, kernel: str = KERNEL_NAME):
     """DRAM bytes per launch from the committed ncu summary of this kernel and
     workload, if it was taken on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
@@ -348,15 +364,7 @@ def e2e_measure(torch, rsm, shape, n_req, steps, device, groups=8):
     # one public call per layer group: the per-layer tables and slot rows sliced
     bounds = np.linspace(0, sh.L, groups + 1).astype(int)
     spans = [(int(bounds[g]), int(bounds[g + 1])) for g in range(groups) if bounds[g + 1] > bounds[g]]
-    calls = []
-    for l0, l1 in spans:
-        kw = dw.call_kwargs()
-        for key in ("state_ptrs", "state_slot_strides", "x_cache_ptrs", "x_cache_slot_strides", "B_cache_ptrs",
-                    "B_cache_slot_strides", "dt_cache_ptrs", "dt_cache_slot_strides", "A_ptrs", "state_scale_ptrs",
-                    "state_scale_slot_strides", "src_slots", "dst_slots"):
-            if kw[key] is not None:
-                kw[key] = kw[key][l0:l1]
-        calls.append(rsm.prepare(**kw))
+    calls = [rsm.prepare(**dist.layer_shard_kwargs(dw.call_kwargs(), l0, l1)) for l0, l1 in spans]
     s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ng = len(spans)
     ev_in = [torch.cuda.Event() for _ in range(ng)]
@@ -411,60 +419,105 @@ def e2e_measure(torch, rsm, shape, n_req, steps, device, groups=8):
                         f"overlapped on three streams)"}
 
 
-ALU_LANES_PER_SM = 128  # FP32 lanes per SM (Blackwell)
+ALU_LANES_PER_SM = 128  # FP32 lanes per SM (Blackwell: 4 sub-partitions x 32)
+INT_LANES_PER_SM = 64   # 32-bit integer lanes per SM (4 sub-partitions x 16): LOP3, IADD3, SHF, IMAD
 
 
-def measure_workload(torch, rsm, shape, device, steps, peak_gbs, sms, sm_mhz):
-    """State GB/s, microseconds per active request and roofline fractions of
-    one named workload (its own seeded world, timed with CUDA events)."""
+def lane_ops(shape, active, prefix, src, dst):
+    """(fp32 lane-operations, 32-bit integer lane-operations) one call needs,
+    counted from the method, not from the code.  Per element of a replayed
+    tile: one FMUL (the decay product) and one FFMA per token.  With Philox
+    rounding, per element philox_rounds * 6 / 4 integer operations (a round is
+    two 32x32->64-bit multiplies, two three-way XORs and two key additions, and
+    one call gives four words) plus 4 for the rounding decision (shift, add,
+    mask, saturate).  Copies (prefix 0) cost neither."""
     import numpy as np
-    dw = wl.device_world_random(shape, seed=5, device=device)
-    active = dw.active.cpu().numpy()
-    prefix = dw.replay_prefix_len.cpu().numpy()
-    src, dst = dw.src_slots.cpu().numpy(), dw.dst_slots.cpu().numpy()
-    state_b, ring_b, n = workload_bytes(shape, active, prefix, src, dst)
-    call = rsm.prepare(**dw.call_kwargs())
-    stream = torch.cuda.current_stream()
+    n = int(np.argmax(active == -1)) if (active == -1).any() else len(active)
+    elems = shape.H * shape.D * shape.N
+    fp32 = integer = 0
+    sr_per_elem = shape.philox_rounds * 6 / 4 + 4 if shape.philox_rounds > 0 else 0
+    for b in active[:n]:
+        b = int(b)
+        k = int(prefix[b])
+        if k == 0:
+            continue
+        live = sum(1 for l in range(shape.L) if src[l, b] != shape.pad_slot_id and dst[l, b] != shape.pad_slot_id)
+        fp32 += live * elems * (k + 1)
+        integer += live * elems * sr_per_elem
+    return fp32, int(integer)
+
+
+def timed_calls(torch, call, stream, uuid, seconds=1.0):
+    """Device time per call (ms) over about `seconds` of back-to-back calls,
+    with the SM clocks sampled while they run (the sampler needs ~1 s)."""
     for _ in range(3):
         call(stream)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    for _ in range(3):
+        call(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    one = e0.elapsed_time(e1) / 3
+    steps = int(min(5000, max(20, seconds * 1e3 / max(one, 1e-3))))
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.3)
+    e0.record(stream)
     for _ in range(steps):
         call(stream)
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
-    # FP32 lane-FMAs of the replay: one per element per replayed token (+1 for the decay product)
-    nb = int(np.argmax(active == -1)) if (active == -1).any() else len(active)
-    fmas = 0
-    for b in active[:nb]:
-        for l in range(shape.L):
-            if src[l, int(b)] == shape.pad_slot_id or dst[l, int(b)] == shape.pad_slot_id:
-                continue
-            k = int(prefix[int(b)])
-            fmas += shape.H * shape.D * shape.N * (k + 1 if k > 0 else 0)
-    alu_peak = sms * ALU_LANES_PER_SM * sm_mhz * 1e6
+    info = clocks.stop()
+    return e0.elapsed_time(e1) / steps, steps, info
+
+
+def _fractions(nbytes, fp32_ops, int_ops, ms, peak_gbs, sms, clock_info):
+    mhz = (clock_info or {}).get("sm_mhz") or 2070.0
+    sec = ms * 1e-3
+    fr = {"hbm_frac": nbytes / sec / 1e9 / peak_gbs, "hbm_frac_spec": nbytes / sec / 1e9 / SPEC_HBM_GBS,
+          "fp32_lane_frac": fp32_ops / sec / (sms * ALU_LANES_PER_SM * mhz * 1e6),
+          "int_lane_frac": int_ops / sec / (sms * INT_LANES_PER_SM * mhz * 1e6)}
+    fr["bound"] = max((("hbm", fr["hbm_frac"]), ("fp32", fr["fp32_lane_frac"]), ("int", fr["int_lane_frac"])),
+                      key=lambda kv: kv[1])[0]
+    return fr
+
+
+def measure_workload(torch, rsm, shape, device, peak_gbs, sms, uuid):
+    """State GB/s, microseconds per active request and roofline fractions of
+    one named workload (its own seeded world, timed with CUDA events over
+    about a second, clocks sampled meanwhile)."""
+    dw = wl.device_world_random(shape, seed=5, device=device)
+    active = dw.active.cpu().numpy()
+    prefix = dw.replay_prefix_len.cpu().numpy()
+    src, dst = dw.src_slots.cpu().numpy(), dw.dst_slots.cpu().numpy()
+    state_b, ring_b, n = workload_bytes(shape, active, prefix, src, dst)
+    fp32_ops, int_ops = lane_ops(shape, active, prefix, src, dst)
+    kw = dw.call_kwargs()
+    call = rsm.prepare(**kw)
+    kernel = rsm.kernel_name(**kw)
+    ms, steps, clock_info = timed_calls(torch, call, torch.cuda.current_stream(), uuid)
     status = int(dw.status.item())
-    del dw, call
+    del dw, call, kw
     torch.cuda.empty_cache()
-    return {"state_dtype": shape.state_dtype, "layers": shape.L, "heads": shape.H, "n_active": n,
-            "prefix": list(shape.prefix), "ms_per_call": ms, "state_gbs": state_b / (ms * 1e-3) / 1e9,
-            "us_per_request": ms * 1e3 / max(n, 1),
-            "hbm_frac": (state_b + ring_b) / (ms * 1e-3) / 1e9 / peak_gbs,
-            "alu_frac": fmas / (ms * 1e-3) / alu_peak, "device_status": status}
+    out = {"kernel": kernel, "source_hash": kernel_source_hash(kernel), "state_dtype": shape.state_dtype,
+           "layers": shape.L, "heads": shape.H, "batch": shape.Bt, "n_active": n, "prefix": list(shape.prefix),
+           "philox_rounds": shape.philox_rounds, "pad_frac": shape.pad_frac, "ms_per_call": ms, "steps": steps,
+           "algorithmic_bytes": state_b + ring_b, "state_gbs": state_b / (ms * 1e-3) / 1e9,
+           "us_per_request": ms * 1e3 / max(n, 1), "fp32_lane_ops": fp32_ops, "int_lane_ops": int_ops}
+    out.update(_fractions(state_b + ring_b, fp32_ops, int_ops, ms, peak_gbs, sms, clock_info))
+    out["clocks"] = clock_info
+    out["device_status"] = status
+    return out
 
 
-GDN_SOURCES = ["gdn_kernel.cuh", "gdn_params.h", "rsm_ptx.cuh", "rsm_api.cu"]
-
-
-def measure_gdn(torch, rsm, shape, device, steps, peak_gbs, sms, sm_mhz):
+def measure_gdn(torch, rsm, shape, device, peak_gbs, sms, uuid):
     """Time of one gated-delta-rule commit call over a seeded full-size world
     (state updated in place, so every timed call is a fresh commit of the same
     shape), its algorithmic bytes against the HBM peak, and its FP32 lane
     operations (per element and accepted token: the dot-product FMA, the decay
     multiply and the update FMA) against the lane peak."""
-    import numpy as np
     dw = gw.gdn_device_world_random(shape, seed=5, device=device)
     kw = dw.call_kwargs()
     idx, lens = dw.state_indices.cpu().numpy(), dw.accept_lens.cpu().numpy()
@@ -472,27 +525,42 @@ def measure_gdn(torch, rsm, shape, device, steps, peak_gbs, sms, sm_mhz):
     tst = None if dw.track_steps is None else dw.track_steps.cpu().numpy()
     nbytes = gw.gdn_bytes(shape, idx, lens, tidx, tst)
     live = [b for b in range(shape.B) if idx[b] > shape.null_block_id and lens[b] > 0]
-    lane_ops = sum(int(lens[b]) for b in live) * shape.L * shape.HV * gw.DV * gw.DK * 3
+    lane_ops_ = sum(int(lens[b]) for b in live) * shape.L * shape.HV * gw.DV * gw.DK * 3
     stream = torch.cuda.current_stream()
-    for _ in range(3):
-        rsm.gated_delta_rule_replayssm_commit(**kw, stream=stream)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        rsm.gated_delta_rule_replayssm_commit(**kw, stream=stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+    call = lambda st: rsm.gated_delta_rule_replayssm_commit(**kw, stream=st)
+    ms, steps, clock_info = timed_calls(torch, call, stream, uuid)
     status = int(dw.status.item())
     del dw, kw
     torch.cuda.empty_cache()
-    alu_peak = sms * ALU_LANES_PER_SM * sm_mhz * 1e6
-    return {"kernel": "gdn_commit_kernel", "layers": shape.L, "v_heads": shape.HV, "k_heads": shape.H,
-            "window": shape.T, "batch": shape.B, "live_requests": len(live), "track": shape.track,
-            "accept": list(shape.accept), "ms_per_call": ms, "algorithmic_bytes": nbytes,
-            "gbs": nbytes / (ms * 1e-3) / 1e9, "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peak_gbs,
-            "alu_frac": lane_ops / (ms * 1e-3) / alu_peak, "device_status": status}
+    out = {"kernel": "gdn_commit_kernel", "source_hash": kernel_source_hash("gdn_commit_kernel"),
+           "layers": shape.L, "v_heads": shape.HV, "k_heads": shape.H, "window": shape.T, "batch": shape.B,
+           "live_requests": len(live), "track": shape.track, "accept": list(shape.accept), "ms_per_call": ms,
+           "steps": steps, "algorithmic_bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9}
+    out.update(_fractions(nbytes, lane_ops_, 0, ms, peak_gbs, sms, clock_info))
+    out["clocks"] = clock_info
+    out["device_status"] = status
+    return out
+
+
+def measure_named_workloads(torch, rsm, device, peak_gbs, sms, uuid):
+    """The other named workloads, each at its full size on one GPU: the
+    Mamba-2-like fp32 state, int8 state, fp8 state with Philox stochastic
+    rounding and with round-to-nearest, the 64-token ring sweep at every
+    prefix length, and the gated-delta-rule commit."""
+    sweep = {}
+    for name in ("mamba2_2p7b_fp32", "hybrid48_int8", "hybrid48_fp8_sr"):
+        sweep[name] = measure_workload(torch, rsm, wl.SHAPES[name], device, peak_gbs, sms, uuid)
+    sweep["hybrid48_fp8_rne"] = measure_workload(
+        torch, rsm, wl.SHAPES["hybrid48_fp8_sr"].replace(name="hybrid48_fp8_rne", philox_rounds=0), device,
+        peak_gbs, sms, uuid)
+    for k in (0, 1, 4, 16, 64):
+        shp = wl.SHAPES["ring_sweep_fp16"].replace(prefix=("fixed", k))
+        sweep[f"ring_sweep_fp16_k{k}"] = measure_workload(torch, rsm, shp, device, peak_gbs, sms, uuid)
+    gshape = gw.GDN_SHAPES["gdn36_hv32_t8"]
+    sweep["gdn36_hv32_t8"] = measure_gdn(torch, rsm, gshape, device, peak_gbs, sms, uuid)
+    sweep["gdn36_hv32_t8_full"] = measure_gdn(torch, rsm, gshape.replace(accept=("fixed", 8)), device, peak_gbs,
+                                              sms, uuid)
+    return sweep
 
 
 def main():
@@ -510,19 +578,24 @@ def main():
     dist.init("nccl")
     rsm.load_library()
 
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        uuid = None
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    peak, peak_kind = measured_peak()
+
     if args.gdn:
         gshape = gw.GDN_SHAPES["gdn36_hv32_t8"]
         if args.batch is not None:
             gshape = gshape.replace(B=args.batch)
         if args.prefix is not None:
             gshape = gshape.replace(accept=("fixed", args.prefix))
-        gpeak, gsrc = measured_peak()
-        sms = torch.cuda.get_device_properties(device).multi_processor_count
-        res = measure_gdn(torch, rsm, gshape, device, max(args.steps, 1), gpeak, sms, 2070.0)
+        res = measure_gdn(torch, rsm, gshape, device, peak, sms, uuid)
         if rank == 0:
             print(json.dumps({"metric": "gated-delta-rule commit: algorithmic GB/s", "unit": "GB/s",
-                              "value": res["gbs"], "peak_gbs": gpeak, "peak_source": gsrc,
-                              "source_hash": kernel_source_hash(GDN_SOURCES), **res}), flush=True)
+                              "value": res["gbs"], "peak_gbs": peak, "peak_source": peak_kind, **res}), flush=True)
         return 0
 
     shape = wl.SHAPES[args.workload]
@@ -547,11 +620,6 @@ def main():
     cfg = rsm.launch_config(**dw.call_kwargs())
     stream = torch.cuda.current_stream()
 
-    uuid = None
-    try:
-        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
-    except Exception:
-        uuid = None
     clocks = ClockSampler(uuid)
 
     for _ in range(max(args.warmup, 0)):
@@ -599,14 +667,16 @@ def main():
         "gpu_launches": args.steps,
         "device_status": status,
     }
-    peak, peak_kind = measured_peak()
     achieved = (state_b + ring_b) / (ms * 1e-3) / 1e9
-    src_hash = kernel_source_hash()
-    traffic = profile_traffic(shape.name, src_hash) if n == shape.Bt else None
+    kernel = rsm.kernel_name(**dw.call_kwargs())
+    src_hash = kernel_source_hash(kernel)
+    traffic = profile_traffic(shape.name, src_hash, kernel) if n == shape.Bt else None
     out["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                        "frac": achieved / peak, "traffic": traffic,
                        "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
-                       "algorithmic_bytes_per_launch": state_b + ring_b, "kernel": KERNEL_NAME,
+                       "frac_spec": achieved / SPEC_HBM_GBS, "spec_peak": SPEC_HBM_GBS,
+                       "spec_source": "nominal GB300 HBM3e bandwidth (8 TB/s), the target's denominator",
+                       "algorithmic_bytes_per_launch": state_b + ring_b, "kernel": kernel,
                        "source_hash": src_hash}
     out["clocks"] = clock_info
 
@@ -649,31 +719,21 @@ def main():
             try:
                 out["e2e"] = e2e_measure(torch, rsm, shape, min(args.e2e_requests, shape.Bt), args.e2e_steps,
                                          device)
+                if out["e2e"]["h2d_bytes_per_step"] < state_b:
+                    out["e2e"]["note"] = (
+                        f"measured on {min(args.e2e_requests, shape.Bt)} of the {n} requests: the whole step's "
+                        f"{state_b / 2e9:.0f} GB of source state (and as much of results) would not fit in pinned "
+                        f"host memory, and the figure is bound by the CPU-GPU link, not by the request count")
             except RuntimeError as ex:  # pinned memory exhausted etc.
                 out["e2e"] = {"value": None, "error": str(ex)[:200]}
             if world == 1:
                 out["cpu_baseline"] = cpu_baseline_from_device(dw, shape, args.cpu_seconds)
-    if args.all_workloads:
+    if args.all_workloads or not (args.no_extras or args.no_workloads):
         del dw, call
         torch.cuda.empty_cache()
-        sms = torch.cuda.get_device_properties(device).multi_processor_count
-        mhz = (clock_info or {}).get("sm_mhz") or 2070.0
-        sweep = {}
-        for name in ("mamba2_2p7b_fp32", "hybrid48_int8", "hybrid48_fp8_sr"):
-            sweep[name] = measure_workload(torch, rsm, wl.SHAPES[name], device, 20, peak, sms, mhz)
-        # the fp8 state rounded to nearest even (no Philox), for comparison
-        sweep["hybrid48_fp8_rne"] = measure_workload(
-            torch, rsm, wl.SHAPES["hybrid48_fp8_sr"].replace(name="hybrid48_fp8_rne", philox_rounds=0), device, 20,
-            peak, sms, mhz)
-        for k in (0, 1, 4, 16, 64):
-            shp = wl.SHAPES["ring_sweep_fp16"].replace(prefix=("fixed", k))
-            sweep[f"ring_sweep_fp16_k{k}"] = measure_workload(torch, rsm, shp, device, 10, peak, sms, mhz)
-        gshape = gw.GDN_SHAPES["gdn36_hv32_t8"]
-        sweep["gdn36_hv32_t8"] = measure_gdn(torch, rsm, gshape, device, 20, peak, sms, mhz)
-        sweep["gdn36_hv32_t8_full"] = measure_gdn(torch, rsm, gshape.replace(accept=("fixed", 8)), device, 20,
-                                                  peak, sms, mhz)
-        out["workloads"] = sweep
-        out["alu_peak_note"] = f"{sms} SMs x {ALU_LANES_PER_SM} FP32 lanes x {mhz:.0f} MHz lane-FMA/s"
+        out["workloads"] = measure_named_workloads(torch, rsm, device, peak, sms, uuid)
+        out["lane_peaks_note"] = (f"fp32: {sms} SMs x {ALU_LANES_PER_SM} lanes x the sampled SM clock; 32-bit "
+                                  f"integer: {sms} SMs x {INT_LANES_PER_SM} lanes x the sampled SM clock")
     if rank == 0:
         print(json.dumps(out), flush=True)
     dist.barrier()

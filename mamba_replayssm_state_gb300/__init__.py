@@ -16,7 +16,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["replayssm_materialize", "gated_delta_rule_replayssm_commit", "prepare", "launch_config",
+__all__ = ["replayssm_materialize", "gated_delta_rule_replayssm_commit", "prepare", "launch_config", "kernel_name",
            "pointer_table", "stride_table", "library_path", "load_library", "ReplaySSMError", "STATUS_BITS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -63,7 +63,7 @@ class RsmArgs(ctypes.Structure):
 
 
 EXPORTS = ("rsm_materialize", "rsm_last_error", "rsm_args_size", "rsm_abi_version", "rsm_launch_config",
-           "rsm_gdn_commit", "rsm_gdn_args_size")
+           "rsm_kernel_name", "rsm_gdn_commit", "rsm_gdn_args_size")
 
 _lib = None
 
@@ -102,6 +102,8 @@ def load_library(build_if_missing: bool = True):
     lib.rsm_abi_version.restype = ctypes.c_int
     lib.rsm_launch_config.argtypes = [ctypes.POINTER(RsmArgs)] + [ctypes.POINTER(ctypes.c_int)] * 4
     lib.rsm_launch_config.restype = ctypes.c_int
+    lib.rsm_kernel_name.argtypes = [ctypes.POINTER(RsmArgs)]
+    lib.rsm_kernel_name.restype = ctypes.c_char_p
     if lib.rsm_args_size() != ctypes.sizeof(RsmArgs):
         raise OSError("rsm_materialize_args layout mismatch between libreplayssm.so and the binding")
     lib.rsm_gdn_commit.argtypes = [ctypes.POINTER(GdnArgs), ctypes.c_void_p]
@@ -270,6 +272,20 @@ def launch_config(*args, **kwargs) -> dict:
     if rc != 0:
         raise ReplaySSMError(rc, lib.rsm_last_error().decode())
     return dict(zip(("grid", "block", "smem_bytes", "stages"), (o.value for o in out)))
+
+
+def kernel_name(*args, **kwargs) -> str:
+    """Name of the kernel replayssm_materialize launches for these arguments
+    ("materialize_kernel" or "materialize_tc_kernel")."""
+    lib = load_library()
+    kwargs.pop("stream", None)
+    kwargs.pop("dependency_inputs", None)
+    kwargs.pop("dependency_outputs", None)
+    a = _build_args(*args, **kwargs)
+    name = lib.rsm_kernel_name(ctypes.byref(a)).decode()
+    if not name:
+        raise ReplaySSMError(-1, lib.rsm_last_error().decode())
+    return name
 
 
 def pointer_table(tensors, device=None):

@@ -163,6 +163,13 @@ int validate(const rsm_materialize_args* a) {
               dtype_name(a->state_dtype), dtype_name(a->input_dtype), a->dim, a->dstate);
 }
 
+// 16-bit state with bf16 inputs at 64 x 128 and windows of kTcMinWindow or
+// more: the tensor-core variant (the prefix as an MMA)
+bool uses_tensor_cores(const rsm_materialize_args* a) {
+  return (a->state_dtype == RSM_BF16 || a->state_dtype == RSM_F16) && a->input_dtype == RSM_BF16 && a->dim == 64 &&
+         a->dstate == 128 && a->max_window >= rsm::kTcMinWindow;
+}
+
 struct Launch {
   const void* fn;
   int grid, smem, stages;
@@ -190,10 +197,7 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   const int sb = elem_bytes(a->state_dtype), ib = elem_bytes(a->input_dtype);
   const int item_min = static_cast<int>(rsm::item_layout(a->dim, a->dstate, sb, quant, ib, 0).bytes);
   const int item_max = static_cast<int>(rsm::item_layout(a->dim, a->dstate, sb, quant, ib, a->max_window).bytes);
-  // 16-bit state with bf16 inputs at 64 x 128 and windows of kTcMinWindow or
-  // more: the tensor-core variant (the prefix as an MMA)
-  const bool use_tc = (a->state_dtype == RSM_BF16 || a->state_dtype == RSM_F16) && a->input_dtype == RSM_BF16 &&
-                a->dim == 64 && a->dstate == 128 && a->max_window >= rsm::kTcMinWindow;
+  const bool use_tc = uses_tensor_cores(a);
   const int base = static_cast<int>(use_tc ? rsm::kTcArenaBase : rsm::arena_base(a->dim, a->dstate, sb));
   const int two_cta = di.smem_per_sm / 2 - di.smem_reserved - base;
   const int one_cta = di.smem_optin - base;
@@ -437,6 +441,11 @@ int rsm_gdn_commit(const rsm_gdn_commit_args* args, void* stream) {
   if (e != cudaSuccess) return fail(RSM_ECUDA, "launch failed: %s", cudaGetErrorString(e));
   g_last_error.clear();
   return RSM_OK;
+}
+
+const char* rsm_kernel_name(const rsm_materialize_args* args) {
+  if (validate(args) < 0) return "";
+  return uses_tensor_cores(args) ? "materialize_tc_kernel" : "materialize_kernel";
 }
 
 int rsm_gdn_args_size(void) { return static_cast<int>(sizeof(rsm_gdn_commit_args)); }

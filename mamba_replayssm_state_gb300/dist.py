@@ -1,10 +1,17 @@
 """Multi-GPU plumbing for the data-parallel case.
 
 Every (request, layer, head) item is independent and no step of the
-materialization exchanges data, so N GPUs run N independent shards: each rank
-owns a contiguous block of the global batch (its own state pool and rings)
-and launches its own kernel.  The only cross-rank traffic is measurement
-(barriers and a max over ranks of the elapsed time), never the data path.
+materialization exchanges data, so N GPUs run N independent shards and each
+launches its own kernel on its own part of the slot pools:
+  - request shards (data parallel): a contiguous block of the global batch;
+  - head shards (tensor parallel): a contiguous block of every layer's heads,
+    made of whole B groups (a rank holds only its own groups' B cache);
+  - layer shards (pipeline parallel): a contiguous block of the layers.
+The only cross-rank traffic is measurement (barriers and a max over ranks of
+the elapsed time), never the data path.  Stochastic rounding draws its Philox
+words from each call's own (layer, head) numbering, so a sharded run rounds
+differently from an unsharded one (each is a valid draw); round-to-nearest
+results are identical.
 """
 from __future__ import annotations
 
@@ -59,4 +66,41 @@ def shard_active(active, start: int, end: int):
     mine = [int(b) - start for b in active[:n] if start <= b < end]
     out = np.full(end - start, -1, np.int32)
     out[:len(mine)] = mine
+    return out
+
+
+def head_shard(num_heads: int, heads_per_group: int, rank: int, world: int) -> tuple[int, int]:
+    """[h0, h1) of the heads a tensor-parallel rank owns: an even split of
+    every layer's heads in which every B group (heads_per_group consecutive
+    heads reading one B cache row) stays on one rank.  Raises ValueError when
+    the split would cut a group."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("bad rank/world")
+    if num_heads % world:
+        raise ValueError(f"{num_heads} heads do not split evenly over {world} ranks")
+    per = num_heads // world
+    if per % heads_per_group:
+        raise ValueError(f"{per} heads per rank would cut a B group of {heads_per_group} heads")
+    return rank * per, (rank + 1) * per
+
+
+def layer_shard(num_layers: int, rank: int, world: int) -> tuple[int, int]:
+    """[l0, l1) of the layers a pipeline-parallel rank owns (contiguous)."""
+    return shard(num_layers, rank, world)
+
+
+# replayssm_materialize arguments with one entry (or row) per layer
+PER_LAYER_KEYS = ("state_ptrs", "state_slot_strides", "x_cache_ptrs", "x_cache_slot_strides", "B_cache_ptrs",
+                  "B_cache_slot_strides", "dt_cache_ptrs", "dt_cache_slot_strides", "A_ptrs", "state_scale_ptrs",
+                  "state_scale_slot_strides", "src_slots", "dst_slots")
+
+
+def layer_shard_kwargs(kwargs: dict, l0: int, l1: int) -> dict:
+    """replayssm_materialize keyword arguments restricted to layers [l0, l1):
+    the per-layer pointer and stride tables and the rows of the slot tables
+    (views, no copies).  Everything per request stays as it is."""
+    out = dict(kwargs)
+    for key in PER_LAYER_KEYS:
+        if out.get(key) is not None:
+            out[key] = out[key][l0:l1]
     return out

@@ -412,29 +412,72 @@ def test_prepared_call_replays_from_a_cuda_graph():
 # full size: the 48-layer x 256-head x 64x128 bf16 call that the benchmark times
 # ----------------------------------------------------------------------------
 
+def _unwritten_destinations_untouched(dw, shape, n):
+    """On the device: every destination-half slot of every layer that no
+    selected (layer, request) writes is still the 0xFF sentinel."""
+    active = dw.active.cpu().numpy()[:n]
+    src, dst = dw.src_slots.cpu().numpy(), dw.dst_slots.cpu().numpy()
+    pad, half = shape.pad_slot_id, dw.pool // 2
+    checked = 0
+    for l in range(shape.L):
+        written = {int(dst[l, b]) for b in active if src[l, b] != pad and dst[l, b] != pad}
+        idle = [d for d in range(half, dw.pool) if d not in written]
+        if idle:
+            idx = torch.tensor(idle, device=dw.state[l].device)
+            assert bool((dw.state[l].index_select(0, idx).view(torch.uint8) == 0xFF).all()), f"layer {l}"
+            checked += len(idle)
+    return checked
+
+
 @pytest.mark.slow
-def test_headline_full_size_sampled():
+@pytest.mark.parametrize("variant", ["bench", "pads_and_terminator"])
+def test_headline_full_size_sampled(variant):
+    """The 48-layer x 256-head x 64x128 bf16 call at full size: as the
+    benchmark times it (all 256 requests active), and with 200 active requests
+    before the -1s and 10% of the (layer, request) entries padded.  Sampled
+    (layer, request) outputs are recomputed by the oracle one by one; every
+    prefix-0 request is a byte copy; every destination slot that nothing
+    writes keeps its sentinel."""
     shape = wl.SHAPES["hybrid48_bf16"]
+    if variant == "pads_and_terminator":
+        shape = shape.replace(n_active=200, pad_frac=0.10)
     dw = wl.device_world_random(shape, seed=0)
     cfg = rsm.launch_config(**dw.call_kwargs())
     assert cfg["grid"] > 0
     rsm.replayssm_materialize(**dw.call_kwargs())
     torch.cuda.synchronize()
     assert int(dw.status.item()) == 0
+    n = shape.n_active
     active = dw.active.cpu().numpy()
+    assert (active[n:] == -1).all() and (active[:n] >= 0).all()
+    live = active[:n]
     prefix = dw.replay_prefix_len.cpu().numpy()
     src = dw.src_slots.cpu().numpy()
     dst = dw.dst_slots.cpu().numpy()
+    pad = shape.pad_slot_id
     rng = np.random.default_rng(5)
-    # property at full size: every prefix-0 request is a bit-exact copy in every layer
-    zero = [int(b) for b in active[active >= 0] if prefix[b] == 0]
+    # property at full size: every prefix-0 request is a bit-exact copy in every unpadded layer
+    zero = [int(b) for b in live if prefix[b] == 0]
     for b in zero[:8]:
         for l in range(shape.L):
-            assert torch.equal(dw.state[l][dst[l, b]], dw.state[l][src[l, b]])
+            if src[l, b] != pad and dst[l, b] != pad:
+                assert torch.equal(dw.state[l][dst[l, b]], dw.state[l][src[l, b]])
+    idle = _unwritten_destinations_untouched(dw, shape, n)
+    if variant == "pads_and_terminator":
+        assert idle >= shape.L * (shape.Bt - n)
     # sampled outputs, each recomputed by the oracle from its own inputs
-    picks = [(int(rng.integers(shape.L)), int(active[int(rng.integers(shape.Bt))])) for _ in range(6)]
-    picks.append((shape.L - 1, int(active[-1])))
+    want = 12 if variant == "bench" else 32
+    picks, tries = [], 0
+    while len(picks) < want and tries < 10 * want:
+        l, b = int(rng.integers(shape.L)), int(live[int(rng.integers(n))])
+        tries += 1
+        if src[l, b] != pad and dst[l, b] != pad and (l, b) not in picks:
+            picks.append((l, b))
+    picks.append((shape.L - 1, int(live[-1])))
+    checked = 0
     for l, b in picks:
+        if src[l, b] == pad or dst[l, b] == pad:
+            continue
         sub = wl.host_subworld(dw, l, b)
         oracle.materialize(sub)
         got = wl._to_np(dw.state[l][dst[l, b]])
@@ -443,6 +486,8 @@ def test_headline_full_size_sampled():
             assert got.tobytes() == ref.tobytes()
         else:
             compare_slot(got, ref, "bf16", where=f"layer {l} request {b}")
+        checked += 1
+    assert checked >= want
     del dw
     torch.cuda.empty_cache()
 
