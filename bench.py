@@ -44,8 +44,8 @@ _SHARED_SOURCES = ["include/replayssm.h", _CSRC + "rsm_api.cu", _CSRC + "rsm_ptx
 # summary is valid only for the hash of the files it was taken on
 KERNEL_SOURCES = {
     "materialize_kernel": _SHARED_SOURCES + [_CSRC + f for f in (
-        "rsm_kernel.cuh", "rsm_formats.cuh", "rsm_inst_f32.cu", "rsm_inst_bf16.cu", "rsm_inst_f16.cu",
-        "rsm_inst_q8.cu")],
+        "rsm_kernel.cuh", "rsm_formats.cuh", "rsm_q8_kernel.cuh", "rsm_inst_f32.cu", "rsm_inst_bf16.cu",
+        "rsm_inst_f16.cu", "rsm_inst_q8.cu", "rsm_inst_q8sr.cu")],
     "materialize_tc_kernel": _SHARED_SOURCES + [_CSRC + f for f in (
         "rsm_kernel.cuh", "rsm_formats.cuh", "rsm_tc_kernel.cuh", "rsm_tc.cuh", "rsm_inst_tc.cu")],
     "gdn_commit_kernel": _SHARED_SOURCES + [_CSRC + f for f in ("gdn_kernel.cuh", "gdn_params.h", "gdn_inst.cu")],
@@ -72,6 +72,8 @@ def parse_args():
                    help="measure the other named workloads even with --no-extras")
     p.add_argument("--no-workloads", action="store_true",
                    help="skip the other named workloads (measured by default, under 'workloads')")
+    p.add_argument("--only", default=None,
+                   help="comma-separated names of the named workloads to measure (default: all of them)")
     p.add_argument("--gdn", action="store_true",
                    help="measure only the gated-delta-rule commit (gdn36_hv32_t8; --batch overrides B)")
     return p.parse_args()
@@ -497,11 +499,13 @@ def measure_workload(torch, rsm, shape, device, peak_gbs, sms, uuid):
     kw = dw.call_kwargs()
     call = rsm.prepare(**kw)
     kernel = rsm.kernel_name(**kw)
+    launch = rsm.launch_config(**kw)
     ms, steps, clock_info = timed_calls(torch, call, torch.cuda.current_stream(), uuid)
     status = int(dw.status.item())
     del dw, call, kw
     torch.cuda.empty_cache()
-    out = {"kernel": kernel, "source_hash": kernel_source_hash(kernel), "state_dtype": shape.state_dtype,
+    out = {"kernel": kernel, "source_hash": kernel_source_hash(kernel), "launch": launch,
+           "state_dtype": shape.state_dtype,
            "layers": shape.L, "heads": shape.H, "batch": shape.Bt, "n_active": n, "prefix": list(shape.prefix),
            "philox_rounds": shape.philox_rounds, "pad_frac": shape.pad_frac, "ms_per_call": ms, "steps": steps,
            "algorithmic_bytes": state_b + ring_b, "state_gbs": state_b / (ms * 1e-3) / 1e9,
@@ -542,24 +546,29 @@ def measure_gdn(torch, rsm, shape, device, peak_gbs, sms, uuid):
     return out
 
 
-def measure_named_workloads(torch, rsm, device, peak_gbs, sms, uuid):
+def named_workloads():
     """The other named workloads, each at its full size on one GPU: the
     Mamba-2-like fp32 state, int8 state, fp8 state with Philox stochastic
     rounding and with round-to-nearest, the 64-token ring sweep at every
-    prefix length, and the gated-delta-rule commit."""
-    sweep = {}
-    for name in ("mamba2_2p7b_fp32", "hybrid48_int8", "hybrid48_fp8_sr"):
-        sweep[name] = measure_workload(torch, rsm, wl.SHAPES[name], device, peak_gbs, sms, uuid)
-    sweep["hybrid48_fp8_rne"] = measure_workload(
-        torch, rsm, wl.SHAPES["hybrid48_fp8_sr"].replace(name="hybrid48_fp8_rne", philox_rounds=0), device,
-        peak_gbs, sms, uuid)
+    prefix length, and the gated-delta-rule commit.  name -> (kind, shape)."""
+    out = {name: ("materialize", wl.SHAPES[name]) for name in ("mamba2_2p7b_fp32", "hybrid48_int8", "hybrid48_fp8_sr")}
+    out["hybrid48_fp8_rne"] = ("materialize",
+                               wl.SHAPES["hybrid48_fp8_sr"].replace(name="hybrid48_fp8_rne", philox_rounds=0))
     for k in (0, 1, 4, 16, 64):
-        shp = wl.SHAPES["ring_sweep_fp16"].replace(prefix=("fixed", k))
-        sweep[f"ring_sweep_fp16_k{k}"] = measure_workload(torch, rsm, shp, device, peak_gbs, sms, uuid)
+        out[f"ring_sweep_fp16_k{k}"] = ("materialize", wl.SHAPES["ring_sweep_fp16"].replace(prefix=("fixed", k)))
     gshape = gw.GDN_SHAPES["gdn36_hv32_t8"]
-    sweep["gdn36_hv32_t8"] = measure_gdn(torch, rsm, gshape, device, peak_gbs, sms, uuid)
-    sweep["gdn36_hv32_t8_full"] = measure_gdn(torch, rsm, gshape.replace(accept=("fixed", 8)), device, peak_gbs,
-                                              sms, uuid)
+    out["gdn36_hv32_t8"] = ("gdn", gshape)
+    out["gdn36_hv32_t8_full"] = ("gdn", gshape.replace(accept=("fixed", 8)))
+    return out
+
+
+def measure_named_workloads(torch, rsm, device, peak_gbs, sms, uuid, only=None):
+    sweep = {}
+    for name, (kind, shape) in named_workloads().items():
+        if only and name not in only:
+            continue
+        measure = measure_gdn if kind == "gdn" else measure_workload
+        sweep[name] = measure(torch, rsm, shape, device, peak_gbs, sms, uuid)
     return sweep
 
 
@@ -731,7 +740,8 @@ def main():
     if args.all_workloads or not (args.no_extras or args.no_workloads):
         del dw, call
         torch.cuda.empty_cache()
-        out["workloads"] = measure_named_workloads(torch, rsm, device, peak, sms, uuid)
+        only = set(args.only.split(",")) if args.only else None
+        out["workloads"] = measure_named_workloads(torch, rsm, device, peak, sms, uuid, only)
         out["lane_peaks_note"] = (f"fp32: {sms} SMs x {ALU_LANES_PER_SM} lanes x the sampled SM clock; 32-bit "
                                   f"integer: {sms} SMs x {INT_LANES_PER_SM} lanes x the sampled SM clock")
     if rank == 0:

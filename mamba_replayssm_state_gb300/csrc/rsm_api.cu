@@ -36,10 +36,19 @@ int fail(int code, const char* fmt, ...) {
 
 struct Instance {
   int sf, inf, dim, dstate;
-  const void* (*kernel)();
+  const void* (*kernel)();     // philox_rounds == 0 (16-bit and fp32 state: every call)
+  const void* (*kernel_sr)();  // one-byte state with philox_rounds > 0; NULL otherwise
 };
 
-#define RSM_ENTRY(SF, IF, D, N) {SF, IF, D, N, &rsm::kernel_for<SF, IF, D, N>},
+template <int SF, int IF, int D, int N>
+constexpr const void* (*sr_kernel_getter())() {
+  if constexpr (SF == RSM_I8 || SF == RSM_FP8_E4M3)
+    return &rsm::kernel_for_sr<SF, IF, D, N>;
+  else
+    return nullptr;
+}
+
+#define RSM_ENTRY(SF, IF, D, N) {SF, IF, D, N, &rsm::kernel_for<SF, IF, D, N>, sr_kernel_getter<SF, IF, D, N>()},
 const Instance kInstances[] = {RSM_FOR_EACH_INSTANCE(RSM_ENTRY)};
 #undef RSM_ENTRY
 
@@ -77,9 +86,12 @@ constexpr size_t kNumInstances = sizeof(kInstances) / sizeof(kInstances[0]);
 // largest dynamic shared memory size already configured per (device, instance),
 // and the occupancy found for the last size queried (so that calls made while
 // a stream is being captured issue no queries)
-int g_smem_set[kMaxDevices][kNumInstances + 2];  // + the two tensor-core variants
-int g_occ_smem[kMaxDevices][kNumInstances + 2];  // + the two tensor-core variants
-int g_occ_blocks[kMaxDevices][kNumInstances + 2];  // + the two tensor-core variants
+// (indexed by instance; then the two tensor-core variants; then the
+// stochastic-rounding instances of one-byte state, at kNumInstances + 2 + instance)
+constexpr size_t kNumKernels = 2 * kNumInstances + 2;
+int g_smem_set[kMaxDevices][kNumKernels];
+int g_occ_smem[kMaxDevices][kNumKernels];
+int g_occ_blocks[kMaxDevices][kNumKernels];
 
 int device_info(int dev, DeviceInfo* out) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -172,12 +184,13 @@ bool uses_tensor_cores(const rsm_materialize_args* a) {
 
 struct Launch {
   const void* fn;
-  int grid, smem, stages;
+  int grid, threads, smem, stages;
   rsm::Params params;
 };
 
-constexpr int kSlotsPerSm = 6;  // pipeline slots per SM, over its CTAs
-static_assert(kSlotsPerSm <= rsm::kMaxStages, "slot count");
+constexpr int kSlotsPerSm = 6;      // pipeline slots per SM, over its CTAs
+constexpr int kQ8SlotsPerCta = 4;   // one-byte state
+static_assert(kSlotsPerSm <= rsm::kMaxStages && kQ8SlotsPerCta <= rsm::kMaxStages, "slot count");
 
 int plan_launch(const rsm_materialize_args* a, Launch* L) {
   const int inst = validate(a);
@@ -191,30 +204,42 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
 
   const bool quant = elem_bytes(a->state_dtype) == 1;
   // Items are packed into a byte arena, each taking its tile (+ scales) and
-  // only its own k ring rows.  Two CTAs per SM (two loaders in flight) when
-  // each arena still holds two items of the longest window; otherwise one CTA
-  // per SM with the whole shared memory.
+  // only its own k ring rows.  Several CTAs per SM (as many loaders in
+  // flight) while each arena still holds two items of the longest window:
+  // three for one-byte state (CTAs of four consumer warps), two otherwise;
+  // fewer, down to one CTA with the whole shared memory, for long windows.
   const int sb = elem_bytes(a->state_dtype), ib = elem_bytes(a->input_dtype);
   const int item_min = static_cast<int>(rsm::item_layout(a->dim, a->dstate, sb, quant, ib, 0).bytes);
   const int item_max = static_cast<int>(rsm::item_layout(a->dim, a->dstate, sb, quant, ib, a->max_window).bytes);
   const bool use_tc = uses_tensor_cores(a);
-  const int base = static_cast<int>(use_tc ? rsm::kTcArenaBase : rsm::arena_base(a->dim, a->dstate, sb));
-  const int two_cta = di.smem_per_sm / 2 - di.smem_reserved - base;
-  const int one_cta = di.smem_optin - base;
-  const bool two = two_cta >= 2 * item_max;
-  const int arena = (two ? two_cta : one_cta) / 128 * 128;
-  if (arena < 2 * item_max)
-    return fail(RSM_ENOTSUP, "two work items of %d bytes do not fit in shared memory", item_max);
+  const bool sr_instance = quant && a->philox_rounds > 0;
+  const bool q8 = quant && !sr_instance;  // the four-warp one-byte kernel
+  const int cw = q8 ? rsm::kQ8ConsumerWarps : rsm::kConsumerWarps;
+  const int base = static_cast<int>(use_tc ? rsm::kTcArenaBase : rsm::arena_base(a->dim, a->dstate, sb, cw));
+  const int threads = use_tc ? rsm::kTcThreads : 32 * (1 + cw);
+  int ctas = q8 ? 3 : 2, arena = 0;
+  for (; ctas >= 1; --ctas) {
+    const int per_cta = ctas == 1 ? di.smem_optin : di.smem_per_sm / ctas - di.smem_reserved;
+    arena = (per_cta - base) / 128 * 128;
+    if (arena >= 2 * item_max) break;
+  }
+  if (ctas < 1) return fail(RSM_ENOTSUP, "two work items of %d bytes do not fit in shared memory", item_max);
   // Six items in flight per SM (three per CTA at two CTAs per SM): measured
   // on GB300 against two and four per CTA, it is the fastest with replay at
   // every window length (four per CTA is 2% slower on the 48-layer bf16 shape).
+  // One-byte state: four per CTA (its items are half the size).
   int stages = arena / item_min;
-  if (stages > kSlotsPerSm / (two ? 2 : 1)) stages = kSlotsPerSm / (two ? 2 : 1);
+  const int stage_cap = q8 ? kQ8SlotsPerCta : kSlotsPerSm / ctas;
+  if (stages > stage_cap) stages = stage_cap;
   const int smem = base + arena;
+  const bool two = ctas >= 2;
 
   const void* fn = use_tc ? (a->state_dtype == RSM_BF16 ? rsm::kernel_for_tc<RSM_BF16>() : rsm::kernel_for_tc<RSM_F16>())
-                          : kInstances[inst].kernel();
-  const int ci = use_tc ? static_cast<int>(kNumInstances) + (a->state_dtype == RSM_F16 ? 1 : 0) : inst;
+                   : sr_instance ? kInstances[inst].kernel_sr()
+                                 : kInstances[inst].kernel();
+  const int ci = use_tc        ? static_cast<int>(kNumInstances) + (a->state_dtype == RSM_F16 ? 1 : 0)
+                 : sr_instance ? static_cast<int>(kNumInstances) + 2 + inst
+                               : inst;
   int per_sm = 0;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -226,15 +251,16 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
     if (g_occ_smem[dev][ci] == smem) {
       per_sm = g_occ_blocks[dev][ci];
     } else {
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, rsm::kThreads, smem);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
       if (e != cudaSuccess) return fail(RSM_ECUDA, "occupancy query: %s", cudaGetErrorString(e));
       g_occ_smem[dev][ci] = smem;
       g_occ_blocks[dev][ci] = per_sm;
     }
   }
+  if (verbose()) std::fprintf(stderr, "[replayssm] occupancy query: %d CTAs per SM\n", per_sm);
   // The occupancy query reports one CTA per SM for the tensor-core kernel
   // although its shared memory, registers and threads fit two; on GB300 two
-  // run side by side (each allocates 64 of the SM's 512 TMEM columns).  Were
+  // run side by side (each allocates 128 of the SM's 512 TMEM columns).  Were
   // they not co-scheduled, the persistent grid would only take a second wave.
   if (use_tc && two && per_sm < 2) per_sm = 2;
   if (per_sm < 1) return fail(RSM_ENOTSUP, "kernel does not fit on an SM with %d bytes of shared memory", smem);
@@ -268,13 +294,14 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   p.philox_rounds = a->philox_rounds;
   p.num_slots = a->num_slots;
   p.tc_min_k = use_tc ? rsm::kTcMinK : 0;
-  p.desc0 = use_tc ? rsm::kTcDescBase : rsm::desc_base(a->dim, a->dstate, sb);
+  p.desc0 = use_tc ? rsm::kTcDescBase : rsm::desc_base(a->dim, a->dstate, sb, cw);
   p.arena0 = static_cast<uint32_t>(base);
   p.arena_bytes = static_cast<uint32_t>(arena);
   p.stages = static_cast<uint32_t>(stages);
 
   L->fn = fn;
   L->grid = di.sms * per_sm;
+  L->threads = threads;
   L->smem = smem;
   L->stages = stages;
   return RSM_OK;
@@ -402,9 +429,9 @@ int rsm_materialize(const rsm_materialize_args* args, void* stream) {
   if (verbose())
     std::fprintf(stderr, "[replayssm] state=%s input=%s dim=%d dstate=%d grid=%d block=%d smem=%d stages=%d\n",
                  dtype_name(args->state_dtype), dtype_name(args->input_dtype), args->dim, args->dstate, L.grid,
-                 rsm::kThreads, L.smem, L.stages);
+                 L.threads, L.smem, L.stages);
   void* kargs[] = {&L.params};
-  cudaError_t e = cudaLaunchKernel(L.fn, dim3(L.grid), dim3(rsm::kThreads), kargs, static_cast<size_t>(L.smem),
+  cudaError_t e = cudaLaunchKernel(L.fn, dim3(L.grid), dim3(L.threads), kargs, static_cast<size_t>(L.smem),
                                    static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(RSM_ECUDA, "launch failed: %s", cudaGetErrorString(e));
   g_last_error.clear();
@@ -416,7 +443,7 @@ int rsm_launch_config(const rsm_materialize_args* args, int* grid, int* block, i
   const int rc = plan_launch(args, &L);
   if (rc != RSM_OK) return rc;
   if (grid) *grid = L.grid;
-  if (block) *block = rsm::kThreads;
+  if (block) *block = L.threads;
   if (smem_bytes) *smem_bytes = L.smem;
   if (stages) *stages = L.stages;
   return RSM_OK;

@@ -17,9 +17,13 @@
   RSM_INSTANCES_F32(X) RSM_INSTANCES_BF16(X) RSM_INSTANCES_F16(X) RSM_INSTANCES_Q8(X)
 
 namespace rsm {
-// Defined (explicitly instantiated) in the rsm_inst_*.cu translation units.
+// Defined (explicitly instantiated) in the rsm_inst_*.cu translation units:
+// the kernel for philox_rounds == 0 (16-bit and fp32 state: for every call) ...
 template <int SF, int IF, int D, int N>
 const void* kernel_for();
+// ... and, for one-byte state, the stochastic-rounding instance (rsm_inst_q8sr.cu).
+template <int SF, int IF, int D, int N>
+const void* kernel_for_sr();
 // The tensor-core long-window variant (rsm_inst_tc.cu): 16-bit state, bf16 inputs, 64 x 128.
 template <int SF>
 const void* kernel_for_tc();

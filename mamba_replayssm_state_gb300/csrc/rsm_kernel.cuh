@@ -136,6 +136,8 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
   const uint32_t full0 = smem_addr(smem);
   const uint32_t empty0 = full0 + 8u * kMaxStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
+  constexpr int XC = D * IE / 16, BC = N * IE / 16;  // 16-byte chunks per x row and per B row
+  static_assert(XC >= 1 && XC <= 32 && 32 % XC == 0 && BC >= 1 && BC <= 32 && 32 % BC == 0, "ring row chunks");
 
   // n = position of the first -1 (entries after it are ignored)
   int n = p.Bt;
@@ -377,9 +379,11 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
         desc->head = h;
       }
       if (aligned) {
+        const bool row_copies = k < kChunkedRingMinK;  // ring rows by bulk copies (see below)
         if (lane == 0) {
           fence_proxy_async_smem();
-          mbar_expect_tx(fullb, kTileBytes + (Q ? D * 4u : 0u) + static_cast<uint32_t>(k) * (D + (same_B ? 0 : N)) * IE);
+          mbar_expect_tx(fullb, kTileBytes + (Q ? D * 4u : 0u) +
+                                    (row_copies ? static_cast<uint32_t>(k) * (D + (same_B ? 0 : N)) * IE : 0u));
         }
         __syncwarp();
         if (lane == 0) {
@@ -387,18 +391,49 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
           if constexpr (Q) bulk_g2s(sba + il.off_scale, src_sc, D * 4u, fullb);
           if (k > 0) cp_async_4(desca + static_cast<uint32_t>(offsetof(ItemDesc, A)), A_ptr);
         }
-        // ring rows of this lane's tokens t = lane and t = lane + 32
+        // Ring rows: up to kChunkedRingMinK tokens, one bulk copy per row by
+        // the lanes in parallel.  Longer prefixes as 16-byte cp.async chunks
+        // spread over the lanes, through the load/store units: one small bulk
+        // copy per row queues behind the tile copies on the bulk-copy engine
+        // (measured 15% slower at 64 tokens, while at 16 tokens and less the
+        // chunks cost the loader more than they save).  Lane l copies chunk
+        // l % XC of tokens l / XC, then every 32 / XC tokens further; the
+        // chunk's ring row follows modulo R.
+        if (row_copies) {
+          if (lane < k) {
+            const int64_t xr = static_cast<int64_t>(ring_row[0]) * p.H + h;
+            bulk_g2s(sba + il.off_x + static_cast<uint32_t>(lane) * D * IE, x_slot + xr * (D * IE), D * IE, fullb);
+            if (!same_B)
+              bulk_g2s(sba + il.off_B + static_cast<uint32_t>(lane) * N * IE,
+                       B_slot + (static_cast<int64_t>(ring_row[0]) * G + g) * (N * IE), N * IE, fullb);
+          }
+        } else {
+          const int x_t0 = lane / XC, x_part = lane % XC;
+          int pr = rs + x_t0 - (rs + x_t0 >= p.R ? p.R : 0);
+          while (pr >= p.R) pr -= p.R;
+          for (int t = x_t0; t < k; t += 32 / XC) {
+            cp_async_16(sba + il.off_x + static_cast<uint32_t>(t * D * IE + 16 * x_part),
+                        x_slot + (static_cast<int64_t>(pr) * p.H + h) * (D * IE) + 16 * x_part);
+            pr += 32 / XC;
+            while (pr >= p.R) pr -= p.R;
+          }
+          if (!same_B) {
+            const int b_t0 = lane / BC, b_part = lane % BC;
+            int pb = rs + b_t0 - (rs + b_t0 >= p.R ? p.R : 0);
+            while (pb >= p.R) pb -= p.R;
+            for (int t = b_t0; t < k; t += 32 / BC) {
+              cp_async_16(sba + il.off_B + static_cast<uint32_t>(t * N * IE + 16 * b_part),
+                          B_slot + (static_cast<int64_t>(pb) * G + g) * (N * IE) + 16 * b_part);
+              pb += 32 / BC;
+              while (pb >= p.R) pb -= p.R;
+            }
+          }
+        }
+        // dt of this lane's tokens t = lane and t = lane + 32
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           const int t = lane + 32 * q;
-          if (t < k) {
-            const int64_t xr = static_cast<int64_t>(ring_row[q]) * p.H + h;  // x row [p_t, h] and dt [p_t, h]
-            bulk_g2s(sba + il.off_x + static_cast<uint32_t>(t) * D * IE, x_slot + xr * (D * IE), D * IE, fullb);
-            if (!same_B)
-              bulk_g2s(sba + il.off_B + static_cast<uint32_t>(t) * N * IE,
-                       B_slot + (static_cast<int64_t>(ring_row[q]) * G + g) * (N * IE), N * IE, fullb);
-            cp_async_4(sba + il.off_dt + 4u * t, dt_slot + xr);
-          }
+          if (t < k) cp_async_4(sba + il.off_dt + 4u * t, dt_slot + static_cast<int64_t>(ring_row[q]) * p.H + h);
         }
         cp_async_mbar_arrive(fullb);
       } else {
@@ -527,26 +562,32 @@ static __device__ __noinline__ void store_bytes(unsigned char* dst, uint2 v) {
   for (int q = 0; q < 8; ++q) dst[q] = b[q];
 }
 
-// Stochastic rounding of 8 consecutive elements (two Philox blocks, counter
-// (e/4, dst_slot, layer, 0) with e the first element's index), then the exact
+// The 16 random bits of the elements of one Philox block (eight consecutive
+// elements: element q takes the low (q even) or high (q odd) half of word
+// q / 2), each placed in the upper half of a 32-bit word: the form the
+// rounding rule of sr_round takes.
+__device__ __forceinline__ uint32_t sr_lo16(uint32_t w) { return w << 16; }
+__device__ __forceinline__ uint32_t sr_hi16(uint32_t w) { return w & 0xFFFF0000u; }
+
+// Stochastic rounding of 8 consecutive elements (one Philox block, counter
+// (e/8, dst_slot, layer, 0) with e the first element's index), then the exact
 // pack.  Kept out of line, so that the code of the rounding-to-nearest path,
 // which every call without Philox runs, stays compact.
 template <int SF>
 __device__ __noinline__ typename Vec<SF>::Raw sr_pack8(float2 a0, float2 a1, float2 a2, float2 a3, uint32_t blk,
                                                        uint32_t slot, uint32_t layer, uint32_t key0, uint32_t key1,
                                                        int rounds) {
-  const uint4 r0 = philox4x32(make_uint4(blk, slot, layer, 0u), key0, key1, rounds);
-  const uint4 r1 = philox4x32(make_uint4(blk + 1u, slot, layer, 0u), key0, key1, rounds);
+  const uint4 r = philox4x32(make_uint4(blk, slot, layer, 0u), key0, key1, rounds);
   float2 v[4];
-  v[0] = make_float2(sr_fmt<SF>(a0.x, r0.x), sr_fmt<SF>(a0.y, r0.y));
-  v[1] = make_float2(sr_fmt<SF>(a1.x, r0.z), sr_fmt<SF>(a1.y, r0.w));
-  v[2] = make_float2(sr_fmt<SF>(a2.x, r1.x), sr_fmt<SF>(a2.y, r1.y));
-  v[3] = make_float2(sr_fmt<SF>(a3.x, r1.z), sr_fmt<SF>(a3.y, r1.w));
+  v[0] = make_float2(sr_fmt<SF>(a0.x, sr_lo16(r.x)), sr_fmt<SF>(a0.y, sr_hi16(r.x)));
+  v[1] = make_float2(sr_fmt<SF>(a1.x, sr_lo16(r.y)), sr_fmt<SF>(a1.y, sr_hi16(r.y)));
+  v[2] = make_float2(sr_fmt<SF>(a2.x, sr_lo16(r.z)), sr_fmt<SF>(a2.y, sr_hi16(r.z)));
+  v[3] = make_float2(sr_fmt<SF>(a3.x, sr_lo16(r.w)), sr_fmt<SF>(a3.y, sr_hi16(r.w)));
   return pack_vec_rne<SF>(v);
 }
 
-// The same for two rows of 8 elements (blocks blk_a, blk_a + 1 and blk_b,
-// blk_b + 1): four independent Philox chains side by side.
+// The same for two rows of 8 elements (blocks blk_a and blk_b): two
+// independent Philox chains side by side.
 template <int SF>
 struct RawPair {
   typename Vec<SF>::Raw a, b;
@@ -556,27 +597,23 @@ template <int SF>
 __device__ __noinline__ RawPair<SF> sr_pack8x2(float2 a0, float2 a1, float2 a2, float2 a3, float2 b0, float2 b1,
                                                float2 b2, float2 b3, uint32_t blk_a, uint32_t blk_b, uint32_t slot,
                                                uint32_t layer, uint32_t key0, uint32_t key1, int rounds) {
-  uint4 r0, r1, r2, r3;
+  uint4 r0, r1;
   if (rounds == 10) {
     r0 = philox4x32_r<10>(make_uint4(blk_a, slot, layer, 0u), key0, key1);
-    r1 = philox4x32_r<10>(make_uint4(blk_a + 1u, slot, layer, 0u), key0, key1);
-    r2 = philox4x32_r<10>(make_uint4(blk_b, slot, layer, 0u), key0, key1);
-    r3 = philox4x32_r<10>(make_uint4(blk_b + 1u, slot, layer, 0u), key0, key1);
+    r1 = philox4x32_r<10>(make_uint4(blk_b, slot, layer, 0u), key0, key1);
   } else {
     r0 = philox4x32(make_uint4(blk_a, slot, layer, 0u), key0, key1, rounds);
-    r1 = philox4x32(make_uint4(blk_a + 1u, slot, layer, 0u), key0, key1, rounds);
-    r2 = philox4x32(make_uint4(blk_b, slot, layer, 0u), key0, key1, rounds);
-    r3 = philox4x32(make_uint4(blk_b + 1u, slot, layer, 0u), key0, key1, rounds);
+    r1 = philox4x32(make_uint4(blk_b, slot, layer, 0u), key0, key1, rounds);
   }
   float2 v[4], w[4];
-  v[0] = make_float2(sr_fmt<SF>(a0.x, r0.x), sr_fmt<SF>(a0.y, r0.y));
-  v[1] = make_float2(sr_fmt<SF>(a1.x, r0.z), sr_fmt<SF>(a1.y, r0.w));
-  v[2] = make_float2(sr_fmt<SF>(a2.x, r1.x), sr_fmt<SF>(a2.y, r1.y));
-  v[3] = make_float2(sr_fmt<SF>(a3.x, r1.z), sr_fmt<SF>(a3.y, r1.w));
-  w[0] = make_float2(sr_fmt<SF>(b0.x, r2.x), sr_fmt<SF>(b0.y, r2.y));
-  w[1] = make_float2(sr_fmt<SF>(b1.x, r2.z), sr_fmt<SF>(b1.y, r2.w));
-  w[2] = make_float2(sr_fmt<SF>(b2.x, r3.x), sr_fmt<SF>(b2.y, r3.y));
-  w[3] = make_float2(sr_fmt<SF>(b3.x, r3.z), sr_fmt<SF>(b3.y, r3.w));
+  v[0] = make_float2(sr_fmt<SF>(a0.x, sr_lo16(r0.x)), sr_fmt<SF>(a0.y, sr_hi16(r0.x)));
+  v[1] = make_float2(sr_fmt<SF>(a1.x, sr_lo16(r0.y)), sr_fmt<SF>(a1.y, sr_hi16(r0.y)));
+  v[2] = make_float2(sr_fmt<SF>(a2.x, sr_lo16(r0.z)), sr_fmt<SF>(a2.y, sr_hi16(r0.z)));
+  v[3] = make_float2(sr_fmt<SF>(a3.x, sr_lo16(r0.w)), sr_fmt<SF>(a3.y, sr_hi16(r0.w)));
+  w[0] = make_float2(sr_fmt<SF>(b0.x, sr_lo16(r1.x)), sr_fmt<SF>(b0.y, sr_hi16(r1.x)));
+  w[1] = make_float2(sr_fmt<SF>(b1.x, sr_lo16(r1.y)), sr_fmt<SF>(b1.y, sr_hi16(r1.y)));
+  w[2] = make_float2(sr_fmt<SF>(b2.x, sr_lo16(r1.z)), sr_fmt<SF>(b2.y, sr_hi16(r1.z)));
+  w[3] = make_float2(sr_fmt<SF>(b3.x, sr_lo16(r1.w)), sr_fmt<SF>(b3.y, sr_hi16(r1.w)));
   return RawPair<SF>{pack_vec_rne<SF>(v), pack_vec_rne<SF>(w)};
 }
 
@@ -600,7 +637,8 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
   constexpr int V2 = VEC / 2;
   using Raw = typename Vec<SF>::Raw;
   constexpr int XW = SLAB_ROWS % 4 == 0 ? 4 : (SLAB_ROWS % 2 == 0 ? 2 : 1);
-  float* bbuf = cbuf + kTokChunk * SLAB_ROWS;
+  static_assert(RPT == 1 || RPT % 2 == 0, "rows per thread");
+  float* bbuf = cbuf + kTokChunk * 2 * SLAB_ROWS;  // after the (c, c) pairs of kTokChunk tokens
   const int lane_row = lane / LPR, lane_col = lane % LPR;
   const int slab_row0 = (cw / CT) * SLAB_ROWS;
   const int tile_col0 = (cw % CT) * COLS;
@@ -648,8 +686,8 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
     __syncwarp();  // wbuf visible to the whole warp
 
     // the prefix, kTokChunk tokens at a time: convert this warp's share of
-    // the tokens to fp32 (c = w*x for its rows, B for its columns), then one
-    // rank-1 update per token with packed fp32x2 FMAs
+    // the tokens to fp32 (c = w*x for its rows, each as an (c, c) pair, and B
+    // for its columns), then one rank-1 update per token with packed fp32x2 FMAs
     const unsigned char* xs = sb + il.off_x;
     const unsigned char* Bs = sb + il.off_B;
     for (int t0 = 0; t0 < k; t0 += kTokChunk) {
@@ -659,13 +697,16 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
         float xv[XW];
         load_inputs<IF, XW>(xs + ((t0 + t) * D + slab_row0 + rx) * IE, xv);
         const float wt = wbuf[t0 + t];
-        float* dst = cbuf + t * SLAB_ROWS + rx;
-        if constexpr (XW == 4) {
-          *reinterpret_cast<float4*>(dst) = make_float4(xv[0] * wt, xv[1] * wt, xv[2] * wt, xv[3] * wt);
-        } else if constexpr (XW == 2) {
-          *reinterpret_cast<float2*>(dst) = make_float2(xv[0] * wt, xv[1] * wt);
-        } else {
-          dst[0] = xv[0] * wt;
+        float* dst = cbuf + t * 2 * SLAB_ROWS + 2 * rx;
+#pragma unroll
+        for (int q = 0; q < XW; q += 2) {
+          if constexpr (XW == 1) {
+            const float c0 = xv[0] * wt;
+            *reinterpret_cast<float2*>(dst) = make_float2(c0, c0);
+          } else {
+            const float c0 = xv[q] * wt, c1 = xv[q + 1] * wt;
+            *reinterpret_cast<float4*>(dst + 2 * q) = make_float4(c0, c0, c1, c1);
+          }
         }
       }
       for (int u = lane; u < tn * (COLS / 8); u += 32) {
@@ -684,27 +725,18 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
       if (worker) {
 #pragma unroll 2
         for (int t = 0; t < tn; ++t) {
-          float c[RPT];
+          float2 c2[RPT];  // (c_r, c_r) for this thread's rows
           float2 b2[V2];
-          if constexpr (RPT % 4 == 0) {
-#pragma unroll
-            for (int r = 0; r < RPT; r += 4) {
-              const float4 v = *reinterpret_cast<const float4*>(cbuf + t * SLAB_ROWS + rrow + r);
-              c[r] = v.x;
-              c[r + 1] = v.y;
-              c[r + 2] = v.z;
-              c[r + 3] = v.w;
-            }
-          } else if constexpr (RPT % 2 == 0) {
-#pragma unroll
-            for (int r = 0; r < RPT; r += 2) {
-              const float2 v = *reinterpret_cast<const float2*>(cbuf + t * SLAB_ROWS + rrow + r);
-              c[r] = v.x;
-              c[r + 1] = v.y;
-            }
+          const float* cp = cbuf + t * 2 * SLAB_ROWS + 2 * rrow;
+          if constexpr (RPT == 1) {
+            c2[0] = *reinterpret_cast<const float2*>(cp);
           } else {
 #pragma unroll
-            for (int r = 0; r < RPT; ++r) c[r] = cbuf[t * SLAB_ROWS + rrow + r];
+            for (int r = 0; r < RPT; r += 2) {
+              const float4 v = *reinterpret_cast<const float4*>(cp + 2 * r);
+              c2[r] = make_float2(v.x, v.y);
+              c2[r + 1] = make_float2(v.z, v.w);
+            }
           }
 #pragma unroll
           for (int g = 0; g < VEC / 4; ++g) {
@@ -714,9 +746,8 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
           }
 #pragma unroll
           for (int r = 0; r < RPT; ++r) {
-            const float2 c2 = make_float2(c[r], c[r]);
 #pragma unroll
-            for (int u = 0; u < V2; ++u) acc[r][u] = __ffma2_rn(c2, b2[u], acc[r][u]);
+            for (int u = 0; u < V2; ++u) acc[r][u] = __ffma2_rn(c2[r], b2[u], acc[r][u]);
           }
         }
       }
@@ -792,11 +823,11 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
       if (worker) {
         if (use_sr) {
           if constexpr (SF != RSM_F32) {
-            // Philox counter of element e: (e / 4, dst_slot, layer, 0); a row's
-            // 8 elements start on a multiple of 8
+            // Philox counter of element e: (e / 8, dst_slot, layer, 0); a row's
+            // 8 elements start on a multiple of 8, so they are one block
             static_assert(V2 == 4, "stochastic rounding works on 8-element vectors");
-            const uint32_t blk0 = static_cast<uint32_t>(((static_cast<int64_t>(h) * D + row0) * N + col0) >> 2);
-            constexpr uint32_t kRowBlocks = N / 4;
+            const uint32_t blk0 = static_cast<uint32_t>(((static_cast<int64_t>(h) * D + row0) * N + col0) >> 3);
+            constexpr uint32_t kRowBlocks = N / 8;
             if constexpr (RPT % 2 == 0) {
 #pragma unroll
               for (int r = 0; r < RPT; r += 2) {
@@ -830,7 +861,7 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
           if constexpr (SF != RSM_F32) {
             static_assert(V2 == 4, "stochastic rounding works on 8-element vectors");
             const int64_t e0 = (static_cast<int64_t>(h) * D + row0 + r) * N + col0;
-            out = sr_pack8<SF>(acc[r][0], acc[r][1], acc[r][2], acc[r][3], static_cast<uint32_t>(e0 >> 2), dst_slot_id,
+            out = sr_pack8<SF>(acc[r][0], acc[r][1], acc[r][2], acc[r][3], static_cast<uint32_t>(e0 >> 3), dst_slot_id,
                                layer_id, key0, key1, p.philox_rounds);
           }
         } else {
@@ -1003,11 +1034,22 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_kernel(const __grid_c
     run_consumer<SF, IF, D, N>(p, smem, warp - 1, lane);
 }
 
-// Instantiation hook: each translation unit that includes this header with
-// RSM_INSTANTIATE defined provides kernel_for<...>() for its formats.
+// The one-byte kernel (rsm_q8_kernel.cuh).
+template <int SF, int IF, bool SR>
+const void* q8_kernel();
+
+// Instantiation hook: each translation unit that includes this header (and,
+// for one-byte state, rsm_q8_kernel.cuh) provides kernel_for<...>() for its
+// formats: the kernel a call with philox_rounds == 0 launches, and for 16-bit
+// and fp32 state the one for every call.
 template <int SF, int IF, int D, int N>
 const void* kernel_for() {
-  return reinterpret_cast<const void*>(&materialize_kernel<SF, IF, D, N>);
+  if constexpr (Fmt<SF>::quant) {
+    static_assert(D == 64 && N == 128, "one-byte state is 64 x 128");
+    return q8_kernel<SF, IF, false>();
+  } else {
+    return reinterpret_cast<const void*>(&materialize_kernel<SF, IF, D, N>);
+  }
 }
 
 }  // namespace rsm

@@ -5,9 +5,16 @@
 
 namespace rsm {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 8;  // 16-bit and fp32 state, and the tensor-core kernel
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kThreads = 32 + kConsumerThreads;
+// One-byte state rounded to nearest: four consumer warps per CTA (each lane
+// owns 64 codes, so the per-item work of a lane is spread over twice the
+// elements), three CTAs per SM.  (With stochastic rounding, whose Philox
+// chains want more warps in flight, one-byte state takes the eight-warp kernel.)
+constexpr int kQ8ConsumerWarps = 4;
+constexpr int kQ8Threads = 32 * (1 + kQ8ConsumerWarps);
+constexpr int kQ8MaxRegs = 128;  // 15 warps per SM: four on three sub-partitions, 4 x 32 x 128 = 16384
 constexpr int kMaxWindow = 64;
 constexpr int kMaxStages = 16;
 constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // 4 s: never reached by a correct run
@@ -21,6 +28,9 @@ constexpr uint32_t kWeightStride = kMaxWindow + 4;  // floats per consumer warp:
 constexpr uint32_t kWarpBufOff = 3072;  // per-consumer-warp fp32 token-chunk buffers start here
 static_assert(kWeightOff + kConsumerWarps * kWeightStride * 4 <= kWarpBufOff, "smem head overflow");
 constexpr int kTokChunk = 8;  // tokens converted to fp32 per consumer-warp pass
+// Ring rows of prefixes this long or longer are fetched as 16-byte cp.async
+// chunks spread over the loader's lanes; shorter ones as one bulk copy per row.
+constexpr int kChunkedRingMinK = 32;
 
 // How the consumer warps tile a [dim, dstate] state tile.  Each thread owns
 // RPT consecutive rows x VEC consecutive columns (one vector per row).
@@ -31,7 +41,8 @@ struct ThreadLayout {
   int vec, tct, lpr, rpw, ct, slabs, slab_rows, rpt, cols;
 };
 
-__host__ __device__ constexpr ThreadLayout thread_layout(int dim, int dstate, int state_bytes) {
+__host__ __device__ constexpr ThreadLayout thread_layout(int dim, int dstate, int state_bytes,
+                                                         int cw = kConsumerWarps) {
   // 16-byte vectors, except one-byte formats: 8 codes (8 bytes), with a whole
   // row inside one warp so that the row's amax is a warp reduction
   const int vec = state_bytes == 1 ? 8 : 16 / state_bytes;
@@ -39,18 +50,20 @@ __host__ __device__ constexpr ThreadLayout thread_layout(int dim, int dstate, in
   const int lpr = state_bytes == 1 ? tct : (tct < 8 ? tct : 8);
   const int rpw = 32 / lpr;
   const int ct = tct / lpr;
-  const int slabs = kConsumerWarps / ct;
+  const int slabs = cw / ct;
   const int slab_rows = dim / slabs;
   const int rpt = slab_rows >= rpw ? slab_rows / rpw : 1;
   return ThreadLayout{vec, tct, lpr, rpw, ct, slabs, slab_rows, rpt, lpr * vec};
 }
 
 // fp32 floats in one consumer warp's token-chunk buffer: c = w*x for its
-// slab's rows and B for its column tile, kTokChunk tokens each.
-__host__ __device__ constexpr uint32_t warp_buf_floats(int dim, int dstate, int state_bytes) {
+// slab's rows, each stored twice (an (c, c) pair feeds a packed fp32x2 FMA
+// without a register move), and B for its column tile, kTokChunk tokens each.
+__host__ __device__ constexpr uint32_t warp_buf_floats(int dim, int dstate, int state_bytes,
+                                                       int cw = kConsumerWarps) {
   return static_cast<uint32_t>(kTokChunk *
-                               (thread_layout(dim, dstate, state_bytes).slab_rows +
-                                thread_layout(dim, dstate, state_bytes).cols));
+                               (2 * thread_layout(dim, dstate, state_bytes, cw).slab_rows +
+                                thread_layout(dim, dstate, state_bytes, cw).cols));
 }
 
 __host__ __device__ constexpr uint32_t round_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
@@ -58,13 +71,13 @@ __host__ __device__ constexpr uint32_t round_up(uint32_t v, uint32_t a) { return
 constexpr uint32_t kDescBytes = 48;  // sizeof(ItemDesc)
 
 // Offset of the descriptor table: the fixed head plus the consumer warps' buffers.
-__host__ __device__ constexpr uint32_t desc_base(int dim, int dstate, int state_bytes) {
-  return round_up(kWarpBufOff + kConsumerWarps * warp_buf_floats(dim, dstate, state_bytes) * 4u, 128u);
+__host__ __device__ constexpr uint32_t desc_base(int dim, int dstate, int state_bytes, int cw = kConsumerWarps) {
+  return round_up(kWarpBufOff + cw * warp_buf_floats(dim, dstate, state_bytes, cw) * 4u, 128u);
 }
 
 // Offset of the item arena (after one descriptor per pipeline slot).
-__host__ __device__ constexpr uint32_t arena_base(int dim, int dstate, int state_bytes) {
-  return round_up(desc_base(dim, dstate, state_bytes) + kMaxStages * kDescBytes, 128u);
+__host__ __device__ constexpr uint32_t arena_base(int dim, int dstate, int state_bytes, int cw = kConsumerWarps) {
+  return round_up(desc_base(dim, dstate, state_bytes, cw) + kMaxStages * kDescBytes, 128u);
 }
 
 // Byte layout of one work item in the arena: the source tile at offset 0, its
@@ -95,20 +108,33 @@ __host__ __device__ constexpr uint32_t arena_next(uint32_t head, uint32_t item_m
 }
 
 // Shared memory of the tensor-core (long-window) variant: the same head up to
-// kWarpBufOff, then its mbarriers (MMA completion, two consumer-wide
-// barriers and a spare, exit) and the TMEM address word, the two MMA operands, the
-// descriptor table and the arena.
+// kWarpBufOff, then its mbarriers and the TMEM address word, the two MMA
+// operands, the descriptor table and the arena.  Its consumer warps form two
+// groups: a builder group (operands, MMA issue) and an epilogue group (TMEM ->
+// state), joined by two TMEM accumulators so that consecutive items overlap.
 constexpr int kTcMinWindow = 16;                  // tensor path for max_window >= this (16-bit state)
 constexpr int kTcKMax = kMaxWindow;               // tokens one item's MMA covers at most
-constexpr uint32_t kTcBarOff = kWarpBufOff;       // mma, x1, x2, (spare), exit mbarriers (+0 .. +39)
-constexpr uint32_t kTcTmemSlot = kTcBarOff + 40;  // TMEM base address written by tcgen05.alloc
+// CTA of the tensor-core kernel: the loader warp, kTcBuilderWarps builder
+// warps and four epilogue warps (one per TMEM lane quarter); eight warps, so
+// that two CTAs per SM leave 128 registers a thread.
+constexpr int kTcBuilderWarps = 3;
+constexpr int kTcEpilogueWarps = 4;
+constexpr int kTcConsumerWarps = kTcBuilderWarps + kTcEpilogueWarps;
+constexpr int kTcThreads = 32 * (1 + kTcConsumerWarps);
+constexpr uint32_t kTcBarOff = kWarpBufOff;       // mbarriers, see below
+constexpr uint32_t kTcMmaDone = kTcBarOff;        // [2] an accumulator's MMAs completed (1 arrival: commit)
+constexpr uint32_t kTcTmemFree = kTcBarOff + 16;  // [2] the epilogue read an accumulator (kTcEpilogueWarps)
+constexpr uint32_t kTcBuildBar = kTcBarOff + 32;  // the builder group's operands are written (kTcBuilderWarps)
+constexpr uint32_t kTcExitBar = kTcBarOff + 40;   // every consumer warp is done with TMEM (kTcConsumerWarps)
+constexpr uint32_t kTcTmemSlot = kTcBarOff + 48;  // TMEM base address written by tcgen05.alloc
 constexpr uint32_t kTcAOff = kTcBarOff + 128;     // A = B^T: [128 dstate rows][kTcKMax tokens] bf16 core matrices
 constexpr uint32_t kTcBOff = kTcAOff + 128 * kTcKMax * 2;  // C^T: [64 dim rows][kTcKMax tokens] bf16
 constexpr uint32_t kTcSbo = (kTcKMax / 8) * 128;  // bytes between 8-row groups of an operand
-constexpr uint32_t kTcTmemCols = 64;              // fp32 accumulator: 128 lanes x 64 columns
+constexpr uint32_t kTcAccCols = 64;               // one fp32 accumulator: 128 lanes x 64 columns
+constexpr uint32_t kTcTmemCols = 2 * kTcAccCols;  // two accumulators
 constexpr uint32_t kTcDescBase = round_up(kTcBOff + 64 * kTcKMax * 2, 128u);
 constexpr uint32_t kTcArenaBase = round_up(kTcDescBase + kMaxStages * kDescBytes, 128u);
-constexpr int kTcMinK = 7;  // shorter prefixes are applied on the CUDA cores (measured crossover)
+constexpr int kTcMinK = 1;  // every prefix of one token or more goes through the MMA
 
 struct Params {
   const int64_t* state_ptrs;

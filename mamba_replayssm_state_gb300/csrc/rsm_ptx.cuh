@@ -97,6 +97,12 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through L2 (both 16-byte aligned).
+// It goes through the load/store units, not the bulk-copy (TMA) engine.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
 // The mbarrier's current phase will not complete before all of this thread's
 // earlier cp.async copies have landed (pending count +1, async arrive later).
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {

@@ -36,9 +36,10 @@
  *    qmax/amax is not finite (amax == 0, or so small that the scale cannot
  *    be inverted in fp32) is stored as zero codes with scale 0;
  *  - stochastic rounding: Philox-4x32 with philox_rounds rounds,
- *    key = (lo32(seed), hi32(seed)), counter = (e>>2, dst_slot, layer, 0) with
- *    e = (h*dim + i)*dstate + j, word e&3; round the magnitude up iff
- *    word * ulp < (|y| - lo) * 2^32, then saturate.
+ *    key = (lo32(seed), hi32(seed)), counter = (e>>3, dst_slot, layer, 0) with
+ *    e = (h*dim + i)*dstate + j; element e takes the 16-bit half e&1 (low half
+ *    first) of output word (e>>1)&3 as r; round the magnitude up iff
+ *    r * 2^16 * ulp < (|y| - lo) * 2^32, then saturate.
  */
 #include "replayssm_oracle.h"
 
@@ -236,15 +237,18 @@ void oracle_philox4x32(const uint32_t ctr[4], const uint32_t key[2], int rounds,
   out[3] = c3;
 }
 
-/* The stochastic-rounding word of element e of (layer, dst slot). */
+/* The stochastic-rounding word of element e of (layer, dst slot): its 16
+ * random bits r in the upper half of a 32-bit word (r * 2^16), so that the
+ * rounding rule of oracle_round applies to it unchanged. */
 static uint32_t sr_word(const oracle_args *a, int layer, int32_t dst, int64_t e) {
   int64_t seed = *a->rand_seed;
   uint32_t key[2] = {(uint32_t)((uint64_t)seed & 0xFFFFFFFFu),
                      (uint32_t)((uint64_t)seed >> 32)};
-  uint32_t ctr[4] = {(uint32_t)(e >> 2), (uint32_t)dst, (uint32_t)layer, 0u};
+  uint32_t ctr[4] = {(uint32_t)(e >> 3), (uint32_t)dst, (uint32_t)layer, 0u};
   uint32_t out[4];
   oracle_philox4x32(ctr, key, a->philox_rounds, out);
-  return out[e & 3];
+  uint32_t r = (e & 1) ? (out[(e >> 1) & 3] >> 16) : (out[(e >> 1) & 3] & 0xFFFFu);
+  return r << 16;
 }
 
 /* ------------------------------------------------------------------------ */

@@ -611,10 +611,11 @@ def test_one_request_copy_draws_the_calls_philox_words(sd):
 # The counter layout of stochastic rounding is this library's own convention
 # (API page, Parameters: rand_seed, philox_rounds): Philox-4x32 with
 # philox_rounds rounds, key = (lo32(seed), hi32(seed)), counter =
-# (e >> 2, dst_slot, layer, 0) with e = (h*dim + i)*dstate + j, and element e
-# takes word e & 3.  The pins below predict every stored byte of a call from
-# that statement, the known-answer-pinned Philox and the bit-level rounding
-# rule, without the oracle's materialization code.
+# (e >> 3, dst_slot, layer, 0) with e = (h*dim + i)*dstate + j, and element e
+# takes 16 random bits: the low (e even) or high (e odd) half of output word
+# (e >> 1) & 3.  The pins below predict every stored byte of a call from that
+# statement, the known-answer-pinned Philox and the bit-level rounding rule,
+# without the oracle's materialization code.
 
 SR_SEED = 0x0123_4567_89AB_CDEF   # hi32 != lo32, so a dropped or swapped key word shows
 
@@ -653,46 +654,48 @@ def _exact_f32_result(w, l):
 
 
 def _words(w, l, layout="reading"):
-    """The stochastic-rounding word of every element of (layer l, dst slot), [H*D*N]."""
+    """The 16 random bits of every element of (layer l, dst slot), [H*D*N],
+    from the written layout (or from one of the planted wrong ones)."""
     H, D, N = w.H, w.D, w.N
     dst = int(w.dst_slots[l, 0])
     lo, hi = SR_SEED & 0xFFFFFFFF, SR_SEED >> 32
     out = np.zeros(H * D * N, np.uint64)
-    for blk in range(H * D * N // 4):
-        if layout in ("reading", "word_shifted"):
-            ctr, key = (blk, dst, l, 0), (lo, hi)
-        elif layout == "swap_counter_words":
-            ctr, key = (dst, blk, l, 0), (lo, hi)
+    for blk in range(H * D * N // 8):
+        ctr, key = (blk, dst, l, 0), (lo, hi)
+        if layout == "swap_counter_words":
+            ctr = (dst, blk, l, 0)
         elif layout == "slot_and_layer_swapped":
-            ctr, key = (blk, l, dst, 0), (lo, hi)
+            ctr = (blk, l, dst, 0)
         elif layout == "hi32_dropped":
-            ctr, key = (blk, dst, l, 0), (lo, 0)
-        else:
-            raise ValueError(layout)
+            key = (lo, 0)
         r = oracle.philox4x32(ctr, key, 10)
-        for q in range(4):
-            idx = 4 * blk + (q if layout != "word_shifted" else (q + 1) % 4)
-            out[idx] = r[q]
+        for q in range(8):
+            word, half = r[q >> 1], q & 1
+            if layout == "word_shifted":
+                word = r[((q >> 1) + 1) % 4]
+            elif layout == "halves_swapped":
+                half ^= 1
+            out[8 * blk + q] = (word >> 16) if half else (word & 0xFFFF)
     return out
 
 
-def _predict_bf16(y32, words):
-    """Stochastic rounding to bf16 on the bit pattern: the 16 discarded bits are
-    compared with the word's top 16 bits (up iff word * 2^-16 ulp-units < them)."""
+def _predict_bf16(y32, r16):
+    """Stochastic rounding to bf16 on the bit pattern: up iff the 16 random bits
+    are below the 16 discarded bits."""
     bits = y32.reshape(-1).view(np.uint32).astype(np.uint64)
     sign, mag = bits >> 31, bits & 0x7FFFFFFF
-    up = (words >> 16) < (mag & 0xFFFF)
+    up = r16 < (mag & 0xFFFF)
     return (((mag >> 16) + up.astype(np.uint64)) | (sign << 15)).astype(np.uint16)
 
 
-def _predict_e4m3(q32, words):
-    """Stochastic rounding to fp8 e4m3fn where |q| >= 2^-6 (normal grid: the 20
-    discarded bits against the word's top 20 bits), saturated at 448; None
-    below 2^-6 (the subnormal grid, not predicted here)."""
+def _predict_e4m3(q32, r16):
+    """Stochastic rounding to fp8 e4m3fn where |q| >= 2^-6 (normal grid: up iff
+    r * 2^4, the random fraction in units of the 20 discarded bits, is below
+    them), saturated at 448; not predicted below 2^-6 (the subnormal grid)."""
     import torch
     bits = q32.reshape(-1).view(np.uint32).astype(np.uint64)
     sign, mag = bits >> 31, bits & 0x7FFFFFFF
-    up = (words >> 12) < (mag & 0xFFFFF)
+    up = (r16 << 4) < (mag & 0xFFFFF)
     r = (((mag >> 20) + up.astype(np.uint64)) << 20).astype(np.uint32).view(np.float32)
     r = np.minimum(r, np.float32(448.0)) * np.where(sign == 1, -1, 1).astype(np.float32)
     codes = torch.from_numpy(r.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
@@ -709,7 +712,7 @@ def test_philox_counter_layout_predicts_every_bf16_byte():
         got = out.state[l][dst].reshape(-1)
         assert np.array_equal(_predict_bf16(y32, _words(w, l)), got), f"layer {l}"
         # each planted mistake in the layout moves a good share of the bytes
-        for bad in ("swap_counter_words", "slot_and_layer_swapped", "hi32_dropped", "word_shifted"):
+        for bad in ("swap_counter_words", "slot_and_layer_swapped", "hi32_dropped", "word_shifted", "halves_swapped"):
             wrong = _predict_bf16(y32, _words(w, l, bad))
             assert (wrong != got).mean() > 0.2, (l, bad)
 
@@ -729,7 +732,7 @@ def test_philox_counter_layout_predicts_every_fp8_byte():
         got = out.state[l][dst].reshape(-1)
         assert np.array_equal(codes[normal], got[normal]), f"layer {l}"
         predicted += int(normal.sum())
-        for bad in ("swap_counter_words", "slot_and_layer_swapped", "hi32_dropped", "word_shifted"):
+        for bad in ("swap_counter_words", "slot_and_layer_swapped", "hi32_dropped", "word_shifted", "halves_swapped"):
             wrong, _ = _predict_e4m3(q32, _words(w, l, bad))
             assert (wrong[normal] != got[normal]).mean() > 0.2, (l, bad)
     assert predicted >= 0.95 * w.L * w.H * w.D * w.N
