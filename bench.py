@@ -423,21 +423,26 @@ def e2e_measure(torch, rsm, shape, n_req, steps, device, groups=8):
 
 ALU_LANES_PER_SM = 128  # FP32 lanes per SM (Blackwell: 4 sub-partitions x 32)
 INT_LANES_PER_SM = 64   # 32-bit integer lanes per SM (4 sub-partitions x 16): LOP3, IADD3, SHF, IMAD
+# Philox-4x32 output words per SM per clock at 10 rounds, measured on GB300 by
+# a loop of independent generator calls (bound by the 32x32->64-bit multiplies);
+# the rate scales as 10 / rounds.  Stochastic rounding uses 16 bits per element.
+PHILOX10_WORDS_PER_SM_CLK = 6.8
 
 
 def lane_ops(shape, active, prefix, src, dst):
     """(fp32 lane-operations, 32-bit integer lane-operations) one call needs,
-    counted from the method, not from the code.  Per element of a replayed
-    tile: one FMUL (the decay product) and one FFMA per token.  With Philox
-    rounding, per element philox_rounds * 6 / 4 integer operations (a round is
-    two 32x32->64-bit multiplies, two three-way XORs and two key additions, and
-    one call gives four words) plus 4 for the rounding decision (shift, add,
-    mask, saturate).  Copies (prefix 0) cost neither."""
+    counted from the method, not from the code, and the elements rounded
+    stochastically.  Per element of a replayed tile: one FMUL (the decay
+    product) and one FFMA per token.  With Philox rounding, per element
+    philox_rounds * 6 / 8 integer operations (a round is two 32x32->64-bit
+    multiplies, two three-way XORs and two key additions, and one call gives
+    the 16-bit numbers of eight elements) plus 4 for the rounding decision
+    (shift, add, mask, saturate).  Copies (prefix 0) cost neither."""
     import numpy as np
     n = int(np.argmax(active == -1)) if (active == -1).any() else len(active)
     elems = shape.H * shape.D * shape.N
-    fp32 = integer = 0
-    sr_per_elem = shape.philox_rounds * 6 / 4 + 4 if shape.philox_rounds > 0 else 0
+    fp32 = integer = rounded = 0
+    sr_per_elem = shape.philox_rounds * 6 / 8 + 4 if shape.philox_rounds > 0 else 0
     for b in active[:n]:
         b = int(b)
         k = int(prefix[b])
@@ -446,7 +451,8 @@ def lane_ops(shape, active, prefix, src, dst):
         live = sum(1 for l in range(shape.L) if src[l, b] != shape.pad_slot_id and dst[l, b] != shape.pad_slot_id)
         fp32 += live * elems * (k + 1)
         integer += live * elems * sr_per_elem
-    return fp32, int(integer)
+        rounded += live * elems if shape.philox_rounds > 0 else 0
+    return fp32, int(integer), rounded
 
 
 def timed_calls(torch, call, stream, uuid, seconds=1.0):
@@ -475,14 +481,20 @@ def timed_calls(torch, call, stream, uuid, seconds=1.0):
     return e0.elapsed_time(e1) / steps, steps, info
 
 
-def _fractions(nbytes, fp32_ops, int_ops, ms, peak_gbs, sms, clock_info):
+def _fractions(nbytes, fp32_ops, int_ops, ms, peak_gbs, sms, clock_info, rounded=0, rounds=0):
     mhz = (clock_info or {}).get("sm_mhz") or 2070.0
     sec = ms * 1e-3
     fr = {"hbm_frac": nbytes / sec / 1e9 / peak_gbs, "hbm_frac_spec": nbytes / sec / 1e9 / SPEC_HBM_GBS,
           "fp32_lane_frac": fp32_ops / sec / (sms * ALU_LANES_PER_SM * mhz * 1e6),
           "int_lane_frac": int_ops / sec / (sms * INT_LANES_PER_SM * mhz * 1e6)}
-    fr["bound"] = max((("hbm", fr["hbm_frac"]), ("fp32", fr["fp32_lane_frac"]), ("int", fr["int_lane_frac"])),
-                      key=lambda kv: kv[1])[0]
+    if rounds > 0:
+        # Philox words the rounding needs (two elements a word) against the measured generator rate
+        words_peak = PHILOX10_WORDS_PER_SM_CLK * 10.0 / rounds * sms * mhz * 1e6
+        fr["philox_frac"] = rounded / 2 / sec / words_peak
+    cands = [("hbm", fr["hbm_frac"]), ("fp32", fr["fp32_lane_frac"]), ("int", fr["int_lane_frac"])]
+    if "philox_frac" in fr:
+        cands.append(("philox", fr["philox_frac"]))
+    fr["bound"] = max(cands, key=lambda kv: kv[1])[0]
     return fr
 
 
@@ -495,7 +507,7 @@ def measure_workload(torch, rsm, shape, device, peak_gbs, sms, uuid):
     prefix = dw.replay_prefix_len.cpu().numpy()
     src, dst = dw.src_slots.cpu().numpy(), dw.dst_slots.cpu().numpy()
     state_b, ring_b, n = workload_bytes(shape, active, prefix, src, dst)
-    fp32_ops, int_ops = lane_ops(shape, active, prefix, src, dst)
+    fp32_ops, int_ops, rounded = lane_ops(shape, active, prefix, src, dst)
     kw = dw.call_kwargs()
     call = rsm.prepare(**kw)
     kernel = rsm.kernel_name(**kw)
@@ -510,7 +522,8 @@ def measure_workload(torch, rsm, shape, device, peak_gbs, sms, uuid):
            "philox_rounds": shape.philox_rounds, "pad_frac": shape.pad_frac, "ms_per_call": ms, "steps": steps,
            "algorithmic_bytes": state_b + ring_b, "state_gbs": state_b / (ms * 1e-3) / 1e9,
            "us_per_request": ms * 1e3 / max(n, 1), "fp32_lane_ops": fp32_ops, "int_lane_ops": int_ops}
-    out.update(_fractions(state_b + ring_b, fp32_ops, int_ops, ms, peak_gbs, sms, clock_info))
+    out.update(_fractions(state_b + ring_b, fp32_ops, int_ops, ms, peak_gbs, sms, clock_info, rounded,
+                          shape.philox_rounds))
     out["clocks"] = clock_info
     out["device_status"] = status
     return out
@@ -743,7 +756,9 @@ def main():
         only = set(args.only.split(",")) if args.only else None
         out["workloads"] = measure_named_workloads(torch, rsm, device, peak, sms, uuid, only)
         out["lane_peaks_note"] = (f"fp32: {sms} SMs x {ALU_LANES_PER_SM} lanes x the sampled SM clock; 32-bit "
-                                  f"integer: {sms} SMs x {INT_LANES_PER_SM} lanes x the sampled SM clock")
+                                  f"integer: {sms} SMs x {INT_LANES_PER_SM} lanes x the sampled SM clock; Philox: "
+                                  f"{PHILOX10_WORDS_PER_SM_CLK} words per SM per clock at 10 rounds (measured), "
+                                  f"two elements a word")
     if rank == 0:
         print(json.dumps(out), flush=True)
     dist.barrier()

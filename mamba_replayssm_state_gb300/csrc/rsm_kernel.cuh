@@ -137,6 +137,7 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
   const uint32_t empty0 = full0 + 8u * kMaxStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
   constexpr int XC = D * IE / 16, BC = N * IE / 16;  // 16-byte chunks per x row and per B row
+  static_assert(kChunkedRingMinK <= 32, "ring rows by bulk copies: one token per lane");
   static_assert(XC >= 1 && XC <= 32 && 32 % XC == 0 && BC >= 1 && BC <= 32 && 32 % BC == 0, "ring row chunks");
 
   // n = position of the first -1 (entries after it are ignored)

@@ -127,12 +127,19 @@ constexpr uint32_t kTcTmemFree = kTcBarOff + 16;  // [2] the epilogue read an ac
 constexpr uint32_t kTcBuildBar = kTcBarOff + 32;  // the builder group's operands are written (kTcBuilderWarps)
 constexpr uint32_t kTcExitBar = kTcBarOff + 40;   // every consumer warp is done with TMEM (kTcConsumerWarps)
 constexpr uint32_t kTcTmemSlot = kTcBarOff + 48;  // TMEM base address written by tcgen05.alloc
-constexpr uint32_t kTcAOff = kTcBarOff + 128;     // A = B^T: [128 dstate rows][kTcKMax tokens] bf16 core matrices
-constexpr uint32_t kTcBOff = kTcAOff + 128 * kTcKMax * 2;  // C^T: [64 dim rows][kTcKMax tokens] bf16
-constexpr uint32_t kTcSbo = (kTcKMax / 8) * 128;  // bytes between 8-row groups of an operand
+// The two MMA operands, MN-major with the 128-byte swizzle: a token's row of
+// the operand is a contiguous 64-element (128-byte) row of a swizzle atom
+// (8 token rows, 1024 bytes, 1024-byte aligned), 16-byte chunk c of row r
+// stored at chunk c ^ r.  C^T = (w x)^T (64 dim rows): one atom column, token
+// groups of 8 rows 1024 bytes apart.  A = B^T (128 dstate columns): two atom
+// columns 1024 bytes apart, token groups 2048 bytes apart.
+constexpr uint32_t kTcBOff = 4096;                       // C^T, 64 x kTcKMax bf16 (8 KiB)
+constexpr uint32_t kTcAOff = kTcBOff + 64 * kTcKMax * 2;  // A, 128 x kTcKMax bf16 (16 KiB)
+constexpr uint32_t kTcCGroup = 1024, kTcAGroup = 2048;    // bytes between token groups of 8 rows
+static_assert(kTcBarOff + 128 <= kTcBOff && kTcBOff % 1024 == 0 && kTcAOff % 1024 == 0, "operand alignment");
 constexpr uint32_t kTcAccCols = 64;               // one fp32 accumulator: 128 lanes x 64 columns
 constexpr uint32_t kTcTmemCols = 2 * kTcAccCols;  // two accumulators
-constexpr uint32_t kTcDescBase = round_up(kTcBOff + 64 * kTcKMax * 2, 128u);
+constexpr uint32_t kTcDescBase = round_up(kTcAOff + 128 * kTcKMax * 2, 128u);
 constexpr uint32_t kTcArenaBase = round_up(kTcDescBase + kMaxStages * kDescBytes, 128u);
 constexpr int kTcMinK = 1;  // every prefix of one token or more goes through the MMA
 

@@ -28,21 +28,24 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Shared-memory matrix descriptor: K-major operand without swizzling, made of
-// 8-row x 16-byte core matrices (each 128 contiguous bytes); `lbo` = bytes
-// between core matrices adjacent along K, `sbo` = bytes between adjacent
-// 8-row groups.  Bits 46-48 hold the descriptor version (0b001).
-__device__ __forceinline__ uint64_t smem_desc_kmajor(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory descriptor: MN-major operand with the 128-byte swizzle (atoms
+// of 8 K rows x 128 bytes along MN, 1024 bytes, 1024-byte aligned); `lbo` =
+// bytes between atoms adjacent along MN, `sbo` = bytes between atoms adjacent
+// along K (groups of 8 K rows).  Bits 46-48 hold the descriptor version
+// (0b001), bits 61-63 the layout type (2: 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo & 0x3FFFFu) >> 4) << 16) |
-         (static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46);
+         (static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor of kind::f16: bf16 A and B, fp32 accumulator, both
-// operands K-major, an M x N tile.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 accumulator, an
+// M x N tile; a_mn / b_mn: the operand is MN-major (else K-major).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool a_mn = false, bool b_mn = false) {
   return (1u << 4) |                                  // D format: fp32
          (1u << 7) |                                  // A format: bf16
          (1u << 10) |                                 // B format: bf16
+         (a_mn ? 1u << 15 : 0u) |                     // A major-ness
+         (b_mn ? 1u << 16 : 0u) |                     // B major-ness
          (static_cast<uint32_t>(n >> 3) << 17) |      // N / 8
          (static_cast<uint32_t>(m >> 4) << 24);       // M / 16
 }

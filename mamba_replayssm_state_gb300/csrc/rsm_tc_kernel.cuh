@@ -10,12 +10,14 @@
 // The seven consumer warps form two groups that work on consecutive items at
 // the same time:
 //   builder group (warps 1-3): decay weights of the item's tokens, the MMA
-//     operands in shared memory as bf16 K-major core matrices without swizzle
-//     (A = B^T: 128 x k_pad, from the bf16 ring rows exactly, rebuilt only for
-//     the first head of a B group; the second operand C^T: 64 x k_pad, w_t x_t
-//     rounded to bf16), then one thread issues ceil(k/16) tcgen05.mma
+//     operands in shared memory, MN-major with the 128-byte swizzle, so that
+//     a ring row is a row of the operand (A = B^T: 128 x k_pad, the bf16 ring
+//     rows of B copied exactly, rebuilt only for the first head of a B group;
+//     the second operand C^T: 64 x k_pad, w_t x_t rounded to bf16), 16 bytes
+//     a thread at a time, then one thread issues ceil(k/16) tcgen05.mma
 //     (K = 16) into one of two TMEM accumulators and commits them to that
-//     accumulator's mbarrier;
+//     accumulator's mbarrier.  (K-major operands had each 16-byte chunk
+//     gathered from 8 rows; that build was the kernel's critical path);
 //   epilogue group (warps 4-7): the item's S_0 column (one dstate column j per
 //     thread, all 64 dim rows) into registers, the slot released, then after
 //     the MMA the accumulator column read from TMEM lane j, P S_0 added,
@@ -116,7 +118,7 @@ __device__ __forceinline__ void run_builder_tc(const Params& p, unsigned char* s
   unsigned char* aop = smem + kTcAOff;
   unsigned char* bop = smem + kTcBOff;
   const int tid = bw * 32 + lane;  // over the builder group
-  constexpr uint32_t kIdesc = idesc_bf16_f32(128, 64);
+  constexpr uint32_t kIdesc = idesc_bf16_f32(128, 64, true, true);
 
   const uint32_t item_max = item_layout(D, N, ES, false, IE, p.W).bytes;
   uint32_t arena_head = 0;
@@ -155,36 +157,28 @@ __device__ __forceinline__ void run_builder_tc(const Params& p, unsigned char* s
       break;
     }
     const int kp = (k + 15) & ~15;  // K padded to whole MMAs; tokens k .. kp-1 are zero
-    const uint16_t* Brows = reinterpret_cast<const uint16_t*>(sb + il.off_B);
-    const uint16_t* xrows = reinterpret_cast<const uint16_t*>(sb + il.off_x);
-    if (!same_B) {  // A = B^T
-      for (int u = tid; u < 128 * (kp / 8); u += 32 * kTcBuilderWarps) {
-        const int jj = u & 127, tg = u >> 7;
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int t = 8 * tg + 2 * e;
-          const uint32_t lo = t < k ? Brows[t * N + jj] : 0u;
-          const uint32_t hi = t + 1 < k ? Brows[(t + 1) * N + jj] : 0u;
-          w[e] = lo | (hi << 16);
-        }
-        *reinterpret_cast<uint4*>(aop + (jj >> 3) * kTcSbo + tg * 128 + (jj & 7) * 16) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+    if (!same_B) {
+      // A = B^T: token t's 256-byte B row is row t % 8 of atom column c / 8 of
+      // token group t / 8; chunk c % 8 goes to chunk (c % 8) ^ (t % 8)
+      for (int u = tid; u < kp * 16; u += 32 * kTcBuilderWarps) {
+        const int t = u >> 4, c = u & 15;
+        const uint4 v = t < k ? *reinterpret_cast<const uint4*>(sb + il.off_B + t * (N * 2) + c * 16)
+                              : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(aop + (t >> 3) * kTcAGroup + (c >> 3) * 1024 + (t & 7) * 128 +
+                                  (((c & 7) ^ (t & 7)) << 4)) = v;
       }
     }
-    for (int u = tid; u < 64 * (kp / 8); u += 32 * kTcBuilderWarps) {  // C^T = (w x)^T
-      const int ii = u & 63, tg = u >> 6;
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int t = 8 * tg + 2 * e;
-        const float lo = t < k ? wbuf[t] * __uint_as_float(static_cast<uint32_t>(xrows[t * D + ii]) << 16) : 0.0f;
-        const float hi =
-            t + 1 < k ? wbuf[t + 1] * __uint_as_float(static_cast<uint32_t>(xrows[(t + 1) * D + ii]) << 16) : 0.0f;
-        w[e] = pack_bf16x2(lo, hi);
+    // C^T = (w x)^T: token t's 128-byte row w_t x_t, chunk c to chunk c ^ (t % 8)
+    for (int u = tid; u < kp * 8; u += 32 * kTcBuilderWarps) {
+      const int t = u >> 3, c = u & 7;
+      uint4 o = make_uint4(0u, 0u, 0u, 0u);
+      if (t < k) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(sb + il.off_x + t * (D * 2) + c * 16);
+        const float w = wbuf[t];
+        o = make_uint4(pack_bf16x2(bf16lo(xv.x) * w, bf16hi(xv.x) * w), pack_bf16x2(bf16lo(xv.y) * w, bf16hi(xv.y) * w),
+                       pack_bf16x2(bf16lo(xv.z) * w, bf16hi(xv.z) * w), pack_bf16x2(bf16lo(xv.w) * w, bf16hi(xv.w) * w));
       }
-      *reinterpret_cast<uint4*>(bop + (ii >> 3) * kTcSbo + tg * 128 + (ii & 7) * 16) =
-          make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(bop + (t >> 3) * kTcCGroup + (t & 7) * 128 + ((c ^ (t & 7)) << 4)) = o;
     }
     fence_proxy_async_smem();  // the operands, written by this thread, before the tensor cores read them
     // the group is done with the slot's x, B and dt
@@ -209,11 +203,13 @@ __device__ __forceinline__ void run_builder_tc(const Params& p, unsigned char* s
       }
       tc_fence_after();
       if (lane == 0) {
-        const uint64_t adesc0 = smem_desc_kmajor(sbase + kTcAOff, 128u, kTcSbo);
-        const uint64_t bdesc0 = smem_desc_kmajor(sbase + kTcBOff, 128u, kTcSbo);
-        for (int kc = 0; kc < kp / 16; ++kc)  // the start address field counts 16-byte units: +256 B per step
-          tc_mma_bf16(tmem + buf * kTcAccCols, adesc0 + static_cast<uint64_t>(16 * kc),
-                      bdesc0 + static_cast<uint64_t>(16 * kc), kIdesc, kc > 0 ? 1u : 0u);
+        const uint64_t adesc0 = smem_desc_mn_sw128(sbase + kTcAOff, 1024u, kTcAGroup);
+        const uint64_t bdesc0 = smem_desc_mn_sw128(sbase + kTcBOff, 1024u, kTcCGroup);
+        // one MMA per 16 tokens, i.e. per two token groups; the start address
+        // field counts 16-byte units
+        for (int kc = 0; kc < kp / 16; ++kc)
+          tc_mma_bf16(tmem + buf * kTcAccCols, adesc0 + static_cast<uint64_t>(kc * 2 * kTcAGroup / 16),
+                      bdesc0 + static_cast<uint64_t>(kc * 2 * kTcCGroup / 16), kIdesc, kc > 0 ? 1u : 0u);
         tc_commit(sbase + kTcMmaDone + 8u * buf);
       }
       __syncwarp();
@@ -374,6 +370,13 @@ __global__ void __launch_bounds__(kTcThreads, 2) materialize_tc_kernel(const __g
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTcTmemSlot);
+  // the swizzled operands need 1024-byte aligned atoms: a shared-memory base
+  // without that alignment (never seen) ends the CTA with a status bit
+  if ((sbase & 1023u) != 0u) {
+    if (threadIdx.x == 0) flag_status(p.status, RSM_STATUS_WAIT_TIMEOUT);
+    if (warp == 1) tmem_dealloc(tmem, kTcTmemCols);
+    return;
+  }
   if (warp == 0) {
     run_loader<SF, RSM_BF16, 64, 128>(p, smem, lane);
   } else {
