@@ -117,6 +117,26 @@ bool verbose() {
   return v;
 }
 
+// Whether two CTAs of `fn` (`threads` each, `smem` dynamic bytes) fit one SM by
+// registers (allocated per warp in 256-register units out of 64K), shared
+// memory (each CTA's static + dynamic + reserved bytes) and threads.
+cudaError_t tc_two_per_sm_fit(const void* fn, int threads, int smem, const DeviceInfo& di, int* fits) {
+  cudaFuncAttributes fa{};
+  const cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+  if (e != cudaSuccess) return e;
+  const int warps = (threads + 31) / 32;
+  const int regs_per_warp = (fa.numRegs * 32 + 255) / 256 * 256;
+  const bool regs_ok = 2 * warps * regs_per_warp <= 65536;
+  const bool smem_ok = 2 * (static_cast<int>(fa.sharedSizeBytes) + smem + di.smem_reserved) <= di.smem_per_sm;
+  const bool threads_ok = threads <= fa.maxThreadsPerBlock && 2 * threads <= 2048;
+  *fits = regs_ok && smem_ok && threads_ok;
+  if (verbose())
+    std::fprintf(stderr, "[replayssm] two tensor-core CTAs per SM: regs %d (%s), smem %d+%zu (%s)\n", fa.numRegs,
+                 regs_ok ? "fit" : "no", smem, fa.sharedSizeBytes, smem_ok ? "fit" : "no");
+  return cudaSuccess;
+}
+
+
 // Host-side validation; returns the instance index or a negative code.
 int validate(const rsm_materialize_args* a) {
   if (a == nullptr) return fail(RSM_EINVAL, "args is NULL");
@@ -253,16 +273,23 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
     } else {
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
       if (e != cudaSuccess) return fail(RSM_ECUDA, "occupancy query: %s", cudaGetErrorString(e));
+      if (verbose()) std::fprintf(stderr, "[replayssm] occupancy query: %d CTAs per SM\n", per_sm);
+      // The occupancy query reports one CTA per SM for the tensor-core kernel,
+      // while the hardware's own limits (ncu's occupancy section: shared
+      // memory 2, registers 2) let two run side by side, each holding 128 of
+      // the SM's 512 TMEM columns.  Two are planned only after checking those
+      // limits here; were the second not co-scheduled, the persistent grid
+      // would merely take a second wave.
+      if (use_tc && two && per_sm < 2) {
+        int fits = 0;
+        e = tc_two_per_sm_fit(fn, threads, smem, di, &fits);
+        if (e != cudaSuccess) return fail(RSM_ECUDA, "cudaFuncGetAttributes: %s", cudaGetErrorString(e));
+        if (fits) per_sm = 2;
+      }
       g_occ_smem[dev][ci] = smem;
       g_occ_blocks[dev][ci] = per_sm;
     }
   }
-  if (verbose()) std::fprintf(stderr, "[replayssm] occupancy query: %d CTAs per SM\n", per_sm);
-  // The occupancy query reports one CTA per SM for the tensor-core kernel
-  // although its shared memory, registers and threads fit two; on GB300 two
-  // run side by side (each allocates 128 of the SM's 512 TMEM columns).  Were
-  // they not co-scheduled, the persistent grid would only take a second wave.
-  if (use_tc && two && per_sm < 2) per_sm = 2;
   if (per_sm < 1) return fail(RSM_ENOTSUP, "kernel does not fit on an SM with %d bytes of shared memory", smem);
 
   rsm::Params& p = L->params;

@@ -101,26 +101,6 @@ __device__ __forceinline__ uint4 philox4x32(uint4 c, uint32_t k0, uint32_t k1, i
   return c;
 }
 
-// C independent counters through `rounds` rounds, side by side, in one loop
-// that is not unrolled (compact code; the C chains give the parallelism).
-template <int C>
-__device__ __forceinline__ void philox4x32_xc(uint4 (&c)[C], uint32_t k0, uint32_t k1, int rounds) {
-  constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
-  constexpr uint32_t kWeylA = 0x9E3779B9u, kWeylB = 0xBB67AE85u;
-#pragma unroll 1
-  for (int r = 0; r < rounds; ++r) {
-#pragma unroll
-    for (int q = 0; q < C; ++q) {
-      const uint64_t pA = static_cast<uint64_t>(kMulA) * c[q].x;
-      const uint64_t pB = static_cast<uint64_t>(kMulB) * c[q].z;
-      c[q] = make_uint4(static_cast<uint32_t>(pB >> 32) ^ c[q].y ^ k0, static_cast<uint32_t>(pB),
-                        static_cast<uint32_t>(pA >> 32) ^ c[q].w ^ k1, static_cast<uint32_t>(pA));
-    }
-    k0 += kWeylA;
-    k1 += kWeylB;
-  }
-}
-
 // ---------------------------------------------------------------------------
 // stochastic rounding of an fp32 value to a target grid
 // ---------------------------------------------------------------------------

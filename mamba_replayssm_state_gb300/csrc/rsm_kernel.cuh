@@ -623,10 +623,7 @@ __device__ __noinline__ RawPair<SF> sr_pack8x2(float2 a0, float2 a1, float2 a2, 
 // closed form (the tokens converted kTokChunk at a time into the warp's fp32
 // buffer `cbuf`), requantization and the store.  The slot is released (empty
 // barrier) as soon as the warp holds all it still needs.
-// kRowLoop: the tensor-core kernel inlines this path next to its own; there
-// the plain per-row store loop (rounding mode tested per row) measured faster
-// for its tensor-core items than the hoisted two-row form used here otherwise.
-template <int SF, int IF, int D, int N, bool kRowLoop = false>
+template <int SF, int IF, int D, int N>
 __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char* sb, const ItemLayout& il,
                                             const ItemDesc* desc, int k, float* wbuf, float* cbuf, int cw, int lane,
                                             uint32_t empty_bar, uint32_t key0, uint32_t key1, bool sr) {
@@ -808,74 +805,46 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
         for (int u = 0; u < V2; ++u) acc[r][u] = __fmul2_rn(acc[r][u], inv2);
       }
     }
-    if constexpr (!kRowLoop) {
-      auto store_row = [&](int r, Raw out) {
-        if constexpr (Q) {
-          if (zero_rows[r]) out = Raw{};
-        }
-        const uint32_t off = ((row0 + r) * N + col0) * ES;
-        if (dst_aligned)
-          stg_stream(dst_tile + off, out);
-        else
-          store_bytes(dst_tile + off, out);
-      };
-      bool use_sr = false;
-      if constexpr (SF != RSM_F32) use_sr = sr;
-      if (worker) {
-        if (use_sr) {
-          if constexpr (SF != RSM_F32) {
-            // Philox counter of element e: (e / 8, dst_slot, layer, 0); a row's
-            // 8 elements start on a multiple of 8, so they are one block
-            static_assert(V2 == 4, "stochastic rounding works on 8-element vectors");
-            const uint32_t blk0 = static_cast<uint32_t>(((static_cast<int64_t>(h) * D + row0) * N + col0) >> 3);
-            constexpr uint32_t kRowBlocks = N / 8;
-            if constexpr (RPT % 2 == 0) {
-#pragma unroll
-              for (int r = 0; r < RPT; r += 2) {
-                const RawPair<SF> o = sr_pack8x2<SF>(acc[r][0], acc[r][1], acc[r][2], acc[r][3], acc[r + 1][0],
-                                                     acc[r + 1][1], acc[r + 1][2], acc[r + 1][3], blk0 + r * kRowBlocks,
-                                                     blk0 + (r + 1) * kRowBlocks, dst_slot_id, layer_id, key0, key1,
-                                                     p.philox_rounds);
-                store_row(r, o.a);
-                store_row(r + 1, o.b);
-              }
-            } else {
-#pragma unroll
-              for (int r = 0; r < RPT; ++r)
-                store_row(r, sr_pack8<SF>(acc[r][0], acc[r][1], acc[r][2], acc[r][3], blk0 + r * kRowBlocks,
-                                          dst_slot_id, layer_id, key0, key1, p.philox_rounds));
-            }
-          }
-        } else {
-#pragma unroll
-          for (int r = 0; r < RPT; ++r) store_row(r, pack_vec_rne<SF>(acc[r]));
-        }
+    auto store_row = [&](int r, Raw out) {
+      if constexpr (Q) {
+        if (zero_rows[r]) out = Raw{};
       }
-    } else {
+      const uint32_t off = ((row0 + r) * N + col0) * ES;
+      if (dst_aligned)
+        stg_stream(dst_tile + off, out);
+      else
+        store_bytes(dst_tile + off, out);
+    };
+    bool use_sr = false;
+    if constexpr (SF != RSM_F32) use_sr = sr;
+    if (worker) {
+      if (use_sr) {
+        if constexpr (SF != RSM_F32) {
+          // Philox counter of element e: (e / 8, dst_slot, layer, 0); a row's
+          // 8 elements start on a multiple of 8, so they are one block
+          static_assert(V2 == 4, "stochastic rounding works on 8-element vectors");
+          const uint32_t blk0 = static_cast<uint32_t>(((static_cast<int64_t>(h) * D + row0) * N + col0) >> 3);
+          constexpr uint32_t kRowBlocks = N / 8;
+          if constexpr (RPT % 2 == 0) {
 #pragma unroll
-      for (int r = 0; r < RPT; ++r) {
-        if (!worker) continue;
-        Raw out;
-        bool use_sr = false;
-        if constexpr (SF != RSM_F32) use_sr = sr;
-        if (use_sr) {
-          if constexpr (SF != RSM_F32) {
-            static_assert(V2 == 4, "stochastic rounding works on 8-element vectors");
-            const int64_t e0 = (static_cast<int64_t>(h) * D + row0 + r) * N + col0;
-            out = sr_pack8<SF>(acc[r][0], acc[r][1], acc[r][2], acc[r][3], static_cast<uint32_t>(e0 >> 3), dst_slot_id,
-                               layer_id, key0, key1, p.philox_rounds);
+            for (int r = 0; r < RPT; r += 2) {
+              const RawPair<SF> o = sr_pack8x2<SF>(acc[r][0], acc[r][1], acc[r][2], acc[r][3], acc[r + 1][0],
+                                                   acc[r + 1][1], acc[r + 1][2], acc[r + 1][3], blk0 + r * kRowBlocks,
+                                                   blk0 + (r + 1) * kRowBlocks, dst_slot_id, layer_id, key0, key1,
+                                                   p.philox_rounds);
+              store_row(r, o.a);
+              store_row(r + 1, o.b);
+            }
+          } else {
+#pragma unroll
+            for (int r = 0; r < RPT; ++r)
+              store_row(r, sr_pack8<SF>(acc[r][0], acc[r][1], acc[r][2], acc[r][3], blk0 + r * kRowBlocks,
+                                        dst_slot_id, layer_id, key0, key1, p.philox_rounds));
           }
-        } else {
-          out = pack_vec_rne<SF>(acc[r]);
         }
-        if constexpr (Q) {
-          if (zero_rows[r]) out = Raw{};
-        }
-        const uint32_t off = ((row0 + r) * N + col0) * ES;
-        if (dst_aligned)
-          stg_stream(dst_tile + off, out);
-        else
-          store_bytes(dst_tile + off, out);
+      } else {
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) store_row(r, pack_vec_rne<SF>(acc[r]));
       }
     }
     if constexpr (Q) {
@@ -1035,8 +1004,8 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_kernel(const __grid_c
     run_consumer<SF, IF, D, N>(p, smem, warp - 1, lane);
 }
 
-// The one-byte kernel (rsm_q8_kernel.cuh).
-template <int SF, int IF, bool SR>
+// The one-byte kernel (rsm_q8_kernel.cuh), rounding to nearest.
+template <int SF, int IF>
 const void* q8_kernel();
 
 // Instantiation hook: each translation unit that includes this header (and,
@@ -1047,10 +1016,18 @@ template <int SF, int IF, int D, int N>
 const void* kernel_for() {
   if constexpr (Fmt<SF>::quant) {
     static_assert(D == 64 && N == 128, "one-byte state is 64 x 128");
-    return q8_kernel<SF, IF, false>();
+    return q8_kernel<SF, IF>();
   } else {
     return reinterpret_cast<const void*>(&materialize_kernel<SF, IF, D, N>);
   }
+}
+
+// One-byte state with stochastic rounding: this eight-warp kernel, whose two
+// CTAs per SM keep more Philox chains in flight than the four-warp one-byte kernel.
+template <int SF, int IF, int D, int N>
+const void* kernel_for_sr() {
+  static_assert(Fmt<SF>::quant && D == 64 && N == 128, "the stochastic-rounding instance is one-byte state");
+  return reinterpret_cast<const void*>(&materialize_kernel<SF, IF, D, N>);
 }
 
 }  // namespace rsm

@@ -16,81 +16,13 @@
 // 8 lc .. 8 lc + 7, so that the 16 lanes of a row group hold whole rows and a
 // row's amax is a warp reduction.
 //
-// Stochastic rounding is a separate kernel instance (template SR): its Philox
-// work is inline there, and the round-to-nearest instance carries none of it.
+// This kernel rounds to nearest even.  One-byte state with Philox stochastic
+// rounding runs on the eight-warp materialization kernel, whose two CTAs per
+// SM keep more Philox chains in flight (kernel_for_sr in rsm_kernel.cuh).
 #pragma once
 #include "rsm_kernel.cuh"
 
 namespace rsm {
-
-// fp8 e4m3 stochastic rounding of |y| >= 2^-6 (or y == 0) on the bit pattern:
-// adding the complement of the 16 random bits, scaled to the 20 discarded
-// bits, carries into the next grid point exactly when r * 2^4 < the discarded
-// bits (the rule of sr_round for a word r << 16); saturates at 448.
-__device__ __forceinline__ float sr_e4m3_normal(float y, uint32_t r16) {
-  const uint32_t bits = __float_as_uint(y);
-  const uint32_t sign = bits & 0x80000000u;
-  uint32_t r = ((bits ^ sign) + (((r16 ^ 0xFFFFu) << 4) | 0xFu)) & 0xFFF00000u;
-  r = min(r, 0x43E00000u);  // 448
-  return __uint_as_float(r | sign);
-}
-
-__device__ __forceinline__ bool e4m3_normal_or_zero(float y) {
-  const uint32_t ab = __float_as_uint(y) & 0x7FFFFFFFu;
-  return ab >= 0x3C800000u || ab == 0u;  // |y| >= 2^-6
-}
-
-// int8 stochastic rounding on the integer grid in fp32 arithmetic: lo =
-// trunc|y| and the fraction f are exact (|y| < 2^23), and the magnitude goes up
-// iff r < f * 2^16 (the rule of sr_round for a word r << 16); saturates at 127.
-__device__ __forceinline__ float sr_i8_grid(float y, uint32_t r16) {
-  const float a = fabsf(y);
-  const float lo = truncf(a);
-  const float f = (a - lo) * 65536.0f;
-  const float rf = __uint_as_float(0x4B000000u | r16) - 8388608.0f;  // r as fp32, exactly
-  const float r = fminf(lo + (rf < f ? 1.0f : 0.0f), 127.0f);
-  return copysignf(r, y);
-}
-
-// The general fp8 rule for a row vector holding a value below 2^-6 (rare):
-// out of line, so that the kernel's code stays small.
-struct Row8 {
-  float2 v[4];
-};
-static __device__ __noinline__ Row8 sr_e4m3_row8_general(float2 v0, float2 v1, float2 v2, float2 v3, uint32_t w0,
-                                                        uint32_t w1, uint32_t w2, uint32_t w3) {
-  Row8 o;
-  o.v[0] = make_float2(sr_e4m3(v0.x, sr_lo16(w0)), sr_e4m3(v0.y, sr_hi16(w0)));
-  o.v[1] = make_float2(sr_e4m3(v1.x, sr_lo16(w1)), sr_e4m3(v1.y, sr_hi16(w1)));
-  o.v[2] = make_float2(sr_e4m3(v2.x, sr_lo16(w2)), sr_e4m3(v2.y, sr_hi16(w2)));
-  o.v[3] = make_float2(sr_e4m3(v3.x, sr_lo16(w3)), sr_e4m3(v3.y, sr_hi16(w3)));
-  return o;
-}
-
-// Stochastic rounding of one row vector of 8 scaled values (its Philox block
-// gives 16 random bits per element) to the grid of SF, exactly on the grid.
-template <int SF>
-__device__ __forceinline__ void sr_row8(float2 (&v)[4], const uint4& rnd) {
-  const uint32_t w[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
-  if constexpr (SF == RSM_I8) {
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      v[u] = make_float2(sr_i8_grid(v[u].x, w[u] & 0xFFFFu), sr_i8_grid(v[u].y, w[u] >> 16));
-  } else {
-    bool normal = true;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) normal = normal && e4m3_normal_or_zero(v[u].x) && e4m3_normal_or_zero(v[u].y);
-    if (__all_sync(0xFFFFFFFFu, normal)) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        v[u] = make_float2(sr_e4m3_normal(v[u].x, w[u] & 0xFFFFu), sr_e4m3_normal(v[u].y, w[u] >> 16));
-    } else {  // a value below 2^-6 somewhere in the warp: the general rule (rare)
-      const Row8 o = sr_e4m3_row8_general(v[0], v[1], v[2], v[3], w[0], w[1], w[2], w[3]);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = o.v[u];
-    }
-  }
-}
 
 // 8 codes (fp32 values on the format's grid, or int8 values already holding
 // 1.5 * 2^23 + code) -> 8 bytes
@@ -121,45 +53,9 @@ __device__ __forceinline__ void store_row8(const float2 (&v)[4], float inv, unsi
     store_bytes(d, out);
 }
 
-// Stochastic rounding of this lane's 8 row vectors, kSrRows rows at a time so
-// that as many independent Philox chains (one block of 8 elements per row) run
-// side by side, in a compact round loop.
-constexpr int kSrRows = 2;
-template <int SF>
-__device__ __forceinline__ void requant_rows_sr(float2 (&acc)[8][4], float inv_own, int group0, uint32_t blk0,
-                                                uint32_t slot, uint32_t layer, uint32_t key0, uint32_t key1,
-                                                int rounds, unsigned char* dst_tile, int row0, int lc,
-                                                bool dst_aligned) {
-  constexpr int N = 128;
-#pragma unroll
-  for (int r0 = 0; r0 < 8; r0 += kSrRows) {
-    uint4 rnd[kSrRows];
-#pragma unroll
-    for (int q = 0; q < kSrRows; ++q) rnd[q] = make_uint4(blk0 + (r0 + q) * (N / 8), slot, layer, 0u);
-    philox4x32_xc<kSrRows>(rnd, key0, key1, rounds);
-#pragma unroll
-    for (int q = 0; q < kSrRows; ++q) {
-      const int r = r0 + q;
-      const float inv = __shfl_sync(0xFFFFFFFFu, inv_own, group0 + 2 * r);
-      const float2 inv2 = make_float2(inv, inv);
-      float2 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = __fmul2_rn(acc[r][u], inv2);
-      sr_row8<SF>(v, rnd[q]);
-      if constexpr (SF == RSM_I8) {
-        const float2 magic = make_float2(12582912.0f, 12582912.0f);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = __fadd2_rn(v[u], magic);
-      }
-      store_row8<SF>(v, inv, dst_tile + (row0 + r) * N + 8 * lc, dst_aligned);
-    }
-  }
-}
-
-template <int SF, int IF, bool SR>
-__device__ __forceinline__ void replay_q8(const Params& p, const unsigned char* sb, const ItemLayout& il,
-                                          const ItemDesc* desc, int k, float* wbuf, float* cbuf, int cw, int lane,
-                                          uint32_t empty_bar, uint32_t key0, uint32_t key1) {
+template <int SF, int IF>
+__device__ __forceinline__ void replay_q8(const unsigned char* sb, const ItemLayout& il, const ItemDesc* desc, int k,
+                                          float* wbuf, float* cbuf, int cw, int lane, uint32_t empty_bar) {
   constexpr int D = 64, N = 128, IE = In<IF>::bytes;
   constexpr int RPT = 8;            // rows per lane
   constexpr int SLAB = 16;          // rows per warp
@@ -172,11 +68,6 @@ __device__ __forceinline__ void replay_q8(const Params& p, const unsigned char* 
   unsigned char* dst_tile = reinterpret_cast<unsigned char*>(desc->dst_state);
   float* dst_sc = reinterpret_cast<float*>(desc->dst_scale);
   const bool dst_aligned = (flags & kFlagDstAligned) != 0u;
-  // everything else the item needs from its descriptor, read before the slot is released
-  const uint32_t dst_slot_id = static_cast<uint32_t>(desc->dst_slot);
-  const uint32_t layer_id = static_cast<uint32_t>(desc->layer);
-  // Philox block of this lane's first row vector: element (h * D + row) * N + 8 lc, over 8
-  const uint32_t blk0 = static_cast<uint32_t>((static_cast<int64_t>(desc->head) * D + row0) * (N / 8) + lc);
 
   const float P = decay_scan(reinterpret_cast<const float*>(sb + il.off_dt), desc->A, k, lane, wbuf);
 
@@ -280,27 +171,22 @@ __device__ __forceinline__ void replay_q8(const Params& p, const unsigned char* 
   const float scale_own = inv_own <= FLT_MAX ? __fdiv_rn(am, qmax) : 0.0f;
 
   const int group0 = lane & 16;
-  if constexpr (SR) {
-    requant_rows_sr<SF>(acc, inv_own, group0, blk0, dst_slot_id, layer_id, key0, key1, p.philox_rounds, dst_tile,
-                        row0, lc, dst_aligned);
-  } else {
 #pragma unroll
-    for (int r = 0; r < RPT; ++r) {
-      const float inv = __shfl_sync(0xFFFFFFFFu, inv_own, group0 + 2 * r);
-      const float2 inv2 = make_float2(inv, inv);
-      float2 v[4];
-      if constexpr (SF == RSM_I8) {
-        // round to nearest even in one step: fl(v * inv + 1.5 * 2^23) keeps the
-        // exact product's rounding to an integer in its low byte (|v * inv| <= 127.5)
-        const float2 magic = make_float2(12582912.0f, 12582912.0f);
+  for (int r = 0; r < RPT; ++r) {
+    const float inv = __shfl_sync(0xFFFFFFFFu, inv_own, group0 + 2 * r);
+    const float2 inv2 = make_float2(inv, inv);
+    float2 v[4];
+    if constexpr (SF == RSM_I8) {
+      // round to nearest even in one step: fl(v * inv + 1.5 * 2^23) keeps the
+      // exact product's rounding to an integer in its low byte (|v * inv| <= 127.5)
+      const float2 magic = make_float2(12582912.0f, 12582912.0f);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = __ffma2_rn(acc[r][u], inv2, magic);
-      } else {
+      for (int u = 0; u < 4; ++u) v[u] = __ffma2_rn(acc[r][u], inv2, magic);
+    } else {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = __fmul2_rn(acc[r][u], inv2);
-      }
-      store_row8<SF>(v, inv, dst_tile + (row0 + r) * N + 8 * lc, dst_aligned);
+      for (int u = 0; u < 4; ++u) v[u] = __fmul2_rn(acc[r][u], inv2);
     }
+    store_row8<SF>(v, inv, dst_tile + (row0 + r) * N + 8 * lc, dst_aligned);
   }
   if ((lc & 1) == 0) {
     const int srow = row0 + (lc >> 1);
@@ -314,7 +200,7 @@ __device__ __forceinline__ void replay_q8(const Params& p, const unsigned char* 
   }
 }
 
-template <int SF, int IF, bool SR>
+template <int SF, int IF>
 __device__ __forceinline__ void run_consumer_q8(const Params& p, unsigned char* smem, int cw, int lane) {
   constexpr int D = 64, N = 128, IE = In<IF>::bytes;
   const uint32_t full0 = smem_addr(smem);
@@ -324,12 +210,6 @@ __device__ __forceinline__ void run_consumer_q8(const Params& p, unsigned char* 
   float* cbuf = reinterpret_cast<float*>(smem + kWarpBufOff) + cw * warp_buf_floats(D, N, 1, kQ8ConsumerWarps);
   const int tid = cw * 32 + lane;  // 0 .. 127
 
-  uint32_t key0 = 0, key1 = 0;
-  if constexpr (SR) {
-    const uint64_t s = static_cast<uint64_t>(__ldg(p.rand_seed));
-    key0 = static_cast<uint32_t>(s);
-    key1 = static_cast<uint32_t>(s >> 32);
-  }
   const uint32_t item_max = item_layout(D, N, 1, true, IE, p.W).bytes;
   uint32_t arena_head = 0;
   uint32_t stage = 0, phase = 0;
@@ -380,7 +260,7 @@ __device__ __forceinline__ void run_consumer_q8(const Params& p, unsigned char* 
         }
       }
     } else {
-      replay_q8<SF, IF, SR>(p, sb, il, desc, k, wbuf, cbuf, cw, lane, empty_bar, key0, key1);
+      replay_q8<SF, IF>(sb, il, desc, k, wbuf, cbuf, cw, lane, empty_bar);
     }
     if (++stage == p.stages) {
       stage = 0;
@@ -389,7 +269,7 @@ __device__ __forceinline__ void run_consumer_q8(const Params& p, unsigned char* 
   }
 }
 
-template <int SF, int IF, bool SR>
+template <int SF, int IF>
 __global__ void __maxnreg__(kQ8MaxRegs) materialize_q8_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   // empty active list: one load, then out
@@ -409,20 +289,12 @@ __global__ void __maxnreg__(kQ8MaxRegs) materialize_q8_kernel(const __grid_const
   if (warp == 0)
     run_loader<SF, IF, 64, 128>(p, smem, lane);
   else
-    run_consumer_q8<SF, IF, SR>(p, smem, warp - 1, lane);
+    run_consumer_q8<SF, IF>(p, smem, warp - 1, lane);
 }
 
-template <int SF, int IF, bool SR>
+template <int SF, int IF>
 const void* q8_kernel() {
-  return reinterpret_cast<const void*>(&materialize_q8_kernel<SF, IF, SR>);
-}
-
-// One-byte state with stochastic rounding: the eight-warp kernel, whose two
-// CTAs per SM keep more Philox chains in flight than the four-warp one.
-template <int SF, int IF, int D, int N>
-const void* kernel_for_sr() {
-  static_assert(Fmt<SF>::quant && D == 64 && N == 128, "the stochastic-rounding instance is one-byte state");
-  return reinterpret_cast<const void*>(&materialize_kernel<SF, IF, D, N>);
+  return reinterpret_cast<const void*>(&materialize_q8_kernel<SF, IF>);
 }
 
 }  // namespace rsm

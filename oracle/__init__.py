@@ -184,8 +184,8 @@ def philox4x32(ctr, key, rounds=10):
     return tuple(o)
 
 
-def round_to(fmt, y, stochastic=False, word=0):
-    return lib().oracle_round(DTYPE_CODES.get(fmt, fmt), float(y), int(stochastic), int(word) & 0xFFFFFFFF)
+def round_to(fmt, y, stochastic=False, r16=0):
+    return lib().oracle_round(DTYPE_CODES.get(fmt, fmt), float(y), int(stochastic), int(r16) & 0xFFFF)
 
 
 def decode(fmt, bits):

@@ -36,10 +36,18 @@
  *    qmax/amax is not finite (amax == 0, or so small that the scale cannot
  *    be inverted in fp32) is stored as zero codes with scale 0;
  *  - stochastic rounding: Philox-4x32 with philox_rounds rounds,
- *    key = (lo32(seed), hi32(seed)), counter = (e>>3, dst_slot, layer, 0) with
- *    e = (h*dim + i)*dstate + j; element e takes the 16-bit half e&1 (low half
- *    first) of output word (e>>1)&3 as r; round the magnitude up iff
- *    r * 2^16 * ulp < (|y| - lo) * 2^32, then saturate.
+ *    key = (lo32(seed), hi32(seed)); element e = (h*dim + i)*dstate + j gets
+ *    a 16-bit random number r16, and its magnitude goes up to the next grid
+ *    point iff floor((|y| - lo)/ulp * 2^16) + r16 >= 2^16 (the top 16 bits of
+ *    the discarded part plus r16 carry), then saturates to the largest finite
+ *    value.  The bits are assigned as the sm_100-family conversion with
+ *    stochastic rounding (PTX cvt.rs) consumes one 32-bit word:
+ *      16-bit state: counter (e>>3, dst_slot, layer, 0), word w = out[(e>>1)&3],
+ *        half c = low (e even) or high (e odd) 16 bits of w; bf16 r16 = c,
+ *        f16 r16 = (c << 3) mod 2^16 (13 random bits for 13 discarded bits);
+ *      one-byte state: counter (e>>4, dst_slot, layer, 0), w = out[(e>>2)&3],
+ *        c = low (e&3 < 2) or high half of w, r16 = c for e&3 even and c with
+ *        its 16 bits reversed for e&3 odd (two elements per half).
  */
 #include "replayssm_oracle.h"
 
@@ -142,7 +150,7 @@ static double grid_ulp(const grid_t *g, double a) {
   return ldexp(1.0, E - g->mant);
 }
 
-double oracle_round(int fmt, double y, int stochastic, uint32_t word) {
+double oracle_round(int fmt, double y, int stochastic, uint32_t r16) {
   grid_t g;
   if (grid_of(fmt, &g) != 0) return NAN;
   if (isnan(y)) return y;
@@ -161,9 +169,11 @@ double oracle_round(int fmt, double y, int stochastic, uint32_t word) {
     else /* tie: keep the neighbour whose last grid digit is even */
       r = (fmod(lo / ulp, 2.0) == 0.0) ? lo : hi;
   } else {
-    /* up with probability (a-lo)/ulp: u = word/2^32 < (a-lo)/ulp, compared
-     * exactly (both products are exact in fp64) */
-    r = ((double)word * ulp < (a - lo) * 4294967296.0) ? hi : lo;
+    /* up with probability floor((a-lo)/ulp * 2^16) / 2^16: the top 16 bits of
+     * the discarded part (exact in fp64: a power-of-two scaling and a floor)
+     * plus the random number carry past 2^16 */
+    const double d16 = floor((a - lo) / ulp * 65536.0);
+    r = (d16 + (double)(r16 & 0xFFFFu) >= 65536.0) ? hi : lo;
   }
   if (r > g.maxfin) r = (g.inf_on_overflow && !stochastic) ? INFINITY : g.maxfin;
   return copysign(r, y);
@@ -237,18 +247,32 @@ void oracle_philox4x32(const uint32_t ctr[4], const uint32_t key[2], int rounds,
   out[3] = c3;
 }
 
-/* The stochastic-rounding word of element e of (layer, dst slot): its 16
- * random bits r in the upper half of a 32-bit word (r * 2^16), so that the
- * rounding rule of oracle_round applies to it unchanged. */
-static uint32_t sr_word(const oracle_args *a, int layer, int32_t dst, int64_t e) {
+static uint32_t reverse16(uint32_t c) {
+  uint32_t r = 0;
+  for (int i = 0; i < 16; ++i)
+    if (c & (1u << i)) r |= 1u << (15 - i);
+  return r;
+}
+
+/* The 16-bit random number of element e of (layer, dst slot) in format fmt
+ * (the assignment stated at the top of this file). */
+static uint32_t sr_bits(const oracle_args *a, int fmt, int layer, int32_t dst, int64_t e) {
   int64_t seed = *a->rand_seed;
   uint32_t key[2] = {(uint32_t)((uint64_t)seed & 0xFFFFFFFFu),
                      (uint32_t)((uint64_t)seed >> 32)};
-  uint32_t ctr[4] = {(uint32_t)(e >> 3), (uint32_t)dst, (uint32_t)layer, 0u};
   uint32_t out[4];
+  if (fmt == ORACLE_I8 || fmt == ORACLE_FP8_E4M3) {
+    uint32_t ctr[4] = {(uint32_t)(e >> 4), (uint32_t)dst, (uint32_t)layer, 0u};
+    oracle_philox4x32(ctr, key, a->philox_rounds, out);
+    uint32_t w = out[(e >> 2) & 3];
+    uint32_t c = (e & 3) < 2 ? (w & 0xFFFFu) : (w >> 16);
+    return (e & 1) ? reverse16(c) : c;
+  }
+  uint32_t ctr[4] = {(uint32_t)(e >> 3), (uint32_t)dst, (uint32_t)layer, 0u};
   oracle_philox4x32(ctr, key, a->philox_rounds, out);
-  uint32_t r = (e & 1) ? (out[(e >> 1) & 3] >> 16) : (out[(e >> 1) & 3] & 0xFFFFu);
-  return r << 16;
+  uint32_t w = out[(e >> 1) & 3];
+  uint32_t c = (e & 1) ? (w >> 16) : (w & 0xFFFFu);
+  return fmt == ORACLE_F16 ? ((c << 3) & 0xFFFFu) : c;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -390,7 +414,7 @@ static void write_head(const oracle_args *a, int layer, int32_t dst, int64_t h,
     } else if (fmt == ORACLE_BF16 || fmt == ORACLE_F16) {
       for (int j = 0; j < N; ++j) {
         float y = (float)S[i * N + j];
-        uint32_t w = sr ? sr_word(a, layer, dst, row + j) : 0u;
+        uint32_t w = sr ? sr_bits(a, fmt, layer, dst, row + j) : 0u;
         store_bits(dst_state, row + j, fmt, oracle_encode(fmt, oracle_round(fmt, y, sr, w)));
       }
     } else { /* one-byte state: symmetric, one scale per (head, dim-row) */
@@ -409,7 +433,7 @@ static void write_head(const oracle_args *a, int layer, int32_t dst, int64_t h,
       for (int j = 0; j < N; ++j) {
         float v = (float)S[i * N + j];
         float y = v / scale; /* the code in units of the scale, one fp32 division */
-        uint32_t w = sr ? sr_word(a, layer, dst, row + j) : 0u;
+        uint32_t w = sr ? sr_bits(a, fmt, layer, dst, row + j) : 0u;
         store_bits(dst_state, row + j, fmt, oracle_encode(fmt, oracle_round(fmt, y, sr, w)));
       }
       dst_scale[h * D + i] = scale;

@@ -70,8 +70,10 @@ const char *oracle_last_error(void);
 void oracle_philox4x32(const uint32_t ctr[4], const uint32_t key[2], int rounds,
                        uint32_t out[4]);
 /* Round y to the grid of `fmt` (ORACLE_BF16/F16/I8/FP8_E4M3): round to nearest
- * even when stochastic == 0, else stochastic rounding driven by `word`. */
-double oracle_round(int fmt, double y, int stochastic, uint32_t word);
+ * even when stochastic == 0, else stochastic rounding driven by the element's
+ * 16-bit random number r16 (the magnitude goes up iff the top 16 bits of its
+ * discarded part plus r16 carry past 2^16). */
+double oracle_round(int fmt, double y, int stochastic, uint32_t r16);
 /* Storage <-> value for one element of each state format. */
 double oracle_decode(int fmt, uint32_t bits);
 uint32_t oracle_encode(int fmt, double value_on_grid);

@@ -553,31 +553,46 @@ def test_saturation():
 
 
 def test_stochastic_rounding_exact_cases():
-    # y = 2.25 on the integer grid: up iff word < 0.25 * 2^32
-    assert oracle.round_to("i8", 2.25, True, 0) == 3.0
-    assert oracle.round_to("i8", 2.25, True, (1 << 30) - 1) == 3.0
-    assert oracle.round_to("i8", 2.25, True, 1 << 30) == 2.0
-    assert oracle.round_to("i8", -2.25, True, 0) == -3.0
+    # y = 2.25 on the integer grid: the top 16 discarded bits are 0.25 * 2^16 =
+    # 16384, so the magnitude goes up iff r16 >= 65536 - 16384
+    assert oracle.round_to("i8", 2.25, True, 0) == 2.0
+    assert oracle.round_to("i8", 2.25, True, 49151) == 2.0
+    assert oracle.round_to("i8", 2.25, True, 49152) == 3.0
+    assert oracle.round_to("i8", 2.25, True, 65535) == 3.0
+    assert oracle.round_to("i8", -2.25, True, 65535) == -3.0
     # representable values never move
-    for w in (0, 12345, 0xFFFFFFFF):
-        assert oracle.round_to("fp8_e4m3", 1.125, True, w) == 1.125
-        assert oracle.round_to("bf16", 1.0, True, w) == 1.0
-    # bf16 between 1 and 1+2^-7: fraction 0.75
+    for r in (0, 12345, 65535):
+        assert oracle.round_to("fp8_e4m3", 1.125, True, r) == 1.125
+        assert oracle.round_to("bf16", 1.0, True, r) == 1.0
+    # bf16 between 1 and 1+2^-7: fraction 0.75, so up iff r16 >= 16384
     y = 1.0 + 0.75 * 2.0 ** -7
-    assert oracle.round_to("bf16", y, True, int(0.75 * 2 ** 32) - 1) == 1.0 + 2.0 ** -7
-    assert oracle.round_to("bf16", y, True, int(0.75 * 2 ** 32)) == 1.0
+    assert oracle.round_to("bf16", y, True, 16383) == 1.0
+    assert oracle.round_to("bf16", y, True, 16384) == 1.0 + 2.0 ** -7
+    # only the top 16 discarded bits count: fp8 e4m3 at 1 + 2^-20 discards
+    # 2^-17 of a step, whose top 16 bits are zero, so no r16 moves it
+    assert oracle.round_to("fp8_e4m3", 1.0 + 2.0 ** -20, True, 65535) == 1.0
+    # ... while 2^-16 of a step (1 + 2^-19) goes up with r16 = 65535 alone
+    assert oracle.round_to("fp8_e4m3", 1.0 + 2.0 ** -19, True, 65535) == 1.125
+    assert oracle.round_to("fp8_e4m3", 1.0 + 2.0 ** -19, True, 65534) == 1.0
+    # f16 (r16 carries the 13 random bits in its top 13): half a step
+    y = 1.0 + 0.5 * 2.0 ** -10
+    assert oracle.round_to("f16", y, True, 0x8000) == 1.0 + 2.0 ** -10
+    assert oracle.round_to("f16", y, True, 0x7FF8) == 1.0
 
 
 @pytest.mark.parametrize("fmt,y", [("fp8_e4m3", 0.3), ("fp8_e4m3", -13.7), ("fp8_e4m3", 0.0041),
                                    ("i8", 5.3), ("bf16", 0.123456), ("f16", 3.14159)])
 def test_stochastic_rounding_is_unbiased(fmt, y):
     rng = np.random.default_rng(1)
-    words = rng.integers(0, 2 ** 32, size=20000, dtype=np.uint64)
-    vals = np.array([oracle.round_to(fmt, y, True, int(w)) for w in words])
+    r16 = rng.integers(0, 2 ** 16, size=20000, dtype=np.uint64)
+    if fmt == "f16":
+        r16 = (r16 << 3) & 0xFFFF      # 13 random bits, as the f16 assignment gives them
+    vals = np.array([oracle.round_to(fmt, y, True, int(r)) for r in r16])
     lo, hi = np.min(vals), np.max(vals)
     assert set(np.unique(vals)) <= {lo, hi}
+    # truncating the discarded part to 16 bits biases by under 2^-16 of a step
     sigma = (hi - lo) / 2 / np.sqrt(len(vals))
-    assert abs(vals.mean() - np.float32(y)) <= 4 * sigma + 1e-12
+    assert abs(vals.mean() - np.float32(y)) <= 4 * sigma + (hi - lo) * 2.0 ** -16
 
 
 # ----------------------------------------------------------------------------
@@ -608,14 +623,19 @@ def test_one_request_copy_draws_the_calls_philox_words(sd):
         assert plain.state[0][1].tobytes() != full.state[l][dst].tobytes()
 
 
-# The counter layout of stochastic rounding is this library's own convention
-# (API page, Parameters: rand_seed, philox_rounds): Philox-4x32 with
-# philox_rounds rounds, key = (lo32(seed), hi32(seed)), counter =
-# (e >> 3, dst_slot, layer, 0) with e = (h*dim + i)*dstate + j, and element e
-# takes 16 random bits: the low (e even) or high (e odd) half of output word
-# (e >> 1) & 3.  The pins below predict every stored byte of a call from that
-# statement, the known-answer-pinned Philox and the bit-level rounding rule,
-# without the oracle's materialization code.
+# The assignment of random bits in stochastic rounding is this library's own
+# convention (API page, Parameters: rand_seed, philox_rounds fix Philox-4x32
+# and its rounds only): key = (lo32(seed), hi32(seed)); e = (h*dim + i)*dstate + j;
+#   16-bit state: counter (e >> 3, dst_slot, layer, 0), the low (e even) or
+#     high (e odd) half c of output word (e >> 1) & 3; bf16 r16 = c, f16
+#     r16 = (c << 3) mod 2^16;
+#   one-byte state: counter (e >> 4, dst_slot, layer, 0), the low (e & 3 < 2)
+#     or high half c of output word (e >> 2) & 3; r16 = c for e & 3 even, c
+#     bit-reversed for e & 3 odd;
+# and the magnitude goes up iff the top 16 discarded bits plus r16 carry past
+# 2^16.  The pins below predict every stored byte of a call from that
+# statement, the known-answer-pinned Philox and the bit-level rule, without
+# the oracle's materialization code; each planted mistake moves many bytes.
 
 SR_SEED = 0x0123_4567_89AB_CDEF   # hi32 != lo32, so a dropped or swapped key word shows
 
@@ -641,11 +661,14 @@ def _sr_world(sd):
 def _exact_f32_result(w, l):
     """fp32 rounding of S_1 = S_0 + dt x B^T for (layer l, its one request), [H, D, N]."""
     src = int(w.src_slots[l, 0])
-    if w.state_dtype == "bf16":
+    if w.state_dtype in ("bf16", "f16"):
         S0 = decode_state(w, l, src)
     else:  # one-byte: code * scale as an fp32 product
-        import torch
-        codes = torch.from_numpy(w.state[l][src].copy()).view(torch.float8_e4m3fn).float().numpy()
+        if w.state_dtype == "i8":
+            codes = w.state[l][src].view(np.int8).astype(np.float32)
+        else:
+            import torch
+            codes = torch.from_numpy(w.state[l][src].copy()).view(torch.float8_e4m3fn).float().numpy()
         S0 = (codes * w.scale[l][src][..., None]).astype(np.float32).astype(np.float64)
     x = decode_input(w, w.x[l][src, 2])            # [H, D]
     B = decode_input(w, w.B[l][src, 2])            # [G, N], G = H here
@@ -653,14 +676,20 @@ def _exact_f32_result(w, l):
     return S1.astype(np.float32)
 
 
-def _words(w, l, layout="reading"):
-    """The 16 random bits of every element of (layer l, dst slot), [H*D*N],
-    from the written layout (or from one of the planted wrong ones)."""
+def _rev16(c):
+    return int(f"{int(c):016b}"[::-1], 2)
+
+
+def _r16(w, l, layout="reading"):
+    """The 16-bit random number of every element of (layer l, dst slot), [H*D*N],
+    from the written assignment (or from one of the planted wrong ones)."""
     H, D, N = w.H, w.D, w.N
     dst = int(w.dst_slots[l, 0])
     lo, hi = SR_SEED & 0xFFFFFFFF, SR_SEED >> 32
+    one_byte = w.state_dtype in ("i8", "fp8_e4m3")
+    per_call = 16 if one_byte and layout != "eight_per_call" else 8
     out = np.zeros(H * D * N, np.uint64)
-    for blk in range(H * D * N // 8):
+    for blk in range(H * D * N // per_call):
         ctr, key = (blk, dst, l, 0), (lo, hi)
         if layout == "swap_counter_words":
             ctr = (dst, blk, l, 0)
@@ -669,33 +698,55 @@ def _words(w, l, layout="reading"):
         elif layout == "hi32_dropped":
             key = (lo, 0)
         r = oracle.philox4x32(ctr, key, 10)
-        for q in range(8):
-            word, half = r[q >> 1], q & 1
+        for q in range(per_call):
+            if per_call == 16:
+                wi, half, rev = q >> 2, (q & 3) >> 1, q & 1
+            else:
+                wi, half, rev = q >> 1, q & 1, 0
             if layout == "word_shifted":
-                word = r[((q >> 1) + 1) % 4]
+                wi = (wi + 1) % 4
             elif layout == "halves_swapped":
                 half ^= 1
-            out[8 * blk + q] = (word >> 16) if half else (word & 0xFFFF)
+            elif layout == "not_reversed":
+                rev = 0
+            c = (r[wi] >> 16) if half else (r[wi] & 0xFFFF)
+            v = _rev16(c) if rev else c
+            if w.state_dtype == "f16" and layout != "sixteen_bits":
+                v = (v << 3) & 0xFFFF
+            out[per_call * blk + q] = v
     return out
 
 
-def _predict_bf16(y32, r16):
-    """Stochastic rounding to bf16 on the bit pattern: up iff the 16 random bits
-    are below the 16 discarded bits."""
+def _up(d16, r16, rule):
+    """The rounding decision: the carry of d16 + r16 (or a planted wrong rule:
+    r16 compared with the discarded bits, without the carry)."""
+    return (d16 + r16 >= 65536) if rule == "carry" else (r16 < d16)
+
+
+def _predict_16bit(y32, r16, sd, rule="carry"):
+    """Stochastic rounding to bf16 (16 discarded bits) or f16 (13 discarded bits,
+    normal range 2^-14 <= |y| < 65504) on the bit pattern; returns the stored
+    16-bit words and where the prediction applies."""
     bits = y32.reshape(-1).view(np.uint32).astype(np.uint64)
     sign, mag = bits >> 31, bits & 0x7FFFFFFF
-    up = r16 < (mag & 0xFFFF)
-    return (((mag >> 16) + up.astype(np.uint64)) | (sign << 15)).astype(np.uint16)
+    if sd == "bf16":
+        up = _up(mag & 0xFFFF, r16, rule)
+        return (((mag >> 16) + up.astype(np.uint64)) | (sign << 15)).astype(np.uint16), np.ones(len(bits), bool)
+    up = _up((mag & 0x1FFF) << 3, r16, rule)
+    r = (((mag >> 13) + up.astype(np.uint64)) << 13).astype(np.uint32).view(np.float32)
+    r = r * np.where(sign == 1, -1, 1).astype(np.float32)
+    a = np.abs(y32.reshape(-1))
+    return r.astype(np.float16).view(np.uint16), (a >= 2.0 ** -14) & (a < 65504.0)
 
 
-def _predict_e4m3(q32, r16):
-    """Stochastic rounding to fp8 e4m3fn where |q| >= 2^-6 (normal grid: up iff
-    r * 2^4, the random fraction in units of the 20 discarded bits, is below
-    them), saturated at 448; not predicted below 2^-6 (the subnormal grid)."""
+def _predict_e4m3(q32, r16, rule="carry"):
+    """Stochastic rounding to fp8 e4m3fn where |q| >= 2^-6 (normal grid: the top
+    16 of the 20 discarded bits plus r16 carry), saturated at 448; not
+    predicted below 2^-6 (the subnormal grid)."""
     import torch
     bits = q32.reshape(-1).view(np.uint32).astype(np.uint64)
     sign, mag = bits >> 31, bits & 0x7FFFFFFF
-    up = (r16 << 4) < (mag & 0xFFFFF)
+    up = _up((mag & 0xFFFFF) >> 4, r16, rule)
     r = (((mag >> 20) + up.astype(np.uint64)) << 20).astype(np.uint32).view(np.float32)
     r = np.minimum(r, np.float32(448.0)) * np.where(sign == 1, -1, 1).astype(np.float32)
     codes = torch.from_numpy(r.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
@@ -703,21 +754,31 @@ def _predict_e4m3(q32, r16):
     return codes, normal
 
 
-def test_philox_counter_layout_predicts_every_bf16_byte():
-    w = _sr_world("bf16")
+PLANTED_16 = ("swap_counter_words", "slot_and_layer_swapped", "hi32_dropped", "word_shifted", "halves_swapped")
+
+
+@pytest.mark.parametrize("sd", ["bf16", "f16"])
+def test_random_bits_predict_every_16bit_element(sd):
+    w = _sr_world(sd)
     out = run(w)
+    predicted = 0
     for l in range(w.L):
         dst = int(w.dst_slots[l, 0])
         y32 = _exact_f32_result(w, l)
-        got = out.state[l][dst].reshape(-1)
-        assert np.array_equal(_predict_bf16(y32, _words(w, l)), got), f"layer {l}"
-        # each planted mistake in the layout moves a good share of the bytes
-        for bad in ("swap_counter_words", "slot_and_layer_swapped", "hi32_dropped", "word_shifted", "halves_swapped"):
-            wrong = _predict_bf16(y32, _words(w, l, bad))
-            assert (wrong != got).mean() > 0.2, (l, bad)
+        got = out.state[l][dst].reshape(-1).view(np.uint16)
+        want, where = _predict_16bit(y32, _r16(w, l), sd)
+        assert np.array_equal(want[where], got[where]), f"layer {l}"
+        predicted += int(where.sum())
+        planted = PLANTED_16 + (("sixteen_bits",) if sd == "f16" else ())
+        for bad in planted:
+            wrong, _ = _predict_16bit(y32, _r16(w, l, bad), sd)
+            assert (wrong[where] != got[where]).mean() > 0.2, (l, bad)
+        wrong, _ = _predict_16bit(y32, _r16(w, l), sd, rule="compare")
+        assert (wrong[where] != got[where]).mean() > 0.2, (l, "compare")
+    assert predicted >= 0.95 * w.L * w.H * w.D * w.N
 
 
-def test_philox_counter_layout_predicts_every_fp8_byte():
+def test_random_bits_predict_every_fp8_byte():
     w = _sr_world("fp8_e4m3")
     out = run(w)
     predicted = 0
@@ -728,14 +789,45 @@ def test_philox_counter_layout_predicts_every_fp8_byte():
         scale = (amax / np.float32(448.0)).astype(np.float32)   # fp32 division
         assert out.scale[l][dst].tobytes() == scale.tobytes(), f"layer {l}: scales"
         q32 = (y32 / scale[..., None]).astype(np.float32)       # the plain fp32 quotient
-        codes, normal = _predict_e4m3(q32, _words(w, l))
+        codes, normal = _predict_e4m3(q32, _r16(w, l))
         got = out.state[l][dst].reshape(-1)
         assert np.array_equal(codes[normal], got[normal]), f"layer {l}"
         predicted += int(normal.sum())
-        for bad in ("swap_counter_words", "slot_and_layer_swapped", "hi32_dropped", "word_shifted", "halves_swapped"):
-            wrong, _ = _predict_e4m3(q32, _words(w, l, bad))
-            assert (wrong[normal] != got[normal]).mean() > 0.2, (l, bad)
+        odd = (np.arange(len(got)) & 1) == 1     # the elements a missing bit reversal moves
+        for bad in PLANTED_16 + ("not_reversed", "eight_per_call"):
+            wrong, _ = _predict_e4m3(q32, _r16(w, l, bad))
+            sel = normal & odd if bad == "not_reversed" else normal
+            assert (wrong[sel] != got[sel]).mean() > 0.2, (l, bad)
+        wrong, _ = _predict_e4m3(q32, _r16(w, l), rule="compare")
+        assert (wrong[normal] != got[normal]).mean() > 0.2, (l, "compare")
     assert predicted >= 0.95 * w.L * w.H * w.D * w.N
+
+
+def test_random_bits_predict_every_int8_code():
+    """int8: the integer grid, so the discarded part is the fraction of |q|;
+    its top 16 bits plus r16 carry; saturated at 127."""
+    w = _sr_world("i8")
+    out = run(w)
+    for l in range(w.L):
+        dst = int(w.dst_slots[l, 0])
+        y32 = _exact_f32_result(w, l)
+        amax = np.abs(y32).max(axis=-1)
+        scale = (amax / np.float32(127.0)).astype(np.float32)
+        assert out.scale[l][dst].tobytes() == scale.tobytes(), f"layer {l}: scales"
+        q = (y32 / scale[..., None]).astype(np.float32).reshape(-1).astype(np.float64)
+        a = np.abs(q)
+        d16 = np.floor((a - np.floor(a)) * 65536.0)
+        got = out.state[l][dst].reshape(-1).view(np.int8).astype(np.float64)
+        odd = (np.arange(len(got)) & 1) == 1
+        for layout, rule, must_match in (("reading", "carry", True), ("not_reversed", "carry", False),
+                                         ("halves_swapped", "carry", False), ("reading", "compare", False)):
+            up = _up(d16, _r16(w, l, layout).astype(np.float64), rule)
+            want = np.minimum(np.floor(a) + up, 127.0) * np.sign(q)
+            if must_match:
+                assert np.array_equal(want, got), f"layer {l}"
+            else:
+                sel = odd if layout == "not_reversed" else slice(None)
+                assert (want[sel] != got[sel]).mean() > 0.2, (l, layout, rule)
 
 
 def test_philox_known_answer_vectors():
