@@ -430,19 +430,20 @@ PHILOX10_WORDS_PER_SM_CLK = 6.8
 
 
 def lane_ops(shape, active, prefix, src, dst):
-    """(fp32 lane-operations, 32-bit integer lane-operations) one call needs,
-    counted from the method, not from the code, and the elements rounded
-    stochastically.  Per element of a replayed tile: one FMUL (the decay
-    product) and one FFMA per token.  With Philox rounding, per element
-    philox_rounds * 6 / 8 integer operations (a round is two 32x32->64-bit
-    multiplies, two three-way XORs and two key additions, and one call gives
-    the 16-bit numbers of eight elements) plus 4 for the rounding decision
-    (shift, add, mask, saturate).  Copies (prefix 0) cost neither."""
+    """(fp32 lane-operations, 32-bit integer lane-operations, Philox words)
+    one call needs, counted from the method, not from the code.  Per element
+    of a replayed tile: one FMUL (the decay product) and one FFMA per token.
+    With Philox rounding, one call (four words) serves 8 elements of 16-bit
+    state or 16 of one-byte state, and costs philox_rounds * 6 integer
+    operations (a round is two 32x32->64-bit multiplies, two three-way XORs
+    and two key additions); the rounding decision itself is the conversion
+    instruction's (bf16, f16, fp8) and is not counted.  Copies (prefix 0) cost
+    nothing."""
     import numpy as np
     n = int(np.argmax(active == -1)) if (active == -1).any() else len(active)
     elems = shape.H * shape.D * shape.N
-    fp32 = integer = rounded = 0
-    sr_per_elem = shape.philox_rounds * 6 / 8 + 4 if shape.philox_rounds > 0 else 0
+    per_call = 16 if wl.ELEM_SIZE[shape.state_dtype] == 1 else 8
+    fp32 = integer = words = 0
     for b in active[:n]:
         b = int(b)
         k = int(prefix[b])
@@ -450,9 +451,10 @@ def lane_ops(shape, active, prefix, src, dst):
             continue
         live = sum(1 for l in range(shape.L) if src[l, b] != shape.pad_slot_id and dst[l, b] != shape.pad_slot_id)
         fp32 += live * elems * (k + 1)
-        integer += live * elems * sr_per_elem
-        rounded += live * elems if shape.philox_rounds > 0 else 0
-    return fp32, int(integer), rounded
+        if shape.philox_rounds > 0:
+            integer += live * elems * shape.philox_rounds * 6 / per_call
+            words += live * elems * 4 // per_call
+    return fp32, int(integer), words
 
 
 def timed_calls(torch, call, stream, uuid, seconds=1.0):
@@ -481,16 +483,16 @@ def timed_calls(torch, call, stream, uuid, seconds=1.0):
     return e0.elapsed_time(e1) / steps, steps, info
 
 
-def _fractions(nbytes, fp32_ops, int_ops, ms, peak_gbs, sms, clock_info, rounded=0, rounds=0):
+def _fractions(nbytes, fp32_ops, int_ops, ms, peak_gbs, sms, clock_info, words=0, rounds=0):
     mhz = (clock_info or {}).get("sm_mhz") or 2070.0
     sec = ms * 1e-3
     fr = {"hbm_frac": nbytes / sec / 1e9 / peak_gbs, "hbm_frac_spec": nbytes / sec / 1e9 / SPEC_HBM_GBS,
           "fp32_lane_frac": fp32_ops / sec / (sms * ALU_LANES_PER_SM * mhz * 1e6),
           "int_lane_frac": int_ops / sec / (sms * INT_LANES_PER_SM * mhz * 1e6)}
     if rounds > 0:
-        # Philox words the rounding needs (two elements a word) against the measured generator rate
+        # Philox words the rounding needs against the measured generator rate
         words_peak = PHILOX10_WORDS_PER_SM_CLK * 10.0 / rounds * sms * mhz * 1e6
-        fr["philox_frac"] = rounded / 2 / sec / words_peak
+        fr["philox_frac"] = words / sec / words_peak
     cands = [("hbm", fr["hbm_frac"]), ("fp32", fr["fp32_lane_frac"]), ("int", fr["int_lane_frac"])]
     if "philox_frac" in fr:
         cands.append(("philox", fr["philox_frac"]))
@@ -507,7 +509,7 @@ def measure_workload(torch, rsm, shape, device, peak_gbs, sms, uuid):
     prefix = dw.replay_prefix_len.cpu().numpy()
     src, dst = dw.src_slots.cpu().numpy(), dw.dst_slots.cpu().numpy()
     state_b, ring_b, n = workload_bytes(shape, active, prefix, src, dst)
-    fp32_ops, int_ops, rounded = lane_ops(shape, active, prefix, src, dst)
+    fp32_ops, int_ops, words = lane_ops(shape, active, prefix, src, dst)
     kw = dw.call_kwargs()
     call = rsm.prepare(**kw)
     kernel = rsm.kernel_name(**kw)
@@ -522,7 +524,7 @@ def measure_workload(torch, rsm, shape, device, peak_gbs, sms, uuid):
            "philox_rounds": shape.philox_rounds, "pad_frac": shape.pad_frac, "ms_per_call": ms, "steps": steps,
            "algorithmic_bytes": state_b + ring_b, "state_gbs": state_b / (ms * 1e-3) / 1e9,
            "us_per_request": ms * 1e3 / max(n, 1), "fp32_lane_ops": fp32_ops, "int_lane_ops": int_ops}
-    out.update(_fractions(state_b + ring_b, fp32_ops, int_ops, ms, peak_gbs, sms, clock_info, rounded,
+    out.update(_fractions(state_b + ring_b, fp32_ops, int_ops, ms, peak_gbs, sms, clock_info, words,
                           shape.philox_rounds))
     out["clocks"] = clock_info
     out["device_status"] = status
@@ -757,8 +759,8 @@ def main():
         out["workloads"] = measure_named_workloads(torch, rsm, device, peak, sms, uuid, only)
         out["lane_peaks_note"] = (f"fp32: {sms} SMs x {ALU_LANES_PER_SM} lanes x the sampled SM clock; 32-bit "
                                   f"integer: {sms} SMs x {INT_LANES_PER_SM} lanes x the sampled SM clock; Philox: "
-                                  f"{PHILOX10_WORDS_PER_SM_CLK} words per SM per clock at 10 rounds (measured), "
-                                  f"two elements a word")
+                                  f"{PHILOX10_WORDS_PER_SM_CLK} words per SM per clock at 10 rounds (measured); a word "
+                                  f"rounds two 16-bit or four one-byte elements")
     if rank == 0:
         print(json.dumps(out), flush=True)
     dist.barrier()

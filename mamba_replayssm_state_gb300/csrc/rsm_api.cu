@@ -233,7 +233,7 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   const int item_max = static_cast<int>(rsm::item_layout(a->dim, a->dstate, sb, quant, ib, a->max_window).bytes);
   const bool use_tc = uses_tensor_cores(a);
   const bool sr_instance = quant && a->philox_rounds > 0;
-  const bool q8 = quant && !sr_instance;  // the four-warp one-byte kernel
+  const bool q8 = quant;  // the four-warp one-byte kernel (both rounding modes)
   const int cw = q8 ? rsm::kQ8ConsumerWarps : rsm::kConsumerWarps;
   const int base = static_cast<int>(use_tc ? rsm::kTcArenaBase : rsm::arena_base(a->dim, a->dstate, sb, cw));
   const int threads = use_tc ? rsm::kTcThreads : 32 * (1 + cw);

@@ -101,74 +101,75 @@ __device__ __forceinline__ uint4 philox4x32(uint4 c, uint32_t k0, uint32_t k1, i
   return c;
 }
 
-// ---------------------------------------------------------------------------
-// stochastic rounding of an fp32 value to a target grid
-// ---------------------------------------------------------------------------
-// The grid: spacing 2^(max(floor(log2|y|), emin) - mant) (integer grid: 1).
-// Returns the rounded value as fp32 (exactly on the grid), saturated to maxfin.
-template <int MANT, int EMIN, bool INTEGER>
-__device__ __forceinline__ float sr_round(float y, uint32_t word, float maxfin) {
-  const uint32_t bits = __float_as_uint(y);
-  const uint32_t sign = bits & 0x80000000u;
-  const uint32_t ab = bits ^ sign;
-  {
-    // Common case: a normal input whose grid spacing leaves 0 < d < 24 low
-    // bits.  Adding the complement of the d-bit random number r carries into
-    // the next grid point exactly when r < the discarded bits (the rule
-    // below), so the sum truncated to the grid is the rounded value.
-    const int eb = static_cast<int>(ab >> 23);
-    const int d = INTEGER ? 150 - eb : 23 - MANT;
-    if (eb >= (INTEGER ? 127 : EMIN + 127) && eb < 255 && d > 0 && d < 24) {
-      const uint32_t r = (ab + ((~word) >> (32 - d))) & ~((1u << d) - 1u);
-      return __uint_as_float(min(r, __float_as_uint(maxfin)) | sign);
-    }
+// C independent counters through `rounds` rounds side by side (the usual
+// 10 unrolled, so that the chains interleave).
+template <int C>
+__device__ __forceinline__ void philox4x32_n(uint4 (&c)[C], uint32_t k0, uint32_t k1, int rounds) {
+  if (rounds == 10) {
+#pragma unroll
+    for (int q = 0; q < C; ++q) c[q] = philox4x32_r<10>(c[q], k0, k1);
+    return;
   }
-  if (ab == 0u) return y;
-  if (ab >= 0x7F800000u) return ab == 0x7F800000u ? __uint_as_float(__float_as_uint(maxfin) | sign) : y;
-  const int eb = static_cast<int>(ab >> 23);
-  const int E = eb ? eb - 127 : -126;                              // a = M * 2^(E-23)
-  const uint32_t M = (ab & 0x7FFFFFu) | (eb ? 0x800000u : 0u);
-  const int ulp_exp = INTEGER ? 0 : (E > EMIN ? E : EMIN) - MANT;  // grid spacing 2^ulp_exp
-  const int d = ulp_exp - (E - 23);                                // bits of M below the spacing
-  float r;
-  if (d <= 0) {
-    r = __uint_as_float(ab);  // already on the grid
-  } else if (d < 24) {
-    const uint32_t low = ab & ((1u << d) - 1u);
-    const uint32_t lo_bits = ab - low;
-    const bool up = (word >> (32 - d)) < low;
-    r = __uint_as_float(up ? lo_bits + (1u << d) : lo_bits);
-  } else {  // |y| below one spacing: neighbours are 0 and the spacing itself
-    bool up;
-    if (d <= 32)
-      up = (word >> (32 - d)) < M;
-    else if (d < 56)
-      up = (static_cast<uint64_t>(word) << (d - 32)) < M;
-    else
-      up = (word == 0u);
-    const float spacing = ulp_exp >= -126 ? __uint_as_float(static_cast<uint32_t>(ulp_exp + 127) << 23)
-                                          : __uint_as_float(1u << (ulp_exp + 149));
-    r = up ? spacing : 0.0f;
-  }
-  r = fminf(r, maxfin);
-  return __uint_as_float(__float_as_uint(r) | sign);
+#pragma unroll
+  for (int q = 0; q < C; ++q) c[q] = philox4x32(c[q], k0, k1, rounds);
 }
 
-__device__ __forceinline__ float sr_bf16(float y, uint32_t w) {
-  return sr_round<7, -126, false>(y, w, __uint_as_float(0x7F7F0000u));
+// ---------------------------------------------------------------------------
+// stochastic rounding
+// ---------------------------------------------------------------------------
+// An element's magnitude goes up to the next grid point iff the top 16 bits of
+// its discarded part plus its 16-bit random number carry past 2^16; the
+// result saturates to the largest finite value (infinity too) and keeps its
+// sign.  bf16, f16 and fp8 e4m3 take the decision in the conversion
+// instruction with stochastic rounding (cvt.rs, sm_100 family), which reads
+// one 32-bit word of random bits per two 16-bit or four fp8 results:
+//   bf16x2 / f16x2: the low result with rbits[15:0], the high with
+//     rbits[31:16] (f16 compares their low 13 bits with its 13 discarded bits);
+//   e4m3x4: byte 0 with rbits[15:0], byte 1 with rbits[15:0] bit-reversed,
+//     byte 2 with rbits[31:16], byte 3 with rbits[31:16] bit-reversed.
+__device__ __forceinline__ uint32_t sr_bf16x2(float lo, float hi, uint32_t rbits) {
+  uint32_t d;
+  asm("cvt.rs.satfinite.bf16x2.f32 %0, %1, %2, %3;" : "=r"(d) : "f"(hi), "f"(lo), "r"(rbits));
+  return d;
 }
-__device__ __forceinline__ float sr_f16(float y, uint32_t w) { return sr_round<10, -14, false>(y, w, 65504.0f); }
-__device__ __forceinline__ float sr_e4m3(float y, uint32_t w) { return sr_round<3, -6, false>(y, w, 448.0f); }
-__device__ __forceinline__ float sr_i8(float y, uint32_t w) { return sr_round<0, 0, true>(y, w, 127.0f); }
-
-// stochastic rounding to the grid of state format F (fp32: identity)
+__device__ __forceinline__ uint32_t sr_f16x2(float lo, float hi, uint32_t rbits) {
+  uint32_t d;
+  asm("cvt.rs.satfinite.f16x2.f32 %0, %1, %2, %3;" : "=r"(d) : "f"(hi), "f"(lo), "r"(rbits));
+  return d;
+}
+// four values, v0 in byte 0
+__device__ __forceinline__ uint32_t sr_e4m3x4(float v0, float v1, float v2, float v3, uint32_t rbits) {
+  uint32_t d;
+  asm("cvt.rs.satfinite.e4m3x4.f32 %0, {%1, %2, %3, %4}, %5;" : "=r"(d) : "f"(v3), "f"(v2), "f"(v1), "f"(v0), "r"(rbits));
+  return d;
+}
+// two 16-bit state values, `lo` in the low half
 template <int F>
-__device__ __forceinline__ float sr_fmt(float y, uint32_t w) {
-  if constexpr (F == RSM_BF16) return sr_bf16(y, w);
-  else if constexpr (F == RSM_F16) return sr_f16(y, w);
-  else if constexpr (F == RSM_I8) return sr_i8(y, w);
-  else if constexpr (F == RSM_FP8_E4M3) return sr_e4m3(y, w);
-  else return y;
+__device__ __forceinline__ uint32_t sr_pack2(float lo, float hi, uint32_t rbits) {
+  static_assert(F == RSM_BF16 || F == RSM_F16, "16-bit state");
+  if constexpr (F == RSM_BF16) return sr_bf16x2(lo, hi, rbits);
+  else return sr_f16x2(lo, hi, rbits);
+}
+
+// int8 on the integer grid, in fp32: |y| - trunc|y| and its scaling by 2^16
+// are exact (|y| < 2^23), and so is the floor that keeps the top 16 bits.
+__device__ __forceinline__ float sr_i8(float y, uint32_t r16) {
+  const float a = fabsf(y);
+  const float lo = truncf(a);
+  const float d16 = floorf((a - lo) * 65536.0f);
+  const float r = __uint_as_float(0x4B000000u | r16) - 8388608.0f;  // r16 as fp32, exactly
+  const float q = fminf(lo + (d16 + r >= 65536.0f ? 1.0f : 0.0f), 127.0f);
+  return copysignf(q, y);
+}
+
+// The random numbers of four one-byte elements from their word: lo16,
+// lo16 reversed, hi16, hi16 reversed (the e4m3x4 assignment).
+__device__ __forceinline__ void sr_r16x4(uint32_t w, uint32_t (&r)[4]) {
+  const uint32_t rv = __brev(w);
+  r[0] = w & 0xFFFFu;
+  r[1] = rv >> 16;
+  r[2] = w >> 16;
+  r[3] = rv & 0xFFFFu;
 }
 
 // ---------------------------------------------------------------------------

@@ -563,59 +563,36 @@ static __device__ __noinline__ void store_bytes(unsigned char* dst, uint2 v) {
   for (int q = 0; q < 8; ++q) dst[q] = b[q];
 }
 
-// The 16 random bits of the elements of one Philox block (eight consecutive
-// elements: element q takes the low (q even) or high (q odd) half of word
-// q / 2), each placed in the upper half of a 32-bit word: the form the
-// rounding rule of sr_round takes.
-__device__ __forceinline__ uint32_t sr_lo16(uint32_t w) { return w << 16; }
-__device__ __forceinline__ uint32_t sr_hi16(uint32_t w) { return w & 0xFFFF0000u; }
-
-// Stochastic rounding of 8 consecutive elements (one Philox block, counter
-// (e/8, dst_slot, layer, 0) with e the first element's index), then the exact
-// pack.  Kept out of line, so that the code of the rounding-to-nearest path,
-// which every call without Philox runs, stays compact.
+// Stochastic rounding of 8 consecutive 16-bit elements (one Philox call,
+// counter (e/8, dst_slot, layer, 0) with e the first element's index; word i
+// rounds elements 2i and 2i + 1) into their 16 bytes.
 template <int SF>
-__device__ __noinline__ typename Vec<SF>::Raw sr_pack8(float2 a0, float2 a1, float2 a2, float2 a3, uint32_t blk,
-                                                       uint32_t slot, uint32_t layer, uint32_t key0, uint32_t key1,
-                                                       int rounds) {
-  const uint4 r = philox4x32(make_uint4(blk, slot, layer, 0u), key0, key1, rounds);
-  float2 v[4];
-  v[0] = make_float2(sr_fmt<SF>(a0.x, sr_lo16(r.x)), sr_fmt<SF>(a0.y, sr_hi16(r.x)));
-  v[1] = make_float2(sr_fmt<SF>(a1.x, sr_lo16(r.y)), sr_fmt<SF>(a1.y, sr_hi16(r.y)));
-  v[2] = make_float2(sr_fmt<SF>(a2.x, sr_lo16(r.z)), sr_fmt<SF>(a2.y, sr_hi16(r.z)));
-  v[3] = make_float2(sr_fmt<SF>(a3.x, sr_lo16(r.w)), sr_fmt<SF>(a3.y, sr_hi16(r.w)));
-  return pack_vec_rne<SF>(v);
+__device__ __forceinline__ uint4 sr_words8(float2 a0, float2 a1, float2 a2, float2 a3, uint4 r) {
+  return make_uint4(sr_pack2<SF>(a0.x, a0.y, r.x), sr_pack2<SF>(a1.x, a1.y, r.y), sr_pack2<SF>(a2.x, a2.y, r.z),
+                    sr_pack2<SF>(a3.x, a3.y, r.w));
 }
 
-// The same for two rows of 8 elements (blocks blk_a and blk_b): two
-// independent Philox chains side by side.
+// Kept out of line, so that the code of the rounding-to-nearest path, which
+// every call without Philox runs, stays compact.
 template <int SF>
+__device__ __noinline__ uint4 sr_pack8(float2 a0, float2 a1, float2 a2, float2 a3, uint32_t blk, uint32_t slot,
+                                       uint32_t layer, uint32_t key0, uint32_t key1, int rounds) {
+  return sr_words8<SF>(a0, a1, a2, a3, philox4x32(make_uint4(blk, slot, layer, 0u), key0, key1, rounds));
+}
+
+// The same for two rows of 8 elements (calls blk_a and blk_b): two independent
+// Philox chains side by side.
 struct RawPair {
-  typename Vec<SF>::Raw a, b;
+  uint4 a, b;
 };
 
 template <int SF>
-__device__ __noinline__ RawPair<SF> sr_pack8x2(float2 a0, float2 a1, float2 a2, float2 a3, float2 b0, float2 b1,
-                                               float2 b2, float2 b3, uint32_t blk_a, uint32_t blk_b, uint32_t slot,
-                                               uint32_t layer, uint32_t key0, uint32_t key1, int rounds) {
-  uint4 r0, r1;
-  if (rounds == 10) {
-    r0 = philox4x32_r<10>(make_uint4(blk_a, slot, layer, 0u), key0, key1);
-    r1 = philox4x32_r<10>(make_uint4(blk_b, slot, layer, 0u), key0, key1);
-  } else {
-    r0 = philox4x32(make_uint4(blk_a, slot, layer, 0u), key0, key1, rounds);
-    r1 = philox4x32(make_uint4(blk_b, slot, layer, 0u), key0, key1, rounds);
-  }
-  float2 v[4], w[4];
-  v[0] = make_float2(sr_fmt<SF>(a0.x, sr_lo16(r0.x)), sr_fmt<SF>(a0.y, sr_hi16(r0.x)));
-  v[1] = make_float2(sr_fmt<SF>(a1.x, sr_lo16(r0.y)), sr_fmt<SF>(a1.y, sr_hi16(r0.y)));
-  v[2] = make_float2(sr_fmt<SF>(a2.x, sr_lo16(r0.z)), sr_fmt<SF>(a2.y, sr_hi16(r0.z)));
-  v[3] = make_float2(sr_fmt<SF>(a3.x, sr_lo16(r0.w)), sr_fmt<SF>(a3.y, sr_hi16(r0.w)));
-  w[0] = make_float2(sr_fmt<SF>(b0.x, sr_lo16(r1.x)), sr_fmt<SF>(b0.y, sr_hi16(r1.x)));
-  w[1] = make_float2(sr_fmt<SF>(b1.x, sr_lo16(r1.y)), sr_fmt<SF>(b1.y, sr_hi16(r1.y)));
-  w[2] = make_float2(sr_fmt<SF>(b2.x, sr_lo16(r1.z)), sr_fmt<SF>(b2.y, sr_hi16(r1.z)));
-  w[3] = make_float2(sr_fmt<SF>(b3.x, sr_lo16(r1.w)), sr_fmt<SF>(b3.y, sr_hi16(r1.w)));
-  return RawPair<SF>{pack_vec_rne<SF>(v), pack_vec_rne<SF>(w)};
+__device__ __noinline__ RawPair sr_pack8x2(float2 a0, float2 a1, float2 a2, float2 a3, float2 b0, float2 b1, float2 b2,
+                                           float2 b3, uint32_t blk_a, uint32_t blk_b, uint32_t slot, uint32_t layer,
+                                           uint32_t key0, uint32_t key1, int rounds) {
+  uint4 r[2] = {make_uint4(blk_a, slot, layer, 0u), make_uint4(blk_b, slot, layer, 0u)};
+  philox4x32_n<2>(r, key0, key1, rounds);
+  return RawPair{sr_words8<SF>(a0, a1, a2, a3, r[0]), sr_words8<SF>(b0, b1, b2, b3, r[1])};
 }
 
 // One item with a non-empty prefix on the CUDA cores: the decay scan, the
@@ -816,10 +793,10 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
         store_bytes(dst_tile + off, out);
     };
     bool use_sr = false;
-    if constexpr (SF != RSM_F32) use_sr = sr;
+    if constexpr (Fmt<SF>::bytes == 2) use_sr = sr;  // one-byte state rounds in its own kernel
     if (worker) {
       if (use_sr) {
-        if constexpr (SF != RSM_F32) {
+        if constexpr (Fmt<SF>::bytes == 2) {
           // Philox counter of element e: (e / 8, dst_slot, layer, 0); a row's
           // 8 elements start on a multiple of 8, so they are one block
           static_assert(V2 == 4, "stochastic rounding works on 8-element vectors");
@@ -828,7 +805,7 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
           if constexpr (RPT % 2 == 0) {
 #pragma unroll
             for (int r = 0; r < RPT; r += 2) {
-              const RawPair<SF> o = sr_pack8x2<SF>(acc[r][0], acc[r][1], acc[r][2], acc[r][3], acc[r + 1][0],
+              const RawPair o = sr_pack8x2<SF>(acc[r][0], acc[r][1], acc[r][2], acc[r][3], acc[r + 1][0],
                                                    acc[r + 1][1], acc[r + 1][2], acc[r + 1][3], blk0 + r * kRowBlocks,
                                                    blk0 + (r + 1) * kRowBlocks, dst_slot_id, layer_id, key0, key1,
                                                    p.philox_rounds);
@@ -1004,8 +981,9 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_kernel(const __grid_c
     run_consumer<SF, IF, D, N>(p, smem, warp - 1, lane);
 }
 
-// The one-byte kernel (rsm_q8_kernel.cuh), rounding to nearest.
-template <int SF, int IF>
+// The one-byte kernel (rsm_q8_kernel.cuh): rounding to nearest, or
+// stochastic rounding (SR).
+template <int SF, int IF, bool SR>
 const void* q8_kernel();
 
 // Instantiation hook: each translation unit that includes this header (and,
@@ -1016,18 +994,18 @@ template <int SF, int IF, int D, int N>
 const void* kernel_for() {
   if constexpr (Fmt<SF>::quant) {
     static_assert(D == 64 && N == 128, "one-byte state is 64 x 128");
-    return q8_kernel<SF, IF>();
+    return q8_kernel<SF, IF, false>();
   } else {
     return reinterpret_cast<const void*>(&materialize_kernel<SF, IF, D, N>);
   }
 }
 
-// One-byte state with stochastic rounding: this eight-warp kernel, whose two
-// CTAs per SM keep more Philox chains in flight than the four-warp one-byte kernel.
+// One-byte state with stochastic rounding: the one-byte kernel's instance
+// that draws the Philox words.
 template <int SF, int IF, int D, int N>
 const void* kernel_for_sr() {
   static_assert(Fmt<SF>::quant && D == 64 && N == 128, "the stochastic-rounding instance is one-byte state");
-  return reinterpret_cast<const void*>(&materialize_kernel<SF, IF, D, N>);
+  return q8_kernel<SF, IF, true>();
 }
 
 }  // namespace rsm

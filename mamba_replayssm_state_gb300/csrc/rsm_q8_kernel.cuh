@@ -16,9 +16,10 @@
 // 8 lc .. 8 lc + 7, so that the 16 lanes of a row group hold whole rows and a
 // row's amax is a warp reduction.
 //
-// This kernel rounds to nearest even.  One-byte state with Philox stochastic
-// rounding runs on the eight-warp materialization kernel, whose two CTAs per
-// SM keep more Philox chains in flight (kernel_for_sr in rsm_kernel.cuh).
+// Two instances: rounding to nearest even, and Philox stochastic rounding
+// (template SR), whose Philox words cover 16 consecutive elements of a row:
+// the lanes 2m and 2m + 1 of a row group share one call per row, each drawing
+// the call of one row of a row pair and trading the two words the other needs.
 #pragma once
 #include "rsm_kernel.cuh"
 
@@ -53,9 +54,10 @@ __device__ __forceinline__ void store_row8(const float2 (&v)[4], float inv, unsi
     store_bytes(d, out);
 }
 
-template <int SF, int IF>
-__device__ __forceinline__ void replay_q8(const unsigned char* sb, const ItemLayout& il, const ItemDesc* desc, int k,
-                                          float* wbuf, float* cbuf, int cw, int lane, uint32_t empty_bar) {
+template <int SF, int IF, bool SR>
+__device__ __forceinline__ void replay_q8(const Params& p, const unsigned char* sb, const ItemLayout& il,
+                                          const ItemDesc* desc, int k, float* wbuf, float* cbuf, int cw, int lane,
+                                          uint32_t empty_bar, uint32_t key0, uint32_t key1) {
   constexpr int D = 64, N = 128, IE = In<IF>::bytes;
   constexpr int RPT = 8;            // rows per lane
   constexpr int SLAB = 16;          // rows per warp
@@ -68,6 +70,10 @@ __device__ __forceinline__ void replay_q8(const unsigned char* sb, const ItemLay
   unsigned char* dst_tile = reinterpret_cast<unsigned char*>(desc->dst_state);
   float* dst_sc = reinterpret_cast<float*>(desc->dst_scale);
   const bool dst_aligned = (flags & kFlagDstAligned) != 0u;
+  // the Philox counter words of this item, read before the slot is released
+  const uint32_t dst_slot_id = static_cast<uint32_t>(desc->dst_slot);
+  const uint32_t layer_id = static_cast<uint32_t>(desc->layer);
+  const int head = desc->head;
 
   const float P = decay_scan(reinterpret_cast<const float*>(sb + il.off_dt), desc->A, k, lane, wbuf);
 
@@ -171,22 +177,80 @@ __device__ __forceinline__ void replay_q8(const unsigned char* sb, const ItemLay
   const float scale_own = inv_own <= FLT_MAX ? __fdiv_rn(am, qmax) : 0.0f;
 
   const int group0 = lane & 16;
+  if constexpr (SR) {
+    // Philox counter (e / 16, dst_slot, layer, 0) with e = (h * D + row) * N +
+    // col: one call per 16 columns of a row, the columns of lanes lc and lc ^ 1.
+    // For row pair (2q, 2q + 1) the even lane draws row 2q's call and the odd
+    // lane row 2q + 1's; words 0, 1 cover the even lane's 8 columns, 2, 3 the
+    // odd lane's.  Two row pairs (two Philox chains) at a time.
+    const bool odd = (lc & 1) != 0;
 #pragma unroll
-  for (int r = 0; r < RPT; ++r) {
-    const float inv = __shfl_sync(0xFFFFFFFFu, inv_own, group0 + 2 * r);
-    const float2 inv2 = make_float2(inv, inv);
-    float2 v[4];
-    if constexpr (SF == RSM_I8) {
-      // round to nearest even in one step: fl(v * inv + 1.5 * 2^23) keeps the
-      // exact product's rounding to an integer in its low byte (|v * inv| <= 127.5)
-      const float2 magic = make_float2(12582912.0f, 12582912.0f);
+    for (int q0 = 0; q0 < RPT / 2; q0 += 2) {
+      uint4 rw[2];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = __ffma2_rn(acc[r][u], inv2, magic);
-    } else {
+      for (int q = 0; q < 2; ++q) {
+        const int row = row0 + 2 * (q0 + q) + (odd ? 1 : 0);
+        rw[q] = make_uint4(static_cast<uint32_t>((head * D + row) * (N / 16) + (lc >> 1)), dst_slot_id, layer_id, 0u);
+      }
+      philox4x32_n<2>(rw, key0, key1, p.philox_rounds);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = __fmul2_rn(acc[r][u], inv2);
+      for (int q = 0; q < 2; ++q) {
+        const uint32_t g0 = __shfl_xor_sync(0xFFFFFFFFu, odd ? rw[q].x : rw[q].z, 1);
+        const uint32_t g1 = __shfl_xor_sync(0xFFFFFFFFu, odd ? rw[q].y : rw[q].w, 1);
+        const uint2 words[2] = {odd ? make_uint2(g0, g1) : make_uint2(rw[q].x, rw[q].y),
+                                odd ? make_uint2(rw[q].z, rw[q].w) : make_uint2(g0, g1)};
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int r = 2 * (q0 + q) + h2;
+          const float inv = __shfl_sync(0xFFFFFFFFu, inv_own, group0 + 2 * r);
+          const float2 inv2 = make_float2(inv, inv);
+          float2 v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) v[u] = __fmul2_rn(acc[r][u], inv2);
+          uint2 out;
+          if constexpr (SF == RSM_I8) {
+            uint32_t ra[4], rb[4];
+            sr_r16x4(words[h2].x, ra);
+            sr_r16x4(words[h2].y, rb);
+            const float2 magic = make_float2(12582912.0f, 12582912.0f);
+            float2 c[4] = {make_float2(sr_i8(v[0].x, ra[0]), sr_i8(v[0].y, ra[1])),
+                           make_float2(sr_i8(v[1].x, ra[2]), sr_i8(v[1].y, ra[3])),
+                           make_float2(sr_i8(v[2].x, rb[0]), sr_i8(v[2].y, rb[1])),
+                           make_float2(sr_i8(v[3].x, rb[2]), sr_i8(v[3].y, rb[3]))};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) c[u] = __fadd2_rn(c[u], magic);
+            out = pack_row8<SF>(c);
+          } else {
+            out = make_uint2(sr_e4m3x4(v[0].x, v[0].y, v[1].x, v[1].y, words[h2].x),
+                             sr_e4m3x4(v[2].x, v[2].y, v[3].x, v[3].y, words[h2].y));
+          }
+          if (!(inv <= FLT_MAX)) out = make_uint2(0u, 0u);
+          unsigned char* d = dst_tile + (row0 + r) * N + 8 * lc;
+          if (dst_aligned)
+            stg64_stream(d, out);
+          else
+            store_bytes(d, out);
+        }
+      }
     }
-    store_row8<SF>(v, inv, dst_tile + (row0 + r) * N + 8 * lc, dst_aligned);
+  } else {
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+      const float inv = __shfl_sync(0xFFFFFFFFu, inv_own, group0 + 2 * r);
+      const float2 inv2 = make_float2(inv, inv);
+      float2 v[4];
+      if constexpr (SF == RSM_I8) {
+        // round to nearest even in one step: fl(v * inv + 1.5 * 2^23) keeps the
+        // exact product's rounding to an integer in its low byte (|v * inv| <= 127.5)
+        const float2 magic = make_float2(12582912.0f, 12582912.0f);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = __ffma2_rn(acc[r][u], inv2, magic);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = __fmul2_rn(acc[r][u], inv2);
+      }
+      store_row8<SF>(v, inv, dst_tile + (row0 + r) * N + 8 * lc, dst_aligned);
+    }
   }
   if ((lc & 1) == 0) {
     const int srow = row0 + (lc >> 1);
@@ -200,7 +264,7 @@ __device__ __forceinline__ void replay_q8(const unsigned char* sb, const ItemLay
   }
 }
 
-template <int SF, int IF>
+template <int SF, int IF, bool SR>
 __device__ __forceinline__ void run_consumer_q8(const Params& p, unsigned char* smem, int cw, int lane) {
   constexpr int D = 64, N = 128, IE = In<IF>::bytes;
   const uint32_t full0 = smem_addr(smem);
@@ -209,6 +273,13 @@ __device__ __forceinline__ void run_consumer_q8(const Params& p, unsigned char* 
   float* wbuf = reinterpret_cast<float*>(smem + kWeightOff) + cw * kWeightStride;
   float* cbuf = reinterpret_cast<float*>(smem + kWarpBufOff) + cw * warp_buf_floats(D, N, 1, kQ8ConsumerWarps);
   const int tid = cw * 32 + lane;  // 0 .. 127
+
+  uint32_t key0 = 0, key1 = 0;
+  if constexpr (SR) {
+    const uint64_t s = static_cast<uint64_t>(__ldg(p.rand_seed));
+    key0 = static_cast<uint32_t>(s);
+    key1 = static_cast<uint32_t>(s >> 32);
+  }
 
   const uint32_t item_max = item_layout(D, N, 1, true, IE, p.W).bytes;
   uint32_t arena_head = 0;
@@ -260,7 +331,7 @@ __device__ __forceinline__ void run_consumer_q8(const Params& p, unsigned char* 
         }
       }
     } else {
-      replay_q8<SF, IF>(sb, il, desc, k, wbuf, cbuf, cw, lane, empty_bar);
+      replay_q8<SF, IF, SR>(p, sb, il, desc, k, wbuf, cbuf, cw, lane, empty_bar, key0, key1);
     }
     if (++stage == p.stages) {
       stage = 0;
@@ -269,7 +340,7 @@ __device__ __forceinline__ void run_consumer_q8(const Params& p, unsigned char* 
   }
 }
 
-template <int SF, int IF>
+template <int SF, int IF, bool SR>
 __global__ void __maxnreg__(kQ8MaxRegs) materialize_q8_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   // empty active list: one load, then out
@@ -289,12 +360,12 @@ __global__ void __maxnreg__(kQ8MaxRegs) materialize_q8_kernel(const __grid_const
   if (warp == 0)
     run_loader<SF, IF, 64, 128>(p, smem, lane);
   else
-    run_consumer_q8<SF, IF>(p, smem, warp - 1, lane);
+    run_consumer_q8<SF, IF, SR>(p, smem, warp - 1, lane);
 }
 
-template <int SF, int IF>
+template <int SF, int IF, bool SR>
 const void* q8_kernel() {
-  return reinterpret_cast<const void*>(&materialize_q8_kernel<SF, IF>);
+  return reinterpret_cast<const void*>(&materialize_q8_kernel<SF, IF, SR>);
 }
 
 }  // namespace rsm

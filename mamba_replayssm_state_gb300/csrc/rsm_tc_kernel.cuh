@@ -71,16 +71,20 @@ __device__ __noinline__ void tc_epilogue_general(int philox_rounds, uint32_t tad
 #pragma unroll 1
     for (int c = 0; c < 16; ++c) {
       const int i = 16 * part + c;
-      float y = fmaf(P, to_f32_16<SF>(s0_col[i * N]), acc[c]);
+      const float y = fmaf(P, to_f32_16<SF>(s0_col[i * N]), acc[c]);
+      uint32_t v;
       if (sr) {
+        // element e's 16 bits: the low (e even) or high half of word (e >> 1) & 3
+        // of call e >> 3, given to the conversion as the random bits of its low result
         const int64_t e = (static_cast<int64_t>(h) * D + i) * N + j;
         const uint4 rnd =
             philox4x32(make_uint4(static_cast<uint32_t>(e >> 3), dst_slot_id, layer_id, 0u), key0, key1, philox_rounds);
         const int q = static_cast<int>((e >> 1) & 3);
         const uint32_t wsel = q == 0 ? rnd.x : q == 1 ? rnd.y : q == 2 ? rnd.z : rnd.w;
-        y = sr_fmt<SF>(y, (e & 1) ? sr_hi16(wsel) : sr_lo16(wsel));
+        v = sr_pack2<SF>(y, 0.0f, (e & 1) ? (wsel >> 16) : (wsel & 0xFFFFu)) & 0xFFFFu;
+      } else {
+        v = from_f32_16<SF>(y);
       }
-      const uint32_t v = from_f32_16<SF>(y);
       unsigned char* q = out_col + static_cast<uint32_t>(i) * (N * 2u);
       if (dst_aligned) {
         stg16_stream(q, static_cast<uint16_t>(v));

@@ -79,20 +79,21 @@ def test_profile_traffic_follows_the_source_hash(bench):
 
 
 def test_lane_operations_and_philox_fraction(bench):
-    """Per replayed element: k FFMA + 1 FMUL; with Philox rounding 10 * 6 / 8 + 4
-    integer operations and one rounded element (two a Philox word); copies
-    cost nothing."""
-    shape = wl.SHAPES["hybrid48_fp8_sr"]
-    n, k = 4, 3
-    active, prefix, src, dst = _meta(shape, n, k, pad=(0, 1))
-    prefix[2] = 0                                    # request 2 is a copy
-    fp32, integer, rounded = bench.lane_ops(shape, active, prefix, src, dst)
-    elems = 256 * 64 * 128
-    live = (n - 1) * shape.L - 1                     # one copy request, one padded layer
-    assert fp32 == live * elems * (k + 1)
-    assert integer == int(live * elems * (10 * 6 / 8 + 4))
-    assert rounded == live * elems
-    fr = bench._fractions(1e9, fp32, integer, 1.0, 6790.0, 152, {"sm_mhz": 2070.0}, rounded, 10)
+    """Per replayed element: k FFMA + 1 FMUL; with Philox rounding one call
+    (10 rounds x 6 integer operations, four words) per 16 one-byte or 8
+    16-bit elements; copies cost nothing."""
+    for name, per_call in (("hybrid48_fp8_sr", 16), ("hybrid48_bf16", 8)):
+        shape = wl.SHAPES[name].replace(philox_rounds=10)
+        n, k = 4, 3
+        active, prefix, src, dst = _meta(shape, n, k, pad=(0, 1))
+        prefix[2] = 0                                    # request 2 is a copy
+        fp32, integer, words = bench.lane_ops(shape, active, prefix, src, dst)
+        elems = 256 * 64 * 128
+        live = (n - 1) * shape.L - 1                     # one copy request, one padded layer
+        assert fp32 == live * elems * (k + 1)
+        assert integer == int(live * elems * 60 / per_call)
+        assert words == live * elems * 4 // per_call
+    fr = bench._fractions(1e9, fp32, integer, 1.0, 6790.0, 152, {"sm_mhz": 2070.0}, words, 10)
     words_peak = 6.8 * 152 * 2070e6
-    assert abs(fr["philox_frac"] - rounded / 2 / 1e-3 / words_peak) < 1e-12
+    assert abs(fr["philox_frac"] - words / 1e-3 / words_peak) < 1e-12
     assert "philox_frac" not in bench._fractions(1e9, 1, 0, 1.0, 6790.0, 152, None)
