@@ -126,7 +126,11 @@ __device__ __forceinline__ void replay_q8(const Params& p, const unsigned char* 
     }
     const float* cp = cbuf + 2 * RPT * lr;
     const float* bp = bbuf + 4 * lc;
-#pragma unroll 2
+    // two tokens per pass when rounding to nearest; one with stochastic
+    // rounding, whose instance needs the registers (measured on GB300: fp8 SR
+    // 18% faster, the nearest-rounding instances unchanged)
+    constexpr int kTokUnroll = SR ? 1 : 2;
+#pragma unroll kTokUnroll
     for (int t = 0; t < tn; ++t) {
       float2 c2[RPT];
 #pragma unroll
