@@ -412,11 +412,17 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
           const int x_t0 = lane / XC, x_part = lane % XC;
           int pr = rs + x_t0 - (rs + x_t0 >= p.R ? p.R : 0);
           while (pr >= p.R) pr -= p.R;
+          const int64_t row_bytes = static_cast<int64_t>(p.H) * (D * IE);
+          const unsigned char* xp = x_slot + static_cast<int64_t>(h) * (D * IE) + 16 * x_part;
+          const unsigned char* xq = xp + static_cast<int64_t>(pr) * row_bytes;
+          const unsigned char* x_end = xp + static_cast<int64_t>(p.R) * row_bytes;
+          const int64_t step = (32 / XC) * row_bytes, wrap = static_cast<int64_t>(p.R) * row_bytes;
+          uint32_t sdst = sba + il.off_x + static_cast<uint32_t>(x_t0 * D * IE + 16 * x_part);
           for (int t = x_t0; t < k; t += 32 / XC) {
-            cp_async_16(sba + il.off_x + static_cast<uint32_t>(t * D * IE + 16 * x_part),
-                        x_slot + (static_cast<int64_t>(pr) * p.H + h) * (D * IE) + 16 * x_part);
-            pr += 32 / XC;
-            while (pr >= p.R) pr -= p.R;
+            cp_async_16(sdst, xq);
+            sdst += (32 / XC) * D * IE;
+            xq += step;
+            while (xq >= x_end) xq -= wrap;  // rings shorter than the step wrap more than once
           }
           if (!same_B) {
             const int b_t0 = lane / BC, b_part = lane % BC;

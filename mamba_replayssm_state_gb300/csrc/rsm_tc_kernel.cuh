@@ -49,6 +49,10 @@ __device__ __forceinline__ float to_f32_16(uint32_t bits) {
   }
 }
 
+__device__ __forceinline__ void stg32_stream(void* p, uint32_t v) {
+  asm volatile("st.global.cs.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 template <int SF>
 __device__ __forceinline__ uint32_t from_f32_16(float v) {
   // round to nearest even (values already rounded stochastically stay exact)
@@ -296,12 +300,17 @@ __device__ __forceinline__ void run_epilogue_tc(const Params& p, unsigned char* 
     unsigned char* out_col = dst_tile + static_cast<uint32_t>(j) * 2u;
     const uint16_t* s0_col = reinterpret_cast<const uint16_t*>(sb) + j;
     if (!sr && dst_aligned) {
-      // S_0 at this thread's column, all 64 dim rows, as packed 16-bit pairs;
+      // Columns in pairs: lanes 2m and 2m + 1 own columns j and j ^ 1 (TMEM
+      // lanes); of each row pair (i, i + 1) the even lane writes row i and the
+      // odd lane row i + 1, both columns, after trading one accumulator value.
+      const bool odd = (lane & 1) != 0;
+      const int jp = j & ~1;
+      // S_0 of the column pair at this lane's rows 2c + odd, as 16-bit pairs;
       // then the slot goes back to the loader while the MMA runs
+      const uint32_t* s0p = reinterpret_cast<const uint32_t*>(sb) + jp / 2;
       uint32_t s0[D / 2];
 #pragma unroll
-      for (int c = 0; c < D / 2; ++c)
-        s0[c] = static_cast<uint32_t>(s0_col[(2 * c) * N]) | (static_cast<uint32_t>(s0_col[(2 * c + 1) * N]) << 16);
+      for (int c = 0; c < D / 2; ++c) s0[c] = s0p[(2 * c + (odd ? 1 : 0)) * (N / 2)];
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar);
       if (!tc_wait(sbase + kTcMmaDone + 8u * buf, (n_tc >> 1) & 1u, abort_flag)) {
@@ -309,17 +318,21 @@ __device__ __forceinline__ void run_epilogue_tc(const Params& p, unsigned char* 
         break;
       }
       tc_fence_after();
-      // S = P S_0 + (C B), rounded to nearest and stored 16 accumulator columns at a time
+      unsigned char* out_pair = dst_tile + static_cast<uint32_t>(jp) * 2u + (odd ? N * 2u : 0u);
 #pragma unroll
       for (int part = 0; part < D / 16; ++part) {
         float acc[16];
         tmem_ld16(taddr + 16u * part, acc);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint32_t pair = s0[8 * part + c / 2];
-          const float x0 = to_f32_16<SF>(c & 1 ? pair >> 16 : pair & 0xFFFFu);
-          stg16_stream(out_col + static_cast<uint32_t>(16 * part + c) * (N * 2u),
-                       static_cast<uint16_t>(from_f32_16<SF>(fmaf(P, x0, acc[c]))));
+        for (int c2 = 0; c2 < 8; ++c2) {
+          const float a0 = acc[2 * c2], a1 = acc[2 * c2 + 1];
+          const float recv = __shfl_xor_sync(0xFFFFFFFFu, odd ? a0 : a1, 1);
+          const float lo = odd ? recv : a0, hi = odd ? a1 : recv;
+          const uint32_t sp = s0[8 * part + c2];
+          const float x0 = to_f32_16<SF>(sp & 0xFFFFu), x1 = to_f32_16<SF>(sp >> 16);
+          const float y0 = fmaf(P, x0, lo), y1 = fmaf(P, x1, hi);
+          const uint32_t w = SF == RSM_BF16 ? pack_bf16x2(y0, y1) : pack_f16x2(y0, y1);
+          stg32_stream(out_pair + static_cast<uint32_t>(16 * part + 2 * c2) * (N * 2u), w);
         }
       }
     } else {
