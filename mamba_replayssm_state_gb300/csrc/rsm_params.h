@@ -8,10 +8,9 @@ namespace rsm {
 constexpr int kConsumerWarps = 8;  // 16-bit and fp32 state, and the tensor-core kernel
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kThreads = 32 + kConsumerThreads;
-// One-byte state rounded to nearest: four consumer warps per CTA (each lane
-// owns 64 codes, so the per-item work of a lane is spread over twice the
-// elements), three CTAs per SM.  (With stochastic rounding, whose Philox
-// chains want more warps in flight, one-byte state takes the eight-warp kernel.)
+// One-byte state (both rounding modes): four consumer warps per CTA (each
+// lane owns 64 codes, so the per-item work of a lane is spread over twice the
+// elements), three CTAs per SM.
 constexpr int kQ8ConsumerWarps = 4;
 constexpr int kQ8Threads = 32 * (1 + kQ8ConsumerWarps);
 constexpr int kQ8MaxRegs = 128;  // 15 warps per SM: four on three sub-partitions, 4 x 32 x 128 = 16384
