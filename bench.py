@@ -44,8 +44,9 @@ _SHARED_SOURCES = ["include/replayssm.h", _CSRC + "rsm_api.cu", _CSRC + "rsm_ptx
 # summary is valid only for the hash of the files it was taken on
 KERNEL_SOURCES = {
     "materialize_kernel": _SHARED_SOURCES + [_CSRC + f for f in (
-        "rsm_kernel.cuh", "rsm_formats.cuh", "rsm_q8_kernel.cuh", "rsm_inst_f32.cu", "rsm_inst_bf16.cu",
-        "rsm_inst_f16.cu", "rsm_inst_q8.cu", "rsm_inst_q8sr.cu")],
+        "rsm_kernel.cuh", "rsm_formats.cuh", "rsm_inst_f32.cu", "rsm_inst_bf16.cu", "rsm_inst_f16.cu")],
+    "materialize_q8_kernel": _SHARED_SOURCES + [_CSRC + f for f in (
+        "rsm_kernel.cuh", "rsm_formats.cuh", "rsm_q8_kernel.cuh", "rsm_inst_q8.cu", "rsm_inst_q8sr.cu")],
     "materialize_tc_kernel": _SHARED_SOURCES + [_CSRC + f for f in (
         "rsm_kernel.cuh", "rsm_formats.cuh", "rsm_tc_kernel.cuh", "rsm_tc.cuh", "rsm_inst_tc.cu")],
     "gdn_commit_kernel": _SHARED_SOURCES + [_CSRC + f for f in ("gdn_kernel.cuh", "gdn_params.h", "gdn_inst.cu")],

@@ -499,7 +499,8 @@ int rsm_gdn_commit(const rsm_gdn_commit_args* args, void* stream) {
 
 const char* rsm_kernel_name(const rsm_materialize_args* args) {
   if (validate(args) < 0) return "";
-  return uses_tensor_cores(args) ? "materialize_tc_kernel" : "materialize_kernel";
+  if (uses_tensor_cores(args)) return "materialize_tc_kernel";
+  return elem_bytes(args->state_dtype) == 1 ? "materialize_q8_kernel" : "materialize_kernel";
 }
 
 int rsm_gdn_args_size(void) { return static_cast<int>(sizeof(rsm_gdn_commit_args)); }

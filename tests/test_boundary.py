@@ -180,20 +180,22 @@ def test_gdn_empty_batch_enqueues_nothing(lib):
 
 def test_kernel_name_follows_the_launch_rule(lib):
     """rsm_kernel_name needs no GPU: the CUDA-core kernel for the 8-token
-    headline shape, the tensor-core kernel for 16-bit state with bf16 inputs at
-    64 x 128 once max_window reaches 16, and "" (with the reason) when the
-    arguments fail validation."""
+    headline shape and fp32 state, the one-byte kernel for int8 and fp8 state,
+    the tensor-core kernel for 16-bit state with bf16 inputs at 64 x 128 once
+    max_window reaches 16, and "" (with the reason) when the arguments fail
+    validation."""
     a = good_args()
     assert lib.rsm_kernel_name(ctypes.byref(a)) == b"materialize_kernel"
     a.max_window = a.ring_buffer_len = 64
     for sd in (rsm.RSM_BF16, rsm.RSM_F16):
         a.state_dtype = sd
         assert lib.rsm_kernel_name(ctypes.byref(a)) == b"materialize_tc_kernel"
-    for sd in (rsm.RSM_F32, rsm.RSM_I8):
+    a.state_dtype = rsm.RSM_F32
+    assert lib.rsm_kernel_name(ctypes.byref(a)) == b"materialize_kernel"
+    a.state_scale_ptrs = a.state_scale_slot_strides = 0x1000
+    for sd in (rsm.RSM_I8, rsm.RSM_FP8_E4M3):
         a.state_dtype = sd
-        if sd == rsm.RSM_I8:
-            a.state_scale_ptrs = a.state_scale_slot_strides = 0x1000
-        assert lib.rsm_kernel_name(ctypes.byref(a)) == b"materialize_kernel"
+        assert lib.rsm_kernel_name(ctypes.byref(a)) == b"materialize_q8_kernel"
     a.heads_per_group = 33
     assert lib.rsm_kernel_name(ctypes.byref(a)) == b""
     assert b"heads_per_group" in lib.rsm_last_error()
