@@ -54,9 +54,10 @@ struct alignas(16) ItemDesc {
 };
 static_assert(sizeof(ItemDesc) == kDescBytes, "descriptor size");
 constexpr uint32_t kFlagEnd = 1u, kFlagDstAligned = 2u, kFlagScaleAligned = 4u;
-// A tensor-core item whose head continues the previous item's B group (same
-// request and layer): its B rows are not copied, the consumers reuse the MMA
-// operand they built from the previous item's.
+// An item whose head continues the previous item's B group (same request and
+// layer): its B rows are not copied.  The tensor-core kernel reuses the MMA
+// operand it built from the previous item's; the one-byte kernel (prefixes of
+// at most kTokChunk tokens) its warps' fp32 copies of them.
 constexpr uint32_t kFlagSameB = 8u;
 
 __device__ __forceinline__ void flag_status(uint32_t* status, uint32_t bits) {
@@ -344,7 +345,11 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
     const int unit_h0 = h;
 
     for (; h < h_end; ++h) {
-      const bool same_B = tc_items && h != unit_h0 && g_left != p.hpg;
+      // B rows reused from the previous item (same unit, same group): the
+      // tensor-core kernel keeps the operand it built; the one-byte kernel
+      // keeps its fp32 B rows when the whole prefix fits one token chunk
+      const bool b_reuse = tc_items || (Q && k > 0 && k <= kTokChunk);
+      const bool same_B = b_reuse && h != unit_h0 && g_left != p.hpg;
       const ItemLayout il = same_B ? il_noB : il_full;
       uint32_t off = 0;
       if (!alloc(il.bytes, off)) {

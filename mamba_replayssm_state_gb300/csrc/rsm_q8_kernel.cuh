@@ -67,6 +67,7 @@ __device__ __forceinline__ void replay_q8(const Params& p, const unsigned char* 
   const int row0 = SLAB * cw + RPT * lr;  // this lane's first tile row
   float* bbuf = cbuf + kTokChunk * 2 * SLAB;
   const uint32_t flags = desc->flags;
+  const bool same_B = (flags & kFlagSameB) != 0u;  // bbuf still holds this item's B rows
   unsigned char* dst_tile = reinterpret_cast<unsigned char*>(desc->dst_state);
   float* dst_sc = reinterpret_cast<float*>(desc->dst_scale);
   const bool dst_aligned = (flags & kFlagDstAligned) != 0u;
@@ -111,7 +112,9 @@ __device__ __forceinline__ void replay_q8(const Params& p, const unsigned char* 
       *reinterpret_cast<float2*>(cbuf + t * 2 * SLAB + 2 * r) = make_float2(c, c);
     }
     // B: lane column l8's 8 columns as two float4 groups, 64 floats apart, so
-    // that eight lanes reading one group read 128 contiguous bytes
+    // that eight lanes reading one group read 128 contiguous bytes.  An item of
+    // the previous item's B group (one chunk) finds its rows already there.
+    if (!same_B)
     for (int u = lane; u < tn * (N / 8); u += 32) {
       const int t = u >> 4, l8 = u & 15;
       float bv[8];
@@ -302,7 +305,7 @@ __device__ __forceinline__ void run_consumer_q8(const Params& p, unsigned char* 
     const uint32_t flags = desc->flags;
     if (flags & kFlagEnd) break;
     const int k = desc->k;
-    const ItemLayout il = item_layout(D, N, 1, true, IE, k);
+    const ItemLayout il = item_layout(D, N, 1, true, IE, k, (flags & kFlagSameB) == 0u);
     arena_head = off + il.bytes;
     const uint32_t empty_bar = empty0 + 8u * stage;
 
