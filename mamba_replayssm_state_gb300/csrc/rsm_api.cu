@@ -235,7 +235,9 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   const bool sr_instance = quant && a->philox_rounds > 0;
   const bool q8 = quant;  // the four-warp one-byte kernel (both rounding modes)
   const int cw = q8 ? rsm::kQ8ConsumerWarps : rsm::kConsumerWarps;
-  const int base = static_cast<int>(use_tc ? rsm::kTcArenaBase : rsm::arena_base(a->dim, a->dstate, sb, cw));
+  const int base = static_cast<int>(use_tc ? rsm::kTcArenaBase
+                                    : q8   ? rsm::kQ8ArenaBase
+                                           : rsm::arena_base(a->dim, a->dstate, sb, cw));
   const int threads = use_tc ? rsm::kTcThreads : 32 * (1 + cw);
   int ctas = q8 ? 3 : 2, arena = 0;
   for (; ctas >= 1; --ctas) {
@@ -321,7 +323,7 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   p.philox_rounds = a->philox_rounds;
   p.num_slots = a->num_slots;
   p.tc_min_k = use_tc ? rsm::kTcMinK : 0;
-  p.desc0 = use_tc ? rsm::kTcDescBase : rsm::desc_base(a->dim, a->dstate, sb, cw);
+  p.desc0 = use_tc ? rsm::kTcDescBase : q8 ? rsm::kQ8DescBase : rsm::desc_base(a->dim, a->dstate, sb, cw);
   p.arena0 = static_cast<uint32_t>(base);
   p.arena_bytes = static_cast<uint32_t>(arena);
   p.stages = static_cast<uint32_t>(stages);

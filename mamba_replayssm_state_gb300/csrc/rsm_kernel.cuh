@@ -126,7 +126,10 @@ __device__ __forceinline__ void load_inputs(const unsigned char* p, float* out) 
 // ---------------------------------------------------------------------------
 // loader warp
 // ---------------------------------------------------------------------------
-template <int SF, int IF, int D, int N>
+// kChunked: long prefixes' ring rows as 16-byte cp.async chunks (the
+// tensor-core kernel, whose windows reach 64 tokens); otherwise every ring row
+// is one bulk copy, which keeps the other kernels' loader small.
+template <int SF, int IF, int D, int N, bool kChunked = false>
 __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem, int lane) {
   constexpr int ES = Fmt<SF>::bytes;
   constexpr int IE = In<IF>::bytes;
@@ -385,7 +388,7 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
         desc->head = h;
       }
       if (aligned) {
-        const bool row_copies = k < kChunkedRingMinK;  // ring rows by bulk copies (see below)
+        const bool row_copies = !kChunked || k < kChunkedRingMinK;  // ring rows by bulk copies (see below)
         if (lane == 0) {
           fence_proxy_async_smem();
           mbar_expect_tx(fullb, kTileBytes + (Q ? D * 4u : 0u) +
@@ -406,14 +409,18 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
         // l % XC of tokens l / XC, then every 32 / XC tokens further; the
         // chunk's ring row follows modulo R.
         if (row_copies) {
-          if (lane < k) {
-            const int64_t xr = static_cast<int64_t>(ring_row[0]) * p.H + h;
-            bulk_g2s(sba + il.off_x + static_cast<uint32_t>(lane) * D * IE, x_slot + xr * (D * IE), D * IE, fullb);
-            if (!same_B)
-              bulk_g2s(sba + il.off_B + static_cast<uint32_t>(lane) * N * IE,
-                       B_slot + (static_cast<int64_t>(ring_row[0]) * G + g) * (N * IE), N * IE, fullb);
+#pragma unroll
+          for (int q = 0; q < (kChunked ? 1 : 2); ++q) {
+            const int t = lane + 32 * q;
+            if (t < k) {
+              const int64_t xr = static_cast<int64_t>(ring_row[q]) * p.H + h;
+              bulk_g2s(sba + il.off_x + static_cast<uint32_t>(t) * D * IE, x_slot + xr * (D * IE), D * IE, fullb);
+              if (!same_B)
+                bulk_g2s(sba + il.off_B + static_cast<uint32_t>(t) * N * IE,
+                         B_slot + (static_cast<int64_t>(ring_row[q]) * G + g) * (N * IE), N * IE, fullb);
+            }
           }
-        } else {
+        } else if constexpr (kChunked) {
           const int x_t0 = lane / XC, x_part = lane % XC;
           int pr = rs + x_t0 - (rs + x_t0 >= p.R ? p.R : 0);
           while (pr >= p.R) pr -= p.R;
@@ -624,7 +631,7 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
   using Raw = typename Vec<SF>::Raw;
   constexpr int XW = SLAB_ROWS % 4 == 0 ? 4 : (SLAB_ROWS % 2 == 0 ? 2 : 1);
   static_assert(RPT == 1 || RPT % 2 == 0, "rows per thread");
-  float* bbuf = cbuf + kTokChunk * 2 * SLAB_ROWS;  // after the (c, c) pairs of kTokChunk tokens
+  float* bbuf = cbuf + kTokChunk * SLAB_ROWS;  // after c of kTokChunk tokens
   const int lane_row = lane / LPR, lane_col = lane % LPR;
   const int slab_row0 = (cw / CT) * SLAB_ROWS;
   const int tile_col0 = (cw % CT) * COLS;
@@ -672,8 +679,10 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
     __syncwarp();  // wbuf visible to the whole warp
 
     // the prefix, kTokChunk tokens at a time: convert this warp's share of
-    // the tokens to fp32 (c = w*x for its rows, each as an (c, c) pair, and B
-    // for its columns), then one rank-1 update per token with packed fp32x2 FMAs
+    // the tokens to fp32 (c = w*x for its rows, B for its columns), then one
+    // rank-1 update per token with packed fp32x2 FMAs.  (c is stored once and
+    // paired in registers: storing (c, c) pairs made the 48-layer bf16 shape
+    // 0.7% slower, 6% at 8 requests.)
     const unsigned char* xs = sb + il.off_x;
     const unsigned char* Bs = sb + il.off_B;
     for (int t0 = 0; t0 < k; t0 += kTokChunk) {
@@ -683,16 +692,13 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
         float xv[XW];
         load_inputs<IF, XW>(xs + ((t0 + t) * D + slab_row0 + rx) * IE, xv);
         const float wt = wbuf[t0 + t];
-        float* dst = cbuf + t * 2 * SLAB_ROWS + 2 * rx;
-#pragma unroll
-        for (int q = 0; q < XW; q += 2) {
-          if constexpr (XW == 1) {
-            const float c0 = xv[0] * wt;
-            *reinterpret_cast<float2*>(dst) = make_float2(c0, c0);
-          } else {
-            const float c0 = xv[q] * wt, c1 = xv[q + 1] * wt;
-            *reinterpret_cast<float4*>(dst + 2 * q) = make_float4(c0, c0, c1, c1);
-          }
+        float* dst = cbuf + t * SLAB_ROWS + rx;
+        if constexpr (XW == 4) {
+          *reinterpret_cast<float4*>(dst) = make_float4(xv[0] * wt, xv[1] * wt, xv[2] * wt, xv[3] * wt);
+        } else if constexpr (XW == 2) {
+          *reinterpret_cast<float2*>(dst) = make_float2(xv[0] * wt, xv[1] * wt);
+        } else {
+          dst[0] = xv[0] * wt;
         }
       }
       for (int u = lane; u < tn * (COLS / 8); u += 32) {
@@ -711,18 +717,24 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
       if (worker) {
 #pragma unroll 2
         for (int t = 0; t < tn; ++t) {
-          float2 c2[RPT];  // (c_r, c_r) for this thread's rows
+          float c[RPT];
           float2 b2[V2];
-          const float* cp = cbuf + t * 2 * SLAB_ROWS + 2 * rrow;
-          if constexpr (RPT == 1) {
-            c2[0] = *reinterpret_cast<const float2*>(cp);
-          } else {
+          const float* cp = cbuf + t * SLAB_ROWS + rrow;
+          if constexpr (RPT % 4 == 0) {
+#pragma unroll
+            for (int r = 0; r < RPT; r += 4) {
+              const float4 v = *reinterpret_cast<const float4*>(cp + r);
+              c[r] = v.x; c[r + 1] = v.y; c[r + 2] = v.z; c[r + 3] = v.w;
+            }
+          } else if constexpr (RPT % 2 == 0) {
 #pragma unroll
             for (int r = 0; r < RPT; r += 2) {
-              const float4 v = *reinterpret_cast<const float4*>(cp + 2 * r);
-              c2[r] = make_float2(v.x, v.y);
-              c2[r + 1] = make_float2(v.z, v.w);
+              const float2 v = *reinterpret_cast<const float2*>(cp + r);
+              c[r] = v.x; c[r + 1] = v.y;
             }
+          } else {
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) c[r] = cp[r];
           }
 #pragma unroll
           for (int g = 0; g < VEC / 4; ++g) {
@@ -733,7 +745,7 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
 #pragma unroll
           for (int r = 0; r < RPT; ++r) {
 #pragma unroll
-            for (int u = 0; u < V2; ++u) acc[r][u] = __ffma2_rn(c2[r], b2[u], acc[r][u]);
+            for (int u = 0; u < V2; ++u) acc[r][u] = __ffma2_rn(make_float2(c[r], c[r]), b2[u], acc[r][u]);
           }
         }
       }

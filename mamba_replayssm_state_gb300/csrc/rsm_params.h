@@ -56,13 +56,11 @@ __host__ __device__ constexpr ThreadLayout thread_layout(int dim, int dstate, in
 }
 
 // fp32 floats in one consumer warp's token-chunk buffer: c = w*x for its
-// slab's rows, each stored twice (an (c, c) pair feeds a packed fp32x2 FMA
-// without a register move), and B for its column tile, kTokChunk tokens each.
+// slab's rows and B for its column tile, kTokChunk tokens each.
 __host__ __device__ constexpr uint32_t warp_buf_floats(int dim, int dstate, int state_bytes,
                                                        int cw = kConsumerWarps) {
-  return static_cast<uint32_t>(kTokChunk *
-                               (2 * thread_layout(dim, dstate, state_bytes, cw).slab_rows +
-                                thread_layout(dim, dstate, state_bytes, cw).cols));
+  return static_cast<uint32_t>(kTokChunk * (thread_layout(dim, dstate, state_bytes, cw).slab_rows +
+                                            thread_layout(dim, dstate, state_bytes, cw).cols));
 }
 
 __host__ __device__ constexpr uint32_t round_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
@@ -78,6 +76,13 @@ __host__ __device__ constexpr uint32_t desc_base(int dim, int dstate, int state_
 __host__ __device__ constexpr uint32_t arena_base(int dim, int dstate, int state_bytes, int cw = kConsumerWarps) {
   return round_up(desc_base(dim, dstate, state_bytes, cw) + kMaxStages * kDescBytes, 128u);
 }
+
+// The one-byte kernel's token buffer: each of its warps owns a 16-row slab,
+// stored as (c, c) pairs (a pair feeds a packed fp32x2 FMA without a register
+// move), and B for all 128 columns, kTokChunk tokens each.
+constexpr uint32_t kQ8WarpBufFloats = kTokChunk * (2 * 16 + 128);
+constexpr uint32_t kQ8DescBase = round_up(kWarpBufOff + kQ8ConsumerWarps * kQ8WarpBufFloats * 4u, 128u);
+constexpr uint32_t kQ8ArenaBase = round_up(kQ8DescBase + kMaxStages * kDescBytes, 128u);
 
 // Byte layout of one work item in the arena: the source tile at offset 0, its
 // scales (one-byte formats), then the item's own k ring rows of x, of B (left

@@ -62,7 +62,7 @@ __device__ __forceinline__ void replay_q8(const Params& p, const unsigned char* 
   constexpr int RPT = 8;            // rows per lane
   constexpr int SLAB = 16;          // rows per warp
   constexpr float qmax = SF == RSM_I8 ? 127.0f : 448.0f;
-  static_assert(warp_buf_floats(D, N, 1, kQ8ConsumerWarps) == kTokChunk * (2 * SLAB + N), "token buffer plan");
+  static_assert(kQ8WarpBufFloats == kTokChunk * (2 * SLAB + N), "token buffer plan");
   const int lr = lane >> 4, lc = lane & 15;
   const int row0 = SLAB * cw + RPT * lr;  // this lane's first tile row
   float* bbuf = cbuf + kTokChunk * 2 * SLAB;
@@ -278,7 +278,7 @@ __device__ __forceinline__ void run_consumer_q8(const Params& p, unsigned char* 
   const uint32_t empty0 = full0 + 8u * kMaxStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
   float* wbuf = reinterpret_cast<float*>(smem + kWeightOff) + cw * kWeightStride;
-  float* cbuf = reinterpret_cast<float*>(smem + kWarpBufOff) + cw * warp_buf_floats(D, N, 1, kQ8ConsumerWarps);
+  float* cbuf = reinterpret_cast<float*>(smem + kWarpBufOff) + cw * kQ8WarpBufFloats;
   const int tid = cw * 32 + lane;  // 0 .. 127
 
   uint32_t key0 = 0, key1 = 0;

@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) materialize_tc_kernel(const __g
     return;
   }
   if (warp == 0) {
-    run_loader<SF, RSM_BF16, 64, 128>(p, smem, lane);
+    run_loader<SF, RSM_BF16, 64, 128, true>(p, smem, lane);
   } else {
     if (warp <= kTcBuilderWarps)
       run_builder_tc<SF>(p, smem, warp - 1, lane, tmem);
