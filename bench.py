@@ -49,6 +49,8 @@ KERNEL_SOURCES = {
         "rsm_kernel.cuh", "rsm_formats.cuh", "rsm_q8_kernel.cuh", "rsm_inst_q8.cu", "rsm_inst_q8sr.cu")],
     "materialize_tc_kernel": _SHARED_SOURCES + [_CSRC + f for f in (
         "rsm_kernel.cuh", "rsm_formats.cuh", "rsm_tc_kernel.cuh", "rsm_tc.cuh", "rsm_inst_tc.cu")],
+    "materialize_q8tc_kernel": _SHARED_SOURCES + [_CSRC + f for f in (
+        "rsm_kernel.cuh", "rsm_formats.cuh", "rsm_q8tc_kernel.cuh", "rsm_tc.cuh", "rsm_inst_q8tc.cu")],
     "gdn_commit_kernel": _SHARED_SOURCES + [_CSRC + f for f in ("gdn_kernel.cuh", "gdn_params.h", "gdn_inst.cu")],
 }
 

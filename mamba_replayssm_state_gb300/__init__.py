@@ -276,7 +276,8 @@ def launch_config(*args, **kwargs) -> dict:
 
 def kernel_name(*args, **kwargs) -> str:
     """Name of the kernel replayssm_materialize launches for these arguments
-    ("materialize_kernel", "materialize_q8_kernel" or "materialize_tc_kernel")."""
+    ("materialize_kernel", "materialize_q8_kernel", "materialize_q8tc_kernel"
+    or "materialize_tc_kernel")."""
     lib = load_library()
     kwargs.pop("stream", None)
     kwargs.pop("dependency_inputs", None)

@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libreplayssm.so")
 SOURCES = ["rsm_api.cu", "rsm_inst_f32.cu", "rsm_inst_bf16.cu", "rsm_inst_f16.cu", "rsm_inst_q8.cu", "rsm_inst_q8sr.cu",
-           "rsm_inst_tc.cu", "gdn_inst.cu"]
+           "rsm_inst_tc.cu", "rsm_inst_q8tc.cu", "gdn_inst.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               "-I", os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]

@@ -87,8 +87,9 @@ constexpr size_t kNumInstances = sizeof(kInstances) / sizeof(kInstances[0]);
 // and the occupancy found for the last size queried (so that calls made while
 // a stream is being captured issue no queries)
 // (indexed by instance; then the two tensor-core variants; then the
-// stochastic-rounding instances of one-byte state, at kNumInstances + 2 + instance)
-constexpr size_t kNumKernels = 2 * kNumInstances + 2;
+// stochastic-rounding instances of one-byte state, at kNumInstances + 2 + instance;
+// then the four one-byte tensor-core instances)
+constexpr size_t kNumKernels = 2 * kNumInstances + 2 + 4;
 int g_smem_set[kMaxDevices][kNumKernels];
 int g_occ_smem[kMaxDevices][kNumKernels];
 int g_occ_blocks[kMaxDevices][kNumKernels];
@@ -202,6 +203,13 @@ bool uses_tensor_cores(const rsm_materialize_args* a) {
          a->dstate == 128 && a->max_window >= rsm::kTcMinWindow;
 }
 
+// One-byte state with bf16 inputs whose B groups hold an even number of heads:
+// the one-byte tensor-core kernel (items of two heads of one group).
+bool uses_q8_tensor_cores(const rsm_materialize_args* a) {
+  return elem_bytes(a->state_dtype) == 1 && a->input_dtype == RSM_BF16 && a->dim == 64 && a->dstate == 128 &&
+         a->heads_per_group % rsm::kQtHeads == 0;
+}
+
 struct Launch {
   const void* fn;
   int grid, threads, smem, stages;
@@ -229,16 +237,22 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   // three for one-byte state (CTAs of four consumer warps), two otherwise;
   // fewer, down to one CTA with the whole shared memory, for long windows.
   const int sb = elem_bytes(a->state_dtype), ib = elem_bytes(a->input_dtype);
-  const int item_min = static_cast<int>(rsm::item_layout(a->dim, a->dstate, sb, quant, ib, 0).bytes);
-  const int item_max = static_cast<int>(rsm::item_layout(a->dim, a->dstate, sb, quant, ib, a->max_window).bytes);
   const bool use_tc = uses_tensor_cores(a);
+  const bool use_qt = uses_q8_tensor_cores(a);  // one-byte state on the tensor cores
+  const int hpi = use_qt ? rsm::kQtHeads : 1;   // heads per work item
+  const int item_min =
+      static_cast<int>(rsm::item_layout(hpi * a->dim, a->dstate, sb, quant, ib, 0, true, hpi).bytes);
+  const int item_max =
+      static_cast<int>(rsm::item_layout(hpi * a->dim, a->dstate, sb, quant, ib, a->max_window, true, hpi).bytes);
   const bool sr_instance = quant && a->philox_rounds > 0;
-  const bool q8 = quant;  // the four-warp one-byte kernel (both rounding modes)
+  const bool q8 = quant && !use_qt;  // the four-warp one-byte kernel (both rounding modes)
   const int cw = q8 ? rsm::kQ8ConsumerWarps : rsm::kConsumerWarps;
   const int base = static_cast<int>(use_tc ? rsm::kTcArenaBase
-                                    : q8   ? rsm::kQ8ArenaBase
-                                           : rsm::arena_base(a->dim, a->dstate, sb, cw));
-  const int threads = use_tc ? rsm::kTcThreads : 32 * (1 + cw);
+                                    : use_qt ? rsm::qt_arena_base(a->max_window)
+                                    : q8     ? rsm::kQ8ArenaBase
+                                             : rsm::arena_base(a->dim, a->dstate, sb, cw));
+  const int threads = use_tc ? rsm::kTcThreads : use_qt ? rsm::kQtThreads : 32 * (1 + cw);
+  // (the one-byte tensor-core kernel: at most two CTAs of 256 TMEM columns per SM)
   int ctas = q8 ? 3 : 2, arena = 0;
   for (; ctas >= 1; --ctas) {
     const int per_cta = ctas == 1 ? di.smem_optin : di.smem_per_sm / ctas - di.smem_reserved;
@@ -249,17 +263,24 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   // Six items in flight per SM (three per CTA at two CTAs per SM): measured
   // on GB300 against two and four per CTA, it is the fastest with replay at
   // every window length (four per CTA is 2% slower on the 48-layer bf16 shape).
-  // One-byte state: four per CTA (its items are half the size).
+  // One-byte state: four per CTA (its items are half the size; two-head items
+  // of the tensor-core kernel are the size of one 16-bit head).
   int stages = arena / item_min;
-  const int stage_cap = q8 ? kQ8SlotsPerCta : kSlotsPerSm / ctas;
+  const int stage_cap = q8 || use_qt ? kQ8SlotsPerCta : kSlotsPerSm / ctas;
   if (stages > stage_cap) stages = stage_cap;
   const int smem = base + arena;
   const bool two = ctas >= 2;
 
-  const void* fn = use_tc ? (a->state_dtype == RSM_BF16 ? rsm::kernel_for_tc<RSM_BF16>() : rsm::kernel_for_tc<RSM_F16>())
-                   : sr_instance ? kInstances[inst].kernel_sr()
-                                 : kInstances[inst].kernel();
+  const bool fp8 = a->state_dtype == RSM_FP8_E4M3;
+  const void* fn =
+      use_tc   ? (a->state_dtype == RSM_BF16 ? rsm::kernel_for_tc<RSM_BF16>() : rsm::kernel_for_tc<RSM_F16>())
+      : use_qt ? (fp8 ? (sr_instance ? rsm::kernel_for_q8tc<RSM_FP8_E4M3, true>()
+                                     : rsm::kernel_for_q8tc<RSM_FP8_E4M3, false>())
+                      : (sr_instance ? rsm::kernel_for_q8tc<RSM_I8, true>() : rsm::kernel_for_q8tc<RSM_I8, false>()))
+      : sr_instance ? kInstances[inst].kernel_sr()
+                    : kInstances[inst].kernel();
   const int ci = use_tc        ? static_cast<int>(kNumInstances) + (a->state_dtype == RSM_F16 ? 1 : 0)
+                 : use_qt      ? static_cast<int>(2 * kNumInstances) + 2 + (fp8 ? 2 : 0) + (sr_instance ? 1 : 0)
                  : sr_instance ? static_cast<int>(kNumInstances) + 2 + inst
                                : inst;
   int per_sm = 0;
@@ -282,12 +303,13 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
       // the SM's 512 TMEM columns.  Two are planned only after checking those
       // limits here; were the second not co-scheduled, the persistent grid
       // would merely take a second wave.
-      if (use_tc && two && per_sm < 2) {
+      if ((use_tc || use_qt) && two && per_sm < 2) {
         int fits = 0;
         e = tc_two_per_sm_fit(fn, threads, smem, di, &fits);
         if (e != cudaSuccess) return fail(RSM_ECUDA, "cudaFuncGetAttributes: %s", cudaGetErrorString(e));
         if (fits) per_sm = 2;
       }
+      if (use_qt && per_sm > 2) per_sm = 2;  // TMEM: 2 x 256 of 512 columns
       g_occ_smem[dev][ci] = smem;
       g_occ_blocks[dev][ci] = per_sm;
     }
@@ -322,8 +344,11 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   p.pad = a->pad_slot_id;
   p.philox_rounds = a->philox_rounds;
   p.num_slots = a->num_slots;
-  p.tc_min_k = use_tc ? rsm::kTcMinK : 0;
-  p.desc0 = use_tc ? rsm::kTcDescBase : q8 ? rsm::kQ8DescBase : rsm::desc_base(a->dim, a->dstate, sb, cw);
+  p.tc_min_k = use_tc ? rsm::kTcMinK : use_qt ? 1 : 0;
+  p.desc0 = use_tc   ? rsm::kTcDescBase
+            : use_qt ? rsm::qt_desc_base(a->max_window)
+            : q8     ? rsm::kQ8DescBase
+                     : rsm::desc_base(a->dim, a->dstate, sb, cw);
   p.arena0 = static_cast<uint32_t>(base);
   p.arena_bytes = static_cast<uint32_t>(arena);
   p.stages = static_cast<uint32_t>(stages);
@@ -502,6 +527,7 @@ int rsm_gdn_commit(const rsm_gdn_commit_args* args, void* stream) {
 const char* rsm_kernel_name(const rsm_materialize_args* args) {
   if (validate(args) < 0) return "";
   if (uses_tensor_cores(args)) return "materialize_tc_kernel";
+  if (uses_q8_tensor_cores(args)) return "materialize_q8tc_kernel";
   return elem_bytes(args->state_dtype) == 1 ? "materialize_q8_kernel" : "materialize_kernel";
 }
 

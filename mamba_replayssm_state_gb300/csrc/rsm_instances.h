@@ -27,4 +27,8 @@ const void* kernel_for_sr();
 // The tensor-core long-window variant (rsm_inst_tc.cu): 16-bit state, bf16 inputs, 64 x 128.
 template <int SF>
 const void* kernel_for_tc();
+// The one-byte tensor-core kernel (rsm_inst_q8tc.cu): int8 / fp8 state, bf16
+// inputs, 64 x 128, items of two heads; SR: Philox stochastic rounding.
+template <int SF, bool SR>
+const void* kernel_for_q8tc();
 }  // namespace rsm

@@ -48,9 +48,9 @@ struct alignas(16) ItemDesc {
   uint32_t flags;
   int32_t layer;
   int32_t dst_slot;
-  int32_t head;
-  float A;                       // A[h]; landed by cp.async
-  uint32_t unused[2];
+  int32_t head;                  // the item's (first) head
+  float A[2];                    // A of the item's heads; landed by cp.async
+  uint32_t unused;
 };
 static_assert(sizeof(ItemDesc) == kDescBytes, "descriptor size");
 constexpr uint32_t kFlagEnd = 1u, kFlagDstAligned = 2u, kFlagScaleAligned = 4u;
@@ -129,18 +129,24 @@ __device__ __forceinline__ void load_inputs(const unsigned char* p, float* out) 
 // kChunked: long prefixes' ring rows as 16-byte cp.async chunks (the
 // tensor-core kernel, whose windows reach 64 tokens); otherwise every ring row
 // is one bulk copy, which keeps the other kernels' loader small.
-template <int SF, int IF, int D, int N, bool kChunked = false>
+// HPI: heads per item (1, or 2 for the one-byte tensor-core kernel, whose
+// items are two consecutive heads of one B group: their tiles, scales and x
+// rows are adjacent in memory, so they move as one tile of 2D rows; dt and A
+// take one value per head).  Requires heads_per_group % HPI == 0.
+template <int SF, int IF, int D, int N, bool kChunked = false, int HPI = 1>
 __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem, int lane) {
   constexpr int ES = Fmt<SF>::bytes;
   constexpr int IE = In<IF>::bytes;
   constexpr bool Q = Fmt<SF>::quant;
-  constexpr uint32_t kTileBytes = D * N * ES;
-  static_assert(kTileBytes % 16 == 0 && (D * IE) % 16 == 0 && (N * IE) % 16 == 0, "bulk copy sizes");
+  constexpr int DI = HPI * D;  // tile rows of one item
+  constexpr uint32_t kTileBytes = DI * N * ES;
+  static_assert(HPI == 1 || HPI == 2, "one or two heads per item");
+  static_assert(kTileBytes % 16 == 0 && (DI * IE) % 16 == 0 && (N * IE) % 16 == 0, "bulk copy sizes");
 
   const uint32_t full0 = smem_addr(smem);
   const uint32_t empty0 = full0 + 8u * kMaxStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
-  constexpr int XC = D * IE / 16, BC = N * IE / 16;  // 16-byte chunks per x row and per B row
+  constexpr int XC = DI * IE / 16, BC = N * IE / 16;  // 16-byte chunks per item x row and per B row
   static_assert(kChunkedRingMinK <= 32, "ring rows by bulk copies: one token per lane");
   static_assert(XC >= 1 && XC <= 32 && 32 % XC == 0 && BC >= 1 && BC <= 32 && 32 % BC == 0, "ring row chunks");
 
@@ -171,11 +177,13 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
   // contiguous ranges would leave the CTAs of long-prefix requests last),
   // while a unit still shares one metadata lookup and a run of B rows.
   // Smaller batches get shorter runs so that every CTA still has ~16 units.
-  const int64_t total = static_cast<int64_t>(n) * p.L * p.H;
+  // (heads counted in items of HPI heads)
+  const int HI = p.H / HPI, hpg_i = p.hpg / HPI;
+  const int64_t total = static_cast<int64_t>(n) * p.L * HI;
   int chunk = static_cast<int>(min(static_cast<int64_t>(32),
                                    max(static_cast<int64_t>(4), total / (16 * static_cast<int64_t>(gridDim.x)))));
-  if (chunk > p.H) chunk = p.H;
-  const int units_per_seg = (p.H + chunk - 1) / chunk;
+  if (chunk > HI) chunk = HI;
+  const int units_per_seg = (HI + chunk - 1) / chunk;
   const int64_t total_units = static_cast<int64_t>(n) * p.L * units_per_seg;
   const int G = p.H / p.hpg;
   const uint64_t policy = l2_policy_evict_first();
@@ -190,7 +198,7 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
   // warp takes the items in order), so freeing is first in, first out.
   // Placement depends on the item sizes alone (arena_next), so the consumers
   // follow it without reading it from the descriptor.
-  const uint32_t item_max = item_layout(D, N, ES, Q, IE, p.W).bytes;
+  const uint32_t item_max = item_layout(DI, N, ES, Q, IE, p.W, true, HPI).bytes;
   uint32_t head = 0, tail = 0, n_out = 0;
   bool wrapped = false;
   uint32_t slot_start = 0;  // lane s: arena offset of the item in slot s
@@ -241,8 +249,8 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
     const int64_t seg = u / units_per_seg;
     const int i = static_cast<int>(seg / p.L);
     const int l = static_cast<int>(seg - static_cast<int64_t>(i) * p.L);
-    int h = static_cast<int>(u - seg * units_per_seg) * chunk;
-    const int h_end = min(p.H, h + chunk);
+    int h = static_cast<int>(u - seg * units_per_seg) * chunk;  // item index: heads h*HPI .. h*HPI+HPI-1
+    const int h_end = min(HI, h + chunk);
 
     // per-layer table entries, one per lane, fetched together
     int64_t tab = 0;
@@ -338,12 +346,12 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
       const int t = lane + 32 * q;
       ring_row[q] = t < k ? (rs + t) % p.R : 0;
     }
-    int g = h / p.hpg;                     // B group of head h, advanced incrementally
-    int g_left = p.hpg - (h - g * p.hpg);  // heads left in group g, h included
+    int g = h * HPI / p.hpg;                         // B group of item h, advanced incrementally
+    int g_left = hpg_i - (h - g * hpg_i);            // items left in group g, h included
     const uint4 desc_tail = make_uint4(static_cast<uint32_t>(k), dst_flags, static_cast<uint32_t>(l),
                                        static_cast<uint32_t>(dst));
-    const ItemLayout il_full = item_layout(D, N, ES, Q, IE, k);
-    const ItemLayout il_noB = item_layout(D, N, ES, Q, IE, k, false);
+    const ItemLayout il_full = item_layout(DI, N, ES, Q, IE, k, true, HPI);
+    const ItemLayout il_noB = item_layout(DI, N, ES, Q, IE, k, false, HPI);
     const bool tc_items = p.tc_min_k > 0 && k >= p.tc_min_k;  // the tensor-core kernel's MMA path
     const int unit_h0 = h;
 
@@ -352,7 +360,7 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
       // tensor-core kernel keeps the operand it built; the one-byte kernel
       // keeps its fp32 B rows when the whole prefix fits one token chunk
       const bool b_reuse = tc_items || (Q && k > 0 && k <= kTokChunk);
-      const bool same_B = b_reuse && h != unit_h0 && g_left != p.hpg;
+      const bool same_B = b_reuse && h != unit_h0 && g_left != hpg_i;
       const ItemLayout il = same_B ? il_noB : il_full;
       uint32_t off = 0;
       if (!alloc(il.bytes, off)) {
@@ -365,16 +373,16 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
       ItemDesc* desc = reinterpret_cast<ItemDesc*>(smem + p.desc0) + stage;
       const uint32_t desca = smem_addr(desc);
 
-      const int64_t tile_off = static_cast<int64_t>(h) * D * N * ES;
+      const int64_t tile_off = static_cast<int64_t>(h) * DI * N * ES;
       const unsigned char* src_tile = src_slot + tile_off;
       unsigned char* dst_tile = dst_slot + tile_off;
       const float* src_sc = nullptr;
       float* dst_sc = nullptr;
       if constexpr (Q) {
-        src_sc = src_sc_slot + static_cast<int64_t>(h) * D;
-        dst_sc = dst_sc_slot + static_cast<int64_t>(h) * D;
+        src_sc = src_sc_slot + static_cast<int64_t>(h) * DI;
+        dst_sc = dst_sc_slot + static_cast<int64_t>(h) * DI;
       }
-      const float* A_ptr = A_base + h;
+      const float* A_ptr = A_base + h * HPI;
       const bool aligned = seg_aligned;
 
       if (lane == 0) {
@@ -385,20 +393,24 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
                            static_cast<uint32_t>(dc >> 32));
         d4[1] = make_uint4(desc_tail.x, desc_tail.y | (same_B ? kFlagSameB : 0u), desc_tail.z,
                            desc_tail.w);  // k, flags, layer, dst_slot
-        desc->head = h;
+        desc->head = h * HPI;
       }
       if (aligned) {
         const bool row_copies = !kChunked || k < kChunkedRingMinK;  // ring rows by bulk copies (see below)
         if (lane == 0) {
           fence_proxy_async_smem();
-          mbar_expect_tx(fullb, kTileBytes + (Q ? D * 4u : 0u) +
-                                    (row_copies ? static_cast<uint32_t>(k) * (D + (same_B ? 0 : N)) * IE : 0u));
+          mbar_expect_tx(fullb, kTileBytes + (Q ? DI * 4u : 0u) +
+                                    (row_copies ? static_cast<uint32_t>(k) * (DI + (same_B ? 0 : N)) * IE : 0u));
         }
         __syncwarp();
         if (lane == 0) {
           bulk_g2s_hint(sba, src_tile, kTileBytes, fullb, policy);
-          if constexpr (Q) bulk_g2s(sba + il.off_scale, src_sc, D * 4u, fullb);
-          if (k > 0) cp_async_4(desca + static_cast<uint32_t>(offsetof(ItemDesc, A)), A_ptr);
+          if constexpr (Q) bulk_g2s(sba + il.off_scale, src_sc, DI * 4u, fullb);
+          if (k > 0) {
+#pragma unroll
+            for (int j = 0; j < HPI; ++j)
+              cp_async_4(desca + static_cast<uint32_t>(offsetof(ItemDesc, A) + 4 * j), A_ptr + j);
+          }
         }
         // Ring rows: up to kChunkedRingMinK tokens, one bulk copy per row by
         // the lanes in parallel.  Longer prefixes as 16-byte cp.async chunks
@@ -413,8 +425,8 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
           for (int q = 0; q < (kChunked ? 1 : 2); ++q) {
             const int t = lane + 32 * q;
             if (t < k) {
-              const int64_t xr = static_cast<int64_t>(ring_row[q]) * p.H + h;
-              bulk_g2s(sba + il.off_x + static_cast<uint32_t>(t) * D * IE, x_slot + xr * (D * IE), D * IE, fullb);
+              const int64_t xr = static_cast<int64_t>(ring_row[q]) * p.H + h * HPI;
+              bulk_g2s(sba + il.off_x + static_cast<uint32_t>(t) * DI * IE, x_slot + xr * (D * IE), DI * IE, fullb);
               if (!same_B)
                 bulk_g2s(sba + il.off_B + static_cast<uint32_t>(t) * N * IE,
                          B_slot + (static_cast<int64_t>(ring_row[q]) * G + g) * (N * IE), N * IE, fullb);
@@ -425,14 +437,14 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
           int pr = rs + x_t0 - (rs + x_t0 >= p.R ? p.R : 0);
           while (pr >= p.R) pr -= p.R;
           const int64_t row_bytes = static_cast<int64_t>(p.H) * (D * IE);
-          const unsigned char* xp = x_slot + static_cast<int64_t>(h) * (D * IE) + 16 * x_part;
+          const unsigned char* xp = x_slot + static_cast<int64_t>(h) * (DI * IE) + 16 * x_part;
           const unsigned char* xq = xp + static_cast<int64_t>(pr) * row_bytes;
           const unsigned char* x_end = xp + static_cast<int64_t>(p.R) * row_bytes;
           const int64_t step = (32 / XC) * row_bytes, wrap = static_cast<int64_t>(p.R) * row_bytes;
-          uint32_t sdst = sba + il.off_x + static_cast<uint32_t>(x_t0 * D * IE + 16 * x_part);
+          uint32_t sdst = sba + il.off_x + static_cast<uint32_t>(x_t0 * DI * IE + 16 * x_part);
           for (int t = x_t0; t < k; t += 32 / XC) {
             cp_async_16(sdst, xq);
-            sdst += (32 / XC) * D * IE;
+            sdst += (32 / XC) * DI * IE;
             xq += step;
             while (xq >= x_end) xq -= wrap;  // rings shorter than the step wrap more than once
           }
@@ -448,39 +460,46 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
             }
           }
         }
-        // dt of this lane's tokens t = lane and t = lane + 32
+        // dt of this lane's tokens t = lane and t = lane + 32 (head j's k values
+        // at off_dt + 4 j k)
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           const int t = lane + 32 * q;
-          if (t < k) cp_async_4(sba + il.off_dt + 4u * t, dt_slot + static_cast<int64_t>(ring_row[q]) * p.H + h);
+          if (t < k) {
+#pragma unroll
+            for (int j = 0; j < HPI; ++j)
+              cp_async_4(sba + il.off_dt + 4u * (j * k + t),
+                         dt_slot + static_cast<int64_t>(ring_row[q]) * p.H + h * HPI + j);
+          }
         }
         cp_async_mbar_arrive(fullb);
       } else {
         // any alignment: plain byte copies by the whole warp
         copy_bytes_warp(sb, src_tile, kTileBytes, lane);
         if constexpr (Q)
-          copy_bytes_warp(sb + il.off_scale, reinterpret_cast<const unsigned char*>(src_sc), D * 4u, lane);
+          copy_bytes_warp(sb + il.off_scale, reinterpret_cast<const unsigned char*>(src_sc), DI * 4u, lane);
         for (int t = 0; t < k; ++t) {
           const int pr = (rs + t) % p.R;
-          copy_bytes_warp(sb + il.off_x + t * D * IE, x_slot + (static_cast<int64_t>(pr) * p.H + h) * D * IE,
-                          D * IE, lane);
+          copy_bytes_warp(sb + il.off_x + t * DI * IE,
+                          x_slot + (static_cast<int64_t>(pr) * p.H + h * HPI) * D * IE, DI * IE, lane);
           if (!same_B)
             copy_bytes_warp(sb + il.off_B + t * N * IE, B_slot + (static_cast<int64_t>(pr) * G + g) * N * IE,
                             N * IE, lane);
-          copy_bytes_warp(sb + il.off_dt + 4 * t,
-                          reinterpret_cast<const unsigned char*>(dt_slot + static_cast<int64_t>(pr) * p.H + h), 4,
-                          lane);
+          for (int j = 0; j < HPI; ++j)
+            copy_bytes_warp(sb + il.off_dt + 4 * (j * k + t),
+                            reinterpret_cast<const unsigned char*>(dt_slot + static_cast<int64_t>(pr) * p.H + h * HPI + j),
+                            4, lane);
         }
         if (k > 0)
           copy_bytes_warp(reinterpret_cast<unsigned char*>(desc) + offsetof(ItemDesc, A),
-                          reinterpret_cast<const unsigned char*>(A_ptr), 4, lane);
+                          reinterpret_cast<const unsigned char*>(A_ptr), 4 * HPI, lane);
         __threadfence_block();
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(fullb);
       if (--g_left == 0) {
         ++g;
-        g_left = p.hpg;
+        g_left = hpg_i;
       }
       // the item now occupies [off, off + il.bytes) of the arena, in slot `stage`
       if (lane == static_cast<int>(stage)) slot_start = off;
@@ -570,6 +589,22 @@ __device__ __forceinline__ float decay_scan(const float* dts, float A, int k, in
   return p1 * __shfl_sync(0xFFFFFFFFu, i0, 0);
 }
 
+// (Tensor-core kernels.)  Sets the abort flag and the status bit (lane 0), so that the other warps
+// leave at their next wait.
+__device__ __forceinline__ void tc_give_up(const Params& p, volatile int* abort_flag, int lane) {
+  if (lane == 0) {
+    *abort_flag = 1;
+    flag_status(p.status, RSM_STATUS_WAIT_TIMEOUT);
+  }
+}
+
+// Waits for the phase of parity `parity` of `bar` (bounded) with the whole
+// warp agreeing on the outcome; false on time-out or abort.
+__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  const bool ok = mbar_wait(bar, parity, kWaitTimeoutNs) && !*abort_flag;
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // Byte-wise store of a vector to a destination that is not 16-byte aligned
 // (out of line: the aligned path is the one every ordinary call runs).
 static __device__ __noinline__ void store_bytes(unsigned char* dst, uint4 v) {
@@ -654,7 +689,7 @@ __device__ __forceinline__ void replay_ffma(const Params& p, const unsigned char
   };
     // decay of each token, once per warp: a_t = exp(dt_t*A), then
     // w_t = dt_t * prod_{s>t} a_s and P = prod_t a_t by a suffix-product scan
-    const float P = decay_scan(reinterpret_cast<const float*>(sb + il.off_dt), desc->A, k, lane, wbuf);
+    const float P = decay_scan(reinterpret_cast<const float*>(sb + il.off_dt), desc->A[0], k, lane, wbuf);
 
     // this thread's [RPT rows x VEC columns] of the tile, dequantized, times P
     float2 acc[RPT][V2];

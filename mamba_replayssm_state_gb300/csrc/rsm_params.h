@@ -86,20 +86,23 @@ constexpr uint32_t kQ8ArenaBase = round_up(kQ8DescBase + kMaxStages * kDescBytes
 
 // Byte layout of one work item in the arena: the source tile at offset 0, its
 // scales (one-byte formats), then the item's own k ring rows of x, of B (left
-// out for a tensor-core item that reuses the previous item's B) and its k dt
-// values.  Every part starts on a 16-byte boundary (D*N*ES, D*IE and
-// N*IE are multiples of 16); items start on 128-byte boundaries.
+// out for an item that reuses the previous item's B) and its k dt values per
+// head (`heads` > 1: an item of consecutive heads, whose tiles, scales and x
+// rows are adjacent and counted in `dim`; head j's dt at off_dt + 4 j k).
+// Every part starts on a 16-byte boundary (D*N*ES, D*IE and N*IE are
+// multiples of 16); items start on 128-byte boundaries.
 struct ItemLayout {
   uint32_t off_scale, off_x, off_B, off_dt, bytes;
 };
 
 __host__ __device__ constexpr ItemLayout item_layout(int dim, int dstate, int state_bytes, bool quant, int in_bytes,
-                                                     int k, bool with_B = true) {
+                                                     int k, bool with_B = true, int heads = 1) {
   const uint32_t off_scale = static_cast<uint32_t>(dim * dstate * state_bytes);
   const uint32_t off_x = off_scale + (quant ? static_cast<uint32_t>(dim) * 4u : 0u);
   const uint32_t off_B = off_x + static_cast<uint32_t>(k * dim * in_bytes);
   const uint32_t off_dt = off_B + (with_B ? static_cast<uint32_t>(k * dstate * in_bytes) : 0u);
-  return ItemLayout{off_scale, off_x, off_B, off_dt, round_up(off_dt + 4u * static_cast<uint32_t>(k), 128u)};
+  return ItemLayout{off_scale, off_x, off_B, off_dt,
+                    round_up(off_dt + 4u * static_cast<uint32_t>(k * heads), 128u)};
 }
 
 // Arena offset of the next item, given where the previous one ended (`head`):
@@ -146,6 +149,43 @@ constexpr uint32_t kTcTmemCols = 2 * kTcAccCols;  // two accumulators
 constexpr uint32_t kTcDescBase = round_up(kTcAOff + 128 * kTcKMax * 2, 128u);
 constexpr uint32_t kTcArenaBase = round_up(kTcDescBase + kMaxStages * kDescBytes, 128u);
 constexpr int kTcMinK = 1;  // every prefix of one token or more goes through the MMA
+
+// The one-byte tensor-core kernel (rsm_q8tc_kernel.cuh): items of two heads
+// of one B group (HPI = 2), the replay sum_t w_t x_t B_t^T as MMAs of M = 128
+// (two heads x 64 dim rows) x N = 128 (dstate) x K = 16 tokens.  CTA: the
+// loader warp, two builder warps (one per head of the item) and four epilogue
+// warps (one per TMEM lane quarter, a thread per tile row).  Two accumulators
+// of 128 columns.
+constexpr int kQtHeads = 2;
+constexpr int kQtBuilderWarps = 2;
+constexpr int kQtEpilogueWarps = 4;
+constexpr int kQtConsumerWarps = kQtBuilderWarps + kQtEpilogueWarps;
+constexpr int kQtThreads = 32 * (1 + kQtConsumerWarps);
+constexpr int kQtMaxRegs = 128;  // 14 warps per SM at two CTAs: four on three sub-partitions, 4 x 32 x 128 = 16384
+constexpr uint32_t kQtMmaDone = kWarpBufOff;       // [2] an accumulator's MMAs completed (1 arrival: commit)
+constexpr uint32_t kQtTmemFree = kWarpBufOff + 16; // [2] the epilogue is done with an accumulator (kQtEpilogueWarps)
+constexpr uint32_t kQtBuildBar = kWarpBufOff + 32; // the builders' operands are written (kQtBuilderWarps)
+constexpr uint32_t kQtExitBar = kWarpBufOff + 40;  // every consumer warp is done with TMEM (kQtConsumerWarps)
+constexpr uint32_t kQtTmemSlot = kWarpBufOff + 48; // TMEM base address written by tcgen05.alloc
+constexpr uint32_t kQtAccCols = 128;               // one fp32 accumulator: 128 lanes x 128 columns
+constexpr uint32_t kQtTmemCols = 2 * kQtAccCols;
+constexpr uint32_t kQtOpOff = 4096;                // operands from here, 1024-byte aligned
+constexpr uint32_t kQtGroup = 2048;                // bytes between token groups of 8 rows (two atom columns)
+constexpr uint32_t kQtStageBytes = 32 * 128;       // one epilogue warp's store staging: 32 rows x 128 codes
+static_assert(kQtMmaDone + 64 <= kQtOpOff && kWeightOff + kQtBuilderWarps * kWeightStride * 4 <= kWarpBufOff,
+              "one-byte tensor-core smem head");
+// tokens of one item's MMAs (the window rounded up to whole MMAs of 16)
+__host__ __device__ constexpr uint32_t qt_kpad(int window) { return round_up(static_cast<uint32_t>(window), 16u); }
+// bytes of one operand: 128 rows (MN) x kpad tokens of bf16, a multiple of 4096
+__host__ __device__ constexpr uint32_t qt_op_bytes(int window) { return 128u * qt_kpad(window) * 2u; }
+// [C hi | C lo | B] operands, then the epilogue warps' staging, the descriptors and the arena
+__host__ __device__ constexpr uint32_t qt_stage_off(int window) { return kQtOpOff + 3u * qt_op_bytes(window); }
+__host__ __device__ constexpr uint32_t qt_desc_base(int window) {
+  return qt_stage_off(window) + kQtEpilogueWarps * kQtStageBytes;
+}
+__host__ __device__ constexpr uint32_t qt_arena_base(int window) {
+  return round_up(qt_desc_base(window) + kMaxStages * kDescBytes, 128u);
+}
 
 struct Params {
   const int64_t* state_ptrs;

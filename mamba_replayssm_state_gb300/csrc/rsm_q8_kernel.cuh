@@ -76,7 +76,7 @@ __device__ __forceinline__ void replay_q8(const Params& p, const unsigned char* 
   const uint32_t layer_id = static_cast<uint32_t>(desc->layer);
   const int head = desc->head;
 
-  const float P = decay_scan(reinterpret_cast<const float*>(sb + il.off_dt), desc->A, k, lane, wbuf);
+  const float P = decay_scan(reinterpret_cast<const float*>(sb + il.off_dt), desc->A[0], k, lane, wbuf);
 
   // this lane's 8 x 8 codes, decoded and multiplied by scale * P
   float2 acc[RPT][4];

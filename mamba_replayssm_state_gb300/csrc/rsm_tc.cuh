@@ -1,7 +1,7 @@
 // rsm_tc.cuh -- the sm_100/sm_103 tensor-core operations of the long-window
-// kernel, as hand-written PTX: tensor-memory (TMEM) allocation, tcgen05.mma
+// kernels, as hand-written PTX: tensor-memory (TMEM) allocation, tcgen05.mma
 // with both operands in shared memory and the accumulator in TMEM, its commit
-// to an mbarrier, and the TMEM -> register load.
+// to an mbarrier, and the TMEM <-> register loads and stores.
 #pragma once
 #include <cstdint>
 
@@ -102,6 +102,23 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
   for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(r[c]);
 }
+
+// 32 consecutive fp32 columns into this thread's TMEM lane (shape 32x32b,
+// .x32).  Whole warp.  The store is complete only after tmem_st_wait().
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]),
+      "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]),
+      "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]),
+      "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+
+// Waits until this thread's earlier tcgen05.st have completed.  Whole warp.
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Streaming 2-byte store: one element of a 16-bit state tile (a warp's 32
 // lanes write 64 contiguous bytes of a tile row).

@@ -100,22 +100,6 @@ __device__ __noinline__ void tc_epilogue_general(int philox_rounds, uint32_t tad
   }
 }
 
-// Sets the abort flag and the status bit (lane 0), so that the other warps
-// leave at their next wait.
-__device__ __forceinline__ void tc_give_up(const Params& p, volatile int* abort_flag, int lane) {
-  if (lane == 0) {
-    *abort_flag = 1;
-    flag_status(p.status, RSM_STATUS_WAIT_TIMEOUT);
-  }
-}
-
-// Waits for the phase of parity `parity` of `bar` (bounded) with the whole
-// warp agreeing on the outcome; false on time-out or abort.
-__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  const bool ok = mbar_wait(bar, parity, kWaitTimeoutNs) && !*abort_flag;
-  return __all_sync(0xFFFFFFFFu, ok);
-}
-
 template <int SF>
 __device__ __forceinline__ void run_builder_tc(const Params& p, unsigned char* smem, int bw, int lane, uint32_t tmem) {
   constexpr int D = 64, N = 128, ES = 2, IE = 2;
@@ -157,7 +141,7 @@ __device__ __forceinline__ void run_builder_tc(const Params& p, unsigned char* s
       continue;
     }
     // decay weights w_t of the item's tokens, once per warp
-    (void)decay_scan(reinterpret_cast<const float*>(sb + il.off_dt), desc->A, k, lane, wbuf);
+    (void)decay_scan(reinterpret_cast<const float*>(sb + il.off_dt), desc->A[0], k, lane, wbuf);
     __syncwarp();  // wbuf visible to the whole warp
     // the operands are free once the previous item's MMAs have completed
     if (n_tc > 0 && !tc_wait(sbase + kTcMmaDone + 8u * ((n_tc - 1) & 1u), ((n_tc - 1) >> 1) & 1u, abort_flag)) {
@@ -294,7 +278,7 @@ __device__ __forceinline__ void run_epilogue_tc(const Params& p, unsigned char* 
     const int h = desc->head;
     const uint32_t dst_slot_id = static_cast<uint32_t>(desc->dst_slot);
     const uint32_t layer_id = static_cast<uint32_t>(desc->layer);
-    const float P = decay_scan(reinterpret_cast<const float*>(sb + il.off_dt), desc->A, k, lane, wbuf);
+    const float P = decay_scan(reinterpret_cast<const float*>(sb + il.off_dt), desc->A[0], k, lane, wbuf);
     const uint32_t buf = n_tc & 1u;
     const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + buf * kTcAccCols;
     unsigned char* out_col = dst_tile + static_cast<uint32_t>(j) * 2u;

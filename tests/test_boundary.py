@@ -180,10 +180,11 @@ def test_gdn_empty_batch_enqueues_nothing(lib):
 
 def test_kernel_name_follows_the_launch_rule(lib):
     """rsm_kernel_name needs no GPU: the CUDA-core kernel for the 8-token
-    headline shape and fp32 state, the one-byte kernel for int8 and fp8 state,
-    the tensor-core kernel for 16-bit state with bf16 inputs at 64 x 128 once
-    max_window reaches 16, and "" (with the reason) when the arguments fail
-    validation."""
+    headline shape and fp32 state, the tensor-core kernel for 16-bit state with
+    bf16 inputs at 64 x 128 once max_window reaches 16, for int8 and fp8 state
+    the one-byte tensor-core kernel when the inputs are bf16 and a B group has
+    an even number of heads and the one-byte kernel otherwise, and "" (with
+    the reason) when the arguments fail validation."""
     a = good_args()
     assert lib.rsm_kernel_name(ctypes.byref(a)) == b"materialize_kernel"
     a.max_window = a.ring_buffer_len = 64
@@ -193,9 +194,17 @@ def test_kernel_name_follows_the_launch_rule(lib):
     a.state_dtype = rsm.RSM_F32
     assert lib.rsm_kernel_name(ctypes.byref(a)) == b"materialize_kernel"
     a.state_scale_ptrs = a.state_scale_slot_strides = 0x1000
+    assert a.input_dtype == rsm.RSM_BF16 and a.heads_per_group % 2 == 0
     for sd in (rsm.RSM_I8, rsm.RSM_FP8_E4M3):
         a.state_dtype = sd
+        assert lib.rsm_kernel_name(ctypes.byref(a)) == b"materialize_q8tc_kernel"
+        a.input_dtype = rsm.RSM_F32
         assert lib.rsm_kernel_name(ctypes.byref(a)) == b"materialize_q8_kernel"
+        a.input_dtype = rsm.RSM_BF16
+        hpg = a.heads_per_group
+        a.heads_per_group = 1
+        assert lib.rsm_kernel_name(ctypes.byref(a)) == b"materialize_q8_kernel"
+        a.heads_per_group = hpg
     a.heads_per_group = 33
     assert lib.rsm_kernel_name(ctypes.byref(a)) == b""
     assert b"heads_per_group" in lib.rsm_last_error()

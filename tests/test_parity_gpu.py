@@ -677,3 +677,67 @@ def test_tensor_core_empty_active_list_writes_nothing():
     got = run_cuda(hw)
     for l in range(hw.L):
         assert got.state[l].tobytes() == hw.state[l].tobytes()
+
+
+# ----------------------------------------------------------------------------
+# one-byte state on the tensor cores (int8 / fp8 state, bf16 inputs, an even
+# number of heads per B group: items of two heads, the replay as MMAs)
+# ----------------------------------------------------------------------------
+
+def _q8tc_world(shape, seed):
+    hw = wl.host_world(shape, seed=seed)
+    assert rsm.kernel_name(**wl.device_world_from_host(hw).call_kwargs()) == "materialize_q8tc_kernel"
+    return hw
+
+
+@pytest.mark.parametrize("sd", ["i8", "fp8_e4m3"])
+@pytest.mark.parametrize("k", [1, 5, 8, 15, 16, 17, 33, 64])
+def test_one_byte_tensor_core_prefix_lengths(sd, k):
+    """Whole MMAs (16, 64), ragged last ones and a single token, with ring wrap."""
+    shape = wl.Shape("q8tc", L=2, Bt=4, H=8, hpg=4, D=64, N=128, R=64, W=64, state_dtype=sd, n_active=4,
+                     ring_start=(0, 64), prefix=("fixed", k))
+    check(_q8tc_world(shape, seed=500 + k))
+
+
+@pytest.mark.parametrize("sd", ["i8", "fp8_e4m3"])
+@pytest.mark.parametrize("rounds", [0, 10])
+def test_one_byte_tensor_core_mixed_prefixes_many_units_per_cta(sd, rounds):
+    """Prefixes U[0,8] over several (request, layer, head-run) units per CTA:
+    copies and replays follow one another, items alternate between the two
+    accumulators, and the B operand is reused along each B group."""
+    shape = wl.Shape("q8tcmix", L=2, Bt=48, H=32, hpg=8, D=64, N=128, R=8, W=8, state_dtype=sd, n_active=44,
+                     prefix=("uniform", 0, 8), pad_frac=0.05, philox_rounds=rounds, rand_seed=0xC0FFEE)
+    hw = _q8tc_world(shape, seed=92)
+    for i in (2, 11):  # two exact copies among them
+        hw.replay_prefix_len[int(hw.active[i])] = 0
+    assert check(hw) >= 60
+
+
+@pytest.mark.parametrize("sd", ["i8", "fp8_e4m3"])
+def test_one_byte_tensor_core_misaligned_state(sd):
+    """Codes one byte off a 16-byte boundary: the loader copies the tiles
+    byte-wise and the epilogue writes them with byte stores."""
+    shape = wl.Shape("q8tcmis", L=1, Bt=3, H=4, hpg=2, D=64, N=128, R=8, W=8, state_dtype=sd, n_active=3)
+    hw = _q8tc_world(shape, seed=25)
+    dw = wl.device_world_from_host(hw)
+    buf = torch.zeros(hw.state[0].size + 1, dtype=torch.uint8, device="cuda")
+    view = buf[1:].view(hw.state[0].shape)
+    view.copy_(torch.from_numpy(hw.state[0].view(np.uint8)))
+    dw.state[0] = view
+    dw.tables = wl._tables(dw.state, dw.scale, dw.x, dw.B, dw.dt, dw.A, "cuda")
+    assert dw.state[0].data_ptr() % 16 == 1
+    rsm.replayssm_materialize(**dw.call_kwargs())
+    torch.cuda.synchronize()
+    got = hw.copy()
+    got.state = [wl._to_np(t).view(a.dtype) for t, a in zip(dw.state, hw.state)]
+    got.scale = [wl._to_np(t) for t in dw.scale]
+    compare_worlds(got, run_oracle(hw), hw)
+
+
+@pytest.mark.parametrize("sd", ["i8", "fp8_e4m3"])
+def test_one_byte_tensor_core_in_place_commit(sd):
+    shape = wl.Shape("q8tcinplace", L=2, Bt=5, H=6, hpg=2, D=64, N=128, R=8, W=8, state_dtype=sd, n_active=4,
+                     philox_rounds=10 if sd == "fp8_e4m3" else 0, rand_seed=5)
+    hw = _q8tc_world(shape, seed=72)
+    hw.dst_slots[:] = hw.src_slots
+    assert check(hw) >= 4
