@@ -58,14 +58,12 @@ __device__ __forceinline__ uint32_t qt_swz(int r, int c) {
   return static_cast<uint32_t>(r * 128 + (((c ^ r) & 7) << 4));
 }
 
-// fl(fl(a * b) + c) for two fp32 pairs: the product is rounded before the
-// add (the decode rounds code * (scale P) before the replay is added, as the
-// CUDA-core kernels do).  The products are scalar __fmul_rn, which is never
-// merged into a fused multiply-add; a packed fp32x2 multiply followed by a
-// packed add was (measured on GB300: the sums came out rounded once, even
-// with both written as explicit-rounding PTX).
-__device__ __forceinline__ float2 mul_add2_rn(float2 a, float2 b, float2 c) {
-  return __fadd2_rn(make_float2(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y)), c);
+// max(m, |a|, |b|) in one instruction (sm_100 three-input maximum of
+// absolute values); a NaN operand is ignored, as by fmaxf
+__device__ __forceinline__ float absmax3(float m, float a, float b) {
+  float r;
+  asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(m), "f"(a), "f"(b));
+  return r;
 }
 
 template <int SF>
@@ -85,6 +83,11 @@ __device__ __forceinline__ void run_builder_qt(const Params& p, unsigned char* s
   uint32_t arena_head = 0;
   uint32_t stage = 0, phase = 0;
   uint32_t n_tc = 0;  // items with a replay so far
+  // C rows (tokens) t >= c_dirty are zero in both C operands: rows k .. kp-1
+  // of an item must be zero (or at least finite: B's are zero), so only rows
+  // that an earlier, longer item wrote are cleared.  Nothing is known at the
+  // start (the shared memory holds anything).
+  int c_dirty = static_cast<int>(qt_kpad(p.W));
   for (;;) {
     if (!tc_wait(full0 + 8u * stage, phase, abort_flag)) {
       tc_give_up(p, abort_flag, lane);
@@ -121,8 +124,12 @@ __device__ __forceinline__ void run_builder_qt(const Params& p, unsigned char* s
     // token t's row of an operand: 16 chunks of 8 bf16 along MN; chunk c is in
     // atom column c / 8 of token group t / 8, at chunk (c % 8) ^ (t % 8) of the
     // atom's row t % 8.  This warp writes chunks 8 bw .. 8 bw + 7: its head's
-    // 64 rows of C, and half of B's columns.
-    for (int u = lane; u < kp * 8; u += 32) {
+    // 64 rows of C (rows k .. c_dirty-1 cleared), and half of B's columns
+    // (rows k .. kp-1 zero).
+    const int c_rows = max(k, min(c_dirty, kp));
+    const int rows = same_B ? c_rows : kp;
+    c_dirty = c_dirty > kp ? c_dirty : k;
+    for (int u = lane; u < rows * 8; u += 32) {
       const int t = u >> 3, c = 8 * bw + (u & 7);
       const uint32_t o = static_cast<uint32_t>((t >> 3) * kQtGroup + (c >> 3) * 1024 + (t & 7) * 128 +
                                                (((c & 7) ^ (t & 7)) << 4));
@@ -142,8 +149,10 @@ __device__ __forceinline__ void run_builder_qt(const Params& p, unsigned char* s
         hi = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         lo = make_uint4(lw[0], lw[1], lw[2], lw[3]);
       }
-      *reinterpret_cast<uint4*>(chi + o) = hi;
-      *reinterpret_cast<uint4*>(clo + o) = lo;
+      if (t < c_rows) {
+        *reinterpret_cast<uint4*>(chi + o) = hi;
+        *reinterpret_cast<uint4*>(clo + o) = lo;
+      }
       if (!same_B) {
         const uint4 bv = t < k ? *reinterpret_cast<const uint4*>(sb + il.off_B + t * (N * 2) + c * 16)
                                : make_uint4(0u, 0u, 0u, 0u);
@@ -196,15 +205,16 @@ __device__ __forceinline__ void run_builder_qt(const Params& p, unsigned char* s
     (void)mbar_wait(sbase + kQtMmaDone + 8u * ((n_tc - 1) & 1u), ((n_tc - 1) >> 1) & 1u, kWaitTimeoutNs);
 }
 
-// Requantizes 32 consecutive values of a row (already times qmax/amax for the
-// nearest-rounding path: `inv` multiplies here) into 8 words of codes.
-// Stochastic rounding: Philox counters c0 and c0 + 1 cover columns 0-15 and
-// 16-31 of the 32; word q of a call rounds its columns 4q .. 4q + 3.
+// Requantizes 32 consecutive values of a row, times inv = qmax / amax, into 8
+// words of codes.  Stochastic rounding: Philox counters c0 and c0 + 1 cover
+// columns 0-15 and 16-31 of the 32; word q of a call rounds its columns
+// 4q .. 4q + 3.  fp8 values are v * inv + 0, so that a row quantized with
+// inv = 0 gets +0 codes even where v is negative.
 template <int SF, bool SR>
 __device__ __forceinline__ void qt_quantize32(const float (&a)[32], float inv, uint32_t c0, uint32_t dst_slot_id,
                                               uint32_t layer_id, uint32_t key0, uint32_t key1, int rounds,
                                               uint32_t (&w)[8]) {
-  const float2 inv2 = make_float2(inv, inv);
+  const float2 inv2 = make_float2(inv, inv), zero2 = make_float2(0.0f, 0.0f);
   if constexpr (SR) {
     uint4 rw[2] = {make_uint4(c0, dst_slot_id, layer_id, 0u), make_uint4(c0 + 1u, dst_slot_id, layer_id, 0u)};
     philox4x32_n<2>(rw, key0, key1, rounds);
@@ -214,8 +224,8 @@ __device__ __forceinline__ void qt_quantize32(const float (&a)[32], float inv, u
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int e = 16 * g + 4 * q;
-        const float2 v01 = __fmul2_rn(make_float2(a[e], a[e + 1]), inv2);
-        const float2 v23 = __fmul2_rn(make_float2(a[e + 2], a[e + 3]), inv2);
+        const float2 v01 = __ffma2_rn(make_float2(a[e], a[e + 1]), inv2, zero2);
+        const float2 v23 = __ffma2_rn(make_float2(a[e + 2], a[e + 3]), inv2, zero2);
         if constexpr (SF == RSM_I8) {
           uint32_t r[4];
           sr_r16x4(words[q], r);
@@ -242,8 +252,8 @@ __device__ __forceinline__ void qt_quantize32(const float (&a)[32], float inv, u
         w[q] = __byte_perm(__byte_perm(__float_as_uint(c01.x), __float_as_uint(c01.y), 0x0040u),
                            __byte_perm(__float_as_uint(c23.x), __float_as_uint(c23.y), 0x0040u), 0x5410u);
       } else {
-        const float2 v01 = __fmul2_rn(make_float2(a[e], a[e + 1]), inv2);
-        const float2 v23 = __fmul2_rn(make_float2(a[e + 2], a[e + 3]), inv2);
+        const float2 v01 = __ffma2_rn(make_float2(a[e], a[e + 1]), inv2, zero2);
+        const float2 v23 = __ffma2_rn(make_float2(a[e + 2], a[e + 3]), inv2, zero2);
         w[q] = __byte_perm(f32x2_to_e4m3x2(v01.x, v01.y), f32x2_to_e4m3x2(v23.x, v23.y), 0x5410u);
       }
     }
@@ -341,7 +351,7 @@ __device__ __forceinline__ void run_epilogue_qt(const Params& p, unsigned char* 
       for (int o = 16; o > 0; o >>= 1) a *= __shfl_xor_sync(0xFFFFFFFFu, a, o);
       P = a;
     }
-    const float sp = reinterpret_cast<const float*>(sb + il.off_scale)[m] * P;
+    const float sc = reinterpret_cast<const float*>(sb + il.off_scale)[m];
     // this warp's 32 rows of codes, read four rows at a time (coalesced) into
     // the staging buffer, swizzled: from there each thread reads its own row
     // without bank conflicts, and writes its codes back in the same place
@@ -363,11 +373,11 @@ __device__ __forceinline__ void run_epilogue_qt(const Params& p, unsigned char* 
       break;
     }
     tc_fence_after();
-    // S = fl(code * (scale P)) + acc, one fp32 rounding each, back into TMEM,
-    // and the row's amax
+    // S = fl(P S_0 + acc) with S_0 = fl(code * scale), the decoded state, back
+    // into TMEM, and the row's amax
     float am = 0.0f;
     {
-      const float2 sp2 = make_float2(sp, sp);
+      const float2 sc2 = make_float2(sc, sc), P2 = make_float2(P, P);
 #pragma unroll
       for (int c2 = 0; c2 < 4; ++c2) {
         float a[32];
@@ -381,31 +391,31 @@ __device__ __forceinline__ void run_epilogue_qt(const Params& p, unsigned char* 
           unpack_words<SF, 1>(code + q, f);
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const float2 y = mul_add2_rn(make_float2(f[2 * u], f[2 * u + 1]), sp2,
-                                         make_float2(a[4 * q + 2 * u], a[4 * q + 2 * u + 1]));
+            const float2 y = __ffma2_rn(__fmul2_rn(make_float2(f[2 * u], f[2 * u + 1]), sc2), P2,
+                                        make_float2(a[4 * q + 2 * u], a[4 * q + 2 * u + 1]));
             a[4 * q + 2 * u] = y.x;
             a[4 * q + 2 * u + 1] = y.y;
           }
         }
 #pragma unroll
-        for (int u = 0; u < 32; u += 2) am = fmaxf(am, fmaxf(fabsf(a[u]), fabsf(a[u + 1])));
+        for (int u = 0; u < 32; u += 2) am = absmax3(am, a[u], a[u + 1]);
         tmem_st32(taddr + 32u * c2, a);
       }
       tmem_st_wait();
     }
-    const float inv = __fdiv_rn(qmax, am);
-    const bool finite = inv <= FLT_MAX;  // else amax is 0 or tiny: zero codes, scale 0
+    // a row whose qmax / amax is not finite (amax 0 or tiny) gets scale 0 and
+    // zero codes: it is quantized with inv = 0 (its values are all finite and
+    // tiny, so every product is 0)
+    float inv = __fdiv_rn(qmax, am);
+    const bool finite = inv <= FLT_MAX;
     const float scale = finite ? __fdiv_rn(am, qmax) : 0.0f;
+    if (!finite) inv = 0.0f;
 #pragma unroll
     for (int c2 = 0; c2 < 4; ++c2) {
       float a[32];
       tmem_ld32(taddr + 32u * c2, a);
       uint32_t w[8];
       qt_quantize32<SF, SR>(a, inv, row_ctr + 2u * c2, dst_slot_id, layer_id, key0, key1, p.philox_rounds, w);
-      if (!finite) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) w[q] = 0u;
-      }
       *reinterpret_cast<uint4*>(stg + qt_swz(lane, 2 * c2)) = make_uint4(w[0], w[1], w[2], w[3]);
       *reinterpret_cast<uint4*>(stg + qt_swz(lane, 2 * c2 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
     }
