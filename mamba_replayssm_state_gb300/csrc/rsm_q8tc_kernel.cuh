@@ -32,11 +32,11 @@
 //     into accumulator n mod 2 once the epilogue has handed it back, and
 //     commits them to that accumulator's mbarrier.
 //   epilogue warp q (TMEM lane quarter q, tile rows 32q .. 32q + 31; a thread
-//     per row): the warp's 32 rows of codes, read coalesced and passed through
-//     a swizzled staging buffer so that each thread then reads its own row
-//     without bank conflicts, into registers (32 words); the slot goes back to
-//     the loader.  Once the MMAs are done: S = fl(code * (scale P)) + acc,
-//     added in fp32 with one rounding as on the CUDA cores, written back to
+//     per row): the warp's 32 rows of codes, read coalesced into a swizzled
+//     staging buffer, from which each thread then reads its own row without
+//     bank conflicts; the slot goes back to the loader.  Once the MMAs are
+//     done: S = fl(code * (scale P) + acc), one fma (the decoded state
+//     code * scale, decayed, plus the replay, rounded once), written back to
 //     TMEM while the row's amax is taken, then read again, requantized (round
 //     to nearest even, or Philox stochastic rounding), and stored through the
 //     staging buffer as coalesced 16-byte vectors; the accumulator goes back
@@ -373,11 +373,12 @@ __device__ __forceinline__ void run_epilogue_qt(const Params& p, unsigned char* 
       break;
     }
     tc_fence_after();
-    // S = fl(P S_0 + acc) with S_0 = fl(code * scale), the decoded state, back
-    // into TMEM, and the row's amax
+    // S = fl(code * (scale P) + acc): the decoded state code * scale, decayed
+    // and replayed, rounded once; back into TMEM, and the row's amax
     float am = 0.0f;
     {
-      const float2 sc2 = make_float2(sc, sc), P2 = make_float2(P, P);
+      const float sp = sc * P;
+      const float2 sp2 = make_float2(sp, sp);
 #pragma unroll
       for (int c2 = 0; c2 < 4; ++c2) {
         float a[32];
@@ -391,7 +392,7 @@ __device__ __forceinline__ void run_epilogue_qt(const Params& p, unsigned char* 
           unpack_words<SF, 1>(code + q, f);
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const float2 y = __ffma2_rn(__fmul2_rn(make_float2(f[2 * u], f[2 * u + 1]), sc2), P2,
+            const float2 y = __ffma2_rn(make_float2(f[2 * u], f[2 * u + 1]), sp2,
                                         make_float2(a[4 * q + 2 * u], a[4 * q + 2 * u + 1]));
             a[4 * q + 2 * u] = y.x;
             a[4 * q + 2 * u + 1] = y.y;
@@ -405,8 +406,12 @@ __device__ __forceinline__ void run_epilogue_qt(const Params& p, unsigned char* 
     }
     // a row whose qmax / amax is not finite (amax 0 or tiny) gets scale 0 and
     // zero codes: it is quantized with inv = 0 (its values are all finite and
-    // tiny, so every product is 0)
-    float inv = __fdiv_rn(qmax, am);
+    // tiny, so every product is 0).  The stored scale is the correctly rounded
+    // amax / qmax; the multiplier qmax / amax that codes are computed with is a
+    // fast division (within 2 ulps: a code moves only where v * qmax / amax
+    // lies within 2 ulps of a rounding boundary, and |v| * inv stays below
+    // 127.5 for int8)
+    float inv = __fdividef(qmax, am);
     const bool finite = inv <= FLT_MAX;
     const float scale = finite ? __fdiv_rn(am, qmax) : 0.0f;
     if (!finite) inv = 0.0f;

@@ -10,8 +10,9 @@
  * storage formats, so every decision that turns a real number into stored
  * bits (the fp32 value a state element is rounded to, a row's amax and scale,
  * a quantized code, a stochastic-rounding choice) is taken in fp32, the
- * kernel's precision, from the fp64 result rounded once to fp32.  Decoding a
- * stored one-byte state (code * scale) is likewise an fp32 product.
+ * kernel's precision, from the fp64 result rounded once to fp32.  A stored
+ * one-byte state decodes to the real number code * scale, which fp64 holds
+ * exactly, so the decode adds no rounding of its own.
  *
  * Sources (all restated, none copied):
  *  - flashinfer.mamba.replayssm_materialize API page: signature, Parameters
@@ -503,8 +504,8 @@ int oracle_materialize(const oracle_args *a) {
           for (int j = 0; j < N; ++j) {
             uint32_t bits = load_bits(src_state, row + j, fmt);
             if (is_quantized(fmt)) {
-              float code = (float)oracle_decode(fmt, bits);
-              S[ii * N + j] = (double)(code * src_scale[h * D + ii]);
+              /* code * scale, exact in fp64 (8 significant bits times 24) */
+              S[ii * N + j] = oracle_decode(fmt, bits) * (double)src_scale[h * D + ii];
             } else {
               S[ii * N + j] = oracle_decode(fmt, bits);
             }

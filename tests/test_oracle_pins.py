@@ -386,7 +386,7 @@ def test_requantization_error_bound(sd):
         import torch
         dec = lambda b: torch.from_numpy(b.copy()).view(torch.float8_e4m3fn).float().numpy()
         c0, c1 = dec(w0.state[0][0]), dec(w1.state[0][dst])
-    v = (c0 * w0.scale[0][0][..., None]).astype(np.float32)           # fp32 product
+    v = (c0 * w0.scale[0][0][..., None]).astype(np.float32)           # code * scale rounded once
     amax = np.abs(v).max(axis=-1)
     s1 = w1.scale[0][dst]
     assert np.array_equal(s1, (amax / np.float32(qmax)).astype(np.float32))
@@ -663,13 +663,13 @@ def _exact_f32_result(w, l):
     src = int(w.src_slots[l, 0])
     if w.state_dtype in ("bf16", "f16"):
         S0 = decode_state(w, l, src)
-    else:  # one-byte: code * scale as an fp32 product
+    else:  # one-byte: code * scale, the exact product (fp64 holds it)
         if w.state_dtype == "i8":
-            codes = w.state[l][src].view(np.int8).astype(np.float32)
+            codes = w.state[l][src].view(np.int8).astype(np.float64)
         else:
             import torch
-            codes = torch.from_numpy(w.state[l][src].copy()).view(torch.float8_e4m3fn).float().numpy()
-        S0 = (codes * w.scale[l][src][..., None]).astype(np.float32).astype(np.float64)
+            codes = torch.from_numpy(w.state[l][src].copy()).view(torch.float8_e4m3fn).double().numpy()
+        S0 = codes * w.scale[l][src][..., None].astype(np.float64)
     x = decode_input(w, w.x[l][src, 2])            # [H, D]
     B = decode_input(w, w.B[l][src, 2])            # [G, N], G = H here
     S1 = S0 + (0.0625 * x)[:, :, None] * B[:, None, :]
