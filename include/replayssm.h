@@ -182,9 +182,12 @@ RSM_API int rsm_launch_config(const rsm_materialize_args *args, int *grid, int *
 /*
  * Name of the kernel rsm_materialize would launch for *args:
  * "materialize_kernel" (fp32 and 16-bit state on the CUDA cores),
- * "materialize_q8_kernel" (int8 and fp8 state) or "materialize_tc_kernel"
- * (16-bit state with bf16 inputs at dim 64 x dstate 128 and max_window >= 16:
- * every replayed prefix applied as a tensor-core rank-k update).  "" when
+ * "materialize_q8tc_kernel" (int8 and fp8 state with bf16 inputs and an even
+ * heads_per_group: items of two heads, the prefix as a tensor-core rank-k
+ * update), "materialize_q8_kernel" (the other int8 and fp8 calls) or
+ * "materialize_tc_kernel" (16-bit state with bf16 inputs at dim 64 x dstate
+ * 128 and max_window >= 16: every replayed prefix applied as a tensor-core
+ * rank-k update).  "" when
  * *args fails validation (the reason is in rsm_last_error()).  Needs no GPU;
  * the string is static.
  */

@@ -741,3 +741,16 @@ def test_one_byte_tensor_core_in_place_commit(sd):
     hw = _q8tc_world(shape, seed=72)
     hw.dst_slots[:] = hw.src_slots
     assert check(hw) >= 4
+
+
+@pytest.mark.parametrize("sd", ["i8", "fp8_e4m3"])
+@pytest.mark.parametrize("idt,hpg", [("f32", 2), ("bf16", 3)])
+@pytest.mark.parametrize("rounds", [0, 10])
+def test_one_byte_cuda_core_kernel(sd, idt, hpg, rounds):
+    """fp32 inputs, or B groups of an odd number of heads, keep one-byte state on
+    the CUDA-core kernel, with both rounding modes."""
+    shape = wl.Shape("q8cc", L=2, Bt=5, H=6, hpg=hpg, D=64, N=128, R=8, W=8, state_dtype=sd, input_dtype=idt,
+                     n_active=4, prefix=("uniform", 0, 8), philox_rounds=rounds, rand_seed=0xBEEF)
+    hw = wl.host_world(shape, seed=93)
+    assert rsm.kernel_name(**wl.device_world_from_host(hw).call_kwargs()) == "materialize_q8_kernel"
+    check(hw)
