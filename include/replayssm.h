@@ -64,7 +64,7 @@
 extern "C" {
 #endif
 
-#define RSM_ABI_VERSION 3
+#define RSM_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define RSM_API __attribute__((visibility("default")))
@@ -243,7 +243,18 @@ typedef struct rsm_gdn_commit_args {
   int32_t batch;                    /* >= 0; 0 enqueues nothing */
   int32_t use_qk_l2norm;            /* nonzero: normalise k with epsilon 1e-6 */
   int32_t null_block_id;            /* >= -1; slots <= it are ignored */
+  int32_t backend;                  /* RSM_GDN_BACKEND_*; see below */
 } rsm_gdn_commit_args;
+
+/* Backends (GDN page, Parameters: backend).  AUTO and SIMT run the fp32 kernel
+ * (contractions on the CUDA cores).  TCGEN05 runs the contractions on the
+ * tensor cores with TF32 operands (10 explicit mantissa bits, so results
+ * differ from the fp32 kernel's in the fourth significant digit); as on the
+ * page it requires use_qk_l2norm, no tracking (track arrays NULL) and a window
+ * of 4 to 8 tokens, and is refused otherwise (RSM_EINVAL). */
+#define RSM_GDN_BACKEND_AUTO 0
+#define RSM_GDN_BACKEND_SIMT 1
+#define RSM_GDN_BACKEND_TCGEN05 2
 
 /* Enqueue the commit described by *args on `stream`; same return codes as
  * rsm_materialize.  Host checks: non-NULL tensors, positive sizes, divisibility

@@ -80,8 +80,11 @@ class GdnArgs(ctypes.Structure):
         ("device_status", _P),
         ("layers", ctypes.c_int32), ("slots", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
         ("num_k_heads", ctypes.c_int32), ("window", ctypes.c_int32), ("batch", ctypes.c_int32),
-        ("use_qk_l2norm", ctypes.c_int32), ("null_block_id", ctypes.c_int32),
+        ("use_qk_l2norm", ctypes.c_int32), ("null_block_id", ctypes.c_int32), ("backend", ctypes.c_int32),
     ]
+
+
+GDN_BACKENDS = {"auto": 0, "simt": 1, "tcgen05": 2}  # RSM_GDN_BACKEND_* (include/replayssm.h)
 
 
 def load_library(build_if_missing: bool = True):
@@ -304,7 +307,7 @@ def stride_table(tensors, device=None):
 
 
 def _gdn_args(checkpoint_state, rawv_cache, rawk_cache, g_cache, beta_cache, state_indices, accept_lens, *,
-              track_state_indices=None, track_steps=None, use_qk_l2norm=True, null_block_id=-1,
+              track_state_indices=None, track_steps=None, use_qk_l2norm=True, null_block_id=-1, backend="auto",
               device_status=None):
     import torch
     if checkpoint_state.dim() != 5 or tuple(checkpoint_state.shape[3:]) != (128, 128):
@@ -340,6 +343,9 @@ def _gdn_args(checkpoint_state, rawv_cache, rawk_cache, g_cache, beta_cache, sta
     a.window, a.batch = int(T), int(B)
     a.use_qk_l2norm = int(bool(use_qk_l2norm))
     a.null_block_id = int(null_block_id)
+    if backend not in GDN_BACKENDS:
+        raise ValueError(f"backend must be one of {sorted(GDN_BACKENDS)} (got {backend!r})")
+    a.backend = GDN_BACKENDS[backend]
     return a
 
 
@@ -351,19 +357,19 @@ def gated_delta_rule_replayssm_commit(checkpoint_state, rawv_cache, rawk_cache, 
     checkpoints, in place.
 
     Same arguments as flashinfer.gdn_decode.gated_delta_rule_replayssm_commit
-    (API page).  There is one kernel, with fp32 contractions on the CUDA cores:
-    `backend` "auto" and "simt" select it; "tcgen05" is not built and raises.
+    (API page).  `backend` "auto" and "simt" run the kernel with fp32
+    contractions on the CUDA cores; "tcgen05" runs the contractions on the
+    tensor cores with TF32 operands, and (as on the page) requires
+    use_qk_l2norm, no tracking and a window of 4 to 8 tokens.
     `device_status` (optional int32 [1] CUDA tensor) receives RSM_STATUS_* bits
     for skipped out-of-range metadata.  Asynchronous on `stream` (default:
     torch's current stream).
     """
     import torch
-    if backend not in ("auto", "simt"):
-        raise ValueError(f"backend {backend!r} is not available (this library has the fp32 'simt' kernel only)")
     lib = load_library()
     a = _gdn_args(checkpoint_state, rawv_cache, rawk_cache, g_cache, beta_cache, state_indices, accept_lens,
                   track_state_indices=track_state_indices, track_steps=track_steps, use_qk_l2norm=use_qk_l2norm,
-                  null_block_id=null_block_id, device_status=device_status)
+                  null_block_id=null_block_id, device_status=device_status, backend=backend)
     if stream is None:
         stream = torch.cuda.current_stream()
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)

@@ -396,6 +396,17 @@ int validate_gdn(const rsm_gdn_commit_args* a) {
   if (a->window < 1 || a->window > gdn::kMaxWindow)
     return fail(RSM_EINVAL, "window %d outside [1, %d]", a->window, gdn::kMaxWindow);
   if (a->null_block_id < -1) return fail(RSM_EINVAL, "null_block_id must be >= -1");
+  if (a->backend < RSM_GDN_BACKEND_AUTO || a->backend > RSM_GDN_BACKEND_TCGEN05)
+    return fail(RSM_EINVAL, "unknown backend %d", a->backend);
+  if (a->backend == RSM_GDN_BACKEND_TCGEN05) {
+    if (!a->use_qk_l2norm) return fail(RSM_EINVAL, "backend tcgen05 requires use_qk_l2norm");
+    if (a->track_state_indices != nullptr) return fail(RSM_EINVAL, "backend tcgen05 does not support tracking");
+    if (a->window < gdn::kTcMinT || a->window > gdn::kTcMaxT)
+      return fail(RSM_EINVAL, "backend tcgen05 supports windows of %d to %d tokens (got %d)", gdn::kTcMinT,
+                  gdn::kTcMaxT, a->window);
+    if (static_cast<int64_t>(a->layers) * a->slots * a->num_v_heads * gdn::kDV > 0x7FFFFFFFLL)
+      return fail(RSM_EINVAL, "backend tcgen05: checkpoint_state has more than 2^31 rows");
+  }
   const int64_t heads = static_cast<int64_t>(a->layers) * a->slots * a->num_v_heads;
   if (heads * gdn::kDV * gdn::kDK >= (int64_t{1} << 62) / 4)
     return fail(RSM_EINVAL, "checkpoint_state is too large");
@@ -472,6 +483,98 @@ int plan_gdn(const rsm_gdn_commit_args* a, GdnLaunch* L) {
   return RSM_OK;
 }
 
+// The tcgen05 backend: one CTA per SM with the opt-in shared memory, and a
+// tensor map over checkpoint_state viewed as [layers*slots*HV*128 rows, 128]
+// fp32 (boxes of 128 rows x 32 columns, 128-byte swizzle), encoded per call
+// through the driver's entry point (no link against the driver library).
+using TensorMapEncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                       const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                       CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+TensorMapEncodeFn tensor_map_encoder() {
+  static const TensorMapEncodeFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<TensorMapEncodeFn>(nullptr);
+    return reinterpret_cast<TensorMapEncodeFn>(f);
+  }();
+  return fn;
+}
+
+int g_gdn_tc_smem_set[kMaxDevices];
+
+int launch_gdn_tc(const rsm_gdn_commit_args* a, void* stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(RSM_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  DeviceInfo di;
+  int rc = device_info(dev, &di);
+  if (rc != RSM_OK) return rc;
+  const int item_min = static_cast<int>(gdn::tc_item_layout(1).bytes);
+  const int item_max = static_cast<int>(gdn::tc_item_layout(a->window).bytes);
+  const int arena = (di.smem_optin - static_cast<int>(gdn::kTcArenaOff)) / 1024 * 1024;
+  if (arena < 2 * item_max) return fail(RSM_ENOTSUP, "two work items of %d bytes do not fit", item_max);
+  int slots = arena / item_min;
+  if (slots > 4) slots = 4;
+  const int smem = static_cast<int>(gdn::kTcArenaOff) + arena;
+  const TensorMapEncodeFn encode = tensor_map_encoder();
+  if (encode == nullptr) return fail(RSM_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+
+  gdn::TcParams tp{};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(gdn::kDK),
+                              static_cast<cuuint64_t>(a->layers) * a->slots * a->num_v_heads * gdn::kDV};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(gdn::kDK) * 4u};
+  const cuuint32_t box[2] = {32u, static_cast<cuuint32_t>(gdn::kDV)};
+  const cuuint32_t elem_strides[2] = {1u, 1u};
+  const CUresult cr = encode(&tp.tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2u, a->checkpoint_state, dims, strides, box,
+                             elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return fail(RSM_ECUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(cr));
+
+  gdn::Params& p = tp.p;
+  p.state = a->checkpoint_state;
+  p.rawv = a->rawv_cache;
+  p.rawk = a->rawk_cache;
+  p.g = a->g_cache;
+  p.beta = a->beta_cache;
+  p.state_indices = a->state_indices;
+  p.accept_lens = a->accept_lens;
+  p.track_indices = nullptr;
+  p.track_steps = nullptr;
+  p.status = a->device_status;
+  p.L = a->layers;
+  p.SL = a->slots;
+  p.HV = a->num_v_heads;
+  p.H = a->num_k_heads;
+  p.T = a->window;
+  p.B = a->batch;
+  p.l2norm = 1;
+  p.null_id = a->null_block_id;
+  p.arena_bytes = static_cast<uint32_t>(arena);
+  p.slots = static_cast<uint32_t>(slots);
+
+  const void* fn = gdn::commit_tc_kernel();
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_gdn_tc_smem_set[dev] < smem) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return fail(RSM_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+      g_gdn_tc_smem_set[dev] = smem;
+    }
+  }
+  if (verbose())
+    std::fprintf(stderr, "[replayssm] gdn commit (tcgen05) grid=%d block=%d smem=%d slots=%d\n", di.sms,
+                 gdn::kTcThreads, smem, slots);
+  void* kargs[] = {&tp};
+  e = cudaLaunchKernel(fn, dim3(di.sms), dim3(gdn::kTcThreads), kargs, static_cast<size_t>(smem),
+                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(RSM_ECUDA, "launch failed: %s", cudaGetErrorString(e));
+  g_last_error.clear();
+  return RSM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -510,6 +613,7 @@ int rsm_gdn_commit(const rsm_gdn_commit_args* args, void* stream) {
     g_last_error.clear();
     return RSM_OK;
   }
+  if (args->backend == RSM_GDN_BACKEND_TCGEN05) return launch_gdn_tc(args, stream);
   GdnLaunch L;
   rc = plan_gdn(args, &L);
   if (rc != RSM_OK) return rc;

@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_struct_layout_and_version(lib):
     assert lib.rsm_args_size() == ctypes.sizeof(rsm.RsmArgs)
-    assert lib.rsm_abi_version() == 3
+    assert lib.rsm_abi_version() == 4
 
 
 def test_oracle_library_loads():
@@ -170,6 +170,27 @@ def test_gdn_validation_rejects(lib, rule):
         a.layers = 0
     assert lib.rsm_gdn_commit(ctypes.byref(a), None) == -1
     assert lib.rsm_last_error()
+
+
+@pytest.mark.parametrize("rule", ["unknown", "no_l2norm", "tracking", "window_3", "window_9"])
+def test_gdn_tcgen05_backend_preconditions(lib, rule):
+    """The tcgen05 backend takes what the GDN page gives it (normalised K, no
+    tracking, windows of 4 to 8 tokens) and refuses the rest on the host."""
+    a = good_gdn_args()
+    a.backend = rsm.GDN_BACKENDS["tcgen05"]
+    if rule == "unknown":
+        a.backend = 3
+    elif rule == "no_l2norm":
+        a.use_qk_l2norm = 0
+    elif rule == "tracking":
+        a.track_state_indices = a.track_steps = 0x10000
+    elif rule == "window_3":
+        a.window = 3
+    else:
+        a.window = 9
+    assert lib.rsm_gdn_commit(ctypes.byref(a), None) == -1
+    msg = lib.rsm_last_error()
+    assert (b"backend" in msg) if rule == "unknown" else (b"tcgen05" in msg), msg
 
 
 def test_gdn_empty_batch_enqueues_nothing(lib):

@@ -139,3 +139,96 @@ def test_full_size_sampled():
         ref = run_oracle(w)
         got = np.stack([dw.state[l, s].cpu().numpy(), dw.state[l, ts].cpu().numpy()])[None]
         compare(got, ref, w.state)
+
+
+# ----------------------------------------------------------------------------
+# the tcgen05 backend (TF32 contractions): normalised K, windows 4..8, no tracking
+# ----------------------------------------------------------------------------
+
+def _bf16_to_f64(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _tf32_bound(hw):
+    """First-order bound on |tcgen05 result - exact result| for every element
+    the call writes (the derivation is in the design notes): TF32 operands
+    carry a relative error below delta = 2^-10, fp32 accumulation 2^-16 of
+    the summed magnitudes; W = S0 k^ is off by (2 delta + 2^-16) sum|S0 k^|,
+    the triangular solve propagates that through |L|, and the rank-n update
+    adds 2 delta sum|c u k^| of its own."""
+    delta, acc = 2.0 ** -10, 2.0 ** -16
+    sh = hw.shape
+    bound = np.zeros(hw.state.shape, np.float64)
+    per_kh = sh.HV // sh.H
+    for b in range(sh.B):
+        s, n = int(hw.state_indices[b]), int(hw.accept_lens[b])
+        if s <= sh.null_block_id or n == 0:
+            continue
+        for l in range(sh.L):
+            for hv in range(sh.HV):
+                k = _bf16_to_f64(hw.rawk[l, s, hv // per_kh, :n])                  # [n, DK]
+                kh = k / np.sqrt((k * k).sum(-1, keepdims=True) + 1e-6)
+                v = _bf16_to_f64(hw.rawv[l, s, hv, :n])                             # [n, DV]
+                gam = np.cumprod(np.exp(hw.g[l, s, hv, :n].astype(np.float64)))
+                beta = hw.beta[l, s, hv, :n].astype(np.float64)
+                S0 = hw.state[l, s, hv].astype(np.float64)                          # [DV, DK]
+                W = S0 @ kh.T                                                       # [DV, n]
+                L = np.zeros((n, n))
+                for t in range(n):
+                    for q in range(t):
+                        L[q, t] = beta[q] * gam[t] / gam[q] * (kh[q] @ kh[t])
+                u = np.zeros((gw.DV, n))
+                for t in range(n):
+                    u[:, t] = v[t] - gam[t] * W[:, t] - u[:, :t] @ L[:t, t]
+                c = beta * gam[-1] / gam
+                dW = (2 * delta + acc) * (np.abs(S0) @ np.abs(kh).T)                # [DV, n]
+                du = np.zeros((gw.DV, n))
+                for t in range(n):
+                    du[:, t] = gam[t] * dW[:, t] + du[:, :t] @ np.abs(L[:t, t])
+                bound[l, s, hv] = (2 * delta * (np.abs(c * u) @ np.abs(kh))
+                                   + (np.abs(c) * du) @ np.abs(kh))
+    return bound
+
+
+def _check_tc(hw):
+    dw = gw.gdn_device_world_from_host(hw)
+    kw = dw.call_kwargs()
+    kw.update(track_state_indices=None, track_steps=None, backend="tcgen05")
+    rsm.gated_delta_rule_replayssm_commit(**kw)
+    torch.cuda.synchronize()
+    assert int(dw.status.item()) == 0
+    got = dw.state.cpu().numpy()
+    ref = run_oracle(hw)
+    before = hw.state
+    untouched = np.all(ref == before, axis=(-1, -2))
+    assert np.array_equal(got[untouched], before[untouched]), "a slot the oracle leaves alone was written"
+    err = np.abs(got.astype(np.float64) - ref.astype(np.float64))
+    bound = 1.25 * _tf32_bound(hw) + 2.0 ** -22 * np.abs(ref.astype(np.float64)) + 1e-7
+    assert np.all(err <= bound), f"max error {err.max():.3e}, worst excess {(err - bound).max():.3e}"
+    return int((~untouched).sum()), float(err[~untouched].max()) if (~untouched).any() else 0.0
+
+
+@pytest.mark.parametrize("T,HV,H", [(4, 4, 2), (6, 8, 2), (8, 8, 4), (8, 16, 16)])
+def test_gdn_tcgen05_backend_within_the_tf32_bound(T, HV, H):
+    shape = gw.GdnShape("tc", L=2, B=5, HV=HV, H=H, T=T, track=False)
+    hw = gw.gdn_host_world(shape, seed=700 + T * 10 + HV)
+    hw.accept_lens[0] = T                      # the longest prefix
+    written, worst = _check_tc(hw)
+    assert written >= 2 * HV
+
+
+def test_gdn_tcgen05_backend_every_accepted_length_and_null_slots():
+    shape = gw.GdnShape("tclen", L=2, B=9, HV=4, H=2, T=8, slots=24, null_block_id=1, track=False)
+    hw = gw.gdn_host_world(shape, seed=71)
+    hw.accept_lens[:] = np.arange(9)
+    hw.state_indices[4] = 1                    # a null slot (<= null_block_id): left alone
+    _check_tc(hw)
+
+
+def test_gdn_tcgen05_backend_many_items_per_cta():
+    """Several value heads per CTA, so that the arena wraps and both operand
+    and accumulator buffers are reused many times."""
+    shape = gw.GdnShape("tcmany", L=3, B=24, HV=16, H=4, T=8, track=False)
+    hw = gw.gdn_host_world(shape, seed=72)
+    written, _ = _check_tc(hw)
+    assert written > 500
