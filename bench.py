@@ -52,6 +52,8 @@ KERNEL_SOURCES = {
     "materialize_q8tc_kernel": _SHARED_SOURCES + [_CSRC + f for f in (
         "rsm_kernel.cuh", "rsm_formats.cuh", "rsm_q8tc_kernel.cuh", "rsm_tc.cuh", "rsm_inst_q8tc.cu")],
     "gdn_commit_kernel": _SHARED_SOURCES + [_CSRC + f for f in ("gdn_kernel.cuh", "gdn_params.h", "gdn_inst.cu")],
+    "gdn_commit_tc_kernel": _SHARED_SOURCES + [_CSRC + f for f in (
+        "gdn_tc_kernel.cuh", "gdn_params.h", "gdn_inst.cu", "rsm_tc.cuh")],
 }
 
 
@@ -66,6 +68,7 @@ def parse_args():
     p.add_argument("--batch", type=int, default=None, help="batch size (default: the workload's)")
     p.add_argument("--prefix", type=int, default=None, help="fixed replay_prefix_len for every request")
     p.add_argument("--state-dtype", default=None, choices=sorted(wl.ELEM_SIZE), help="override the state format")
+    p.add_argument("--input-dtype", default=None, choices=["bf16", "f32"], help="override the x/B input format")
     p.add_argument("--window", type=int, default=None, help="override max_window (and ring_buffer_len)")
     p.add_argument("--no-extras", action="store_true", help="skip the n sweep, empty latency, e2e and CPU baseline")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work for the oracle baseline sample")
@@ -79,6 +82,8 @@ def parse_args():
                    help="comma-separated names of the named workloads to measure (default: all of them)")
     p.add_argument("--gdn", action="store_true",
                    help="measure only the gated-delta-rule commit (gdn36_hv32_t8; --batch overrides B)")
+    p.add_argument("--gdn-backend", default="auto", choices=["auto", "simt", "tcgen05"],
+                   help="the commit's backend with --gdn (tcgen05: the shape without tracking)")
     return p.parse_args()
 
 
@@ -534,14 +539,16 @@ def measure_workload(torch, rsm, shape, device, peak_gbs, sms, uuid):
     return out
 
 
-def measure_gdn(torch, rsm, shape, device, peak_gbs, sms, uuid):
+def measure_gdn(torch, rsm, shape, device, peak_gbs, sms, uuid, backend="auto"):
     """Time of one gated-delta-rule commit call over a seeded full-size world
     (state updated in place, so every timed call is a fresh commit of the same
     shape), its algorithmic bytes against the HBM peak, and its FP32 lane
     operations (per element and accepted token: the dot-product FMA, the decay
-    multiply and the update FMA) against the lane peak."""
+    multiply and the update FMA) against the lane peak.  `backend` as the
+    call's ("tcgen05": the TF32 tensor-core kernel, no tracking)."""
     dw = gw.gdn_device_world_random(shape, seed=5, device=device)
     kw = dw.call_kwargs()
+    kw["backend"] = backend
     idx, lens = dw.state_indices.cpu().numpy(), dw.accept_lens.cpu().numpy()
     tidx = None if dw.track_state_indices is None else dw.track_state_indices.cpu().numpy()
     tst = None if dw.track_steps is None else dw.track_steps.cpu().numpy()
@@ -554,7 +561,8 @@ def measure_gdn(torch, rsm, shape, device, peak_gbs, sms, uuid):
     status = int(dw.status.item())
     del dw, kw
     torch.cuda.empty_cache()
-    out = {"kernel": "gdn_commit_kernel", "source_hash": kernel_source_hash("gdn_commit_kernel"),
+    kernel = "gdn_commit_tc_kernel" if backend == "tcgen05" else "gdn_commit_kernel"
+    out = {"kernel": kernel, "source_hash": kernel_source_hash(kernel), "backend": backend,
            "layers": shape.L, "v_heads": shape.HV, "k_heads": shape.H, "window": shape.T, "batch": shape.B,
            "live_requests": len(live), "track": shape.track, "accept": list(shape.accept), "ms_per_call": ms,
            "steps": steps, "algorithmic_bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9}
@@ -577,6 +585,9 @@ def named_workloads():
     gshape = gw.GDN_SHAPES["gdn36_hv32_t8"]
     out["gdn36_hv32_t8"] = ("gdn", gshape)
     out["gdn36_hv32_t8_full"] = ("gdn", gshape.replace(accept=("fixed", 8)))
+    # the two backends side by side on the conditions the tcgen05 one takes (no tracking)
+    out["gdn36_hv32_t8_notrack"] = ("gdn", gshape.replace(track=False))
+    out["gdn36_hv32_t8_notrack_tcgen05"] = ("gdn_tcgen05", gshape.replace(track=False))
     return out
 
 
@@ -584,6 +595,9 @@ def measure_named_workloads(torch, rsm, device, peak_gbs, sms, uuid, only=None):
     sweep = {}
     for name, (kind, shape) in named_workloads().items():
         if only and name not in only:
+            continue
+        if kind == "gdn_tcgen05":
+            sweep[name] = measure_gdn(torch, rsm, shape, device, peak_gbs, sms, uuid, backend="tcgen05")
             continue
         measure = measure_gdn if kind == "gdn" else measure_workload
         sweep[name] = measure(torch, rsm, shape, device, peak_gbs, sms, uuid)
@@ -619,7 +633,9 @@ def main():
             gshape = gshape.replace(B=args.batch)
         if args.prefix is not None:
             gshape = gshape.replace(accept=("fixed", args.prefix))
-        res = measure_gdn(torch, rsm, gshape, device, peak, sms, uuid)
+        if args.gdn_backend == "tcgen05":
+            gshape = gshape.replace(track=False)
+        res = measure_gdn(torch, rsm, gshape, device, peak, sms, uuid, backend=args.gdn_backend)
         if rank == 0:
             print(json.dumps({"metric": "gated-delta-rule commit: algorithmic GB/s", "unit": "GB/s",
                               "value": res["gbs"], "peak_gbs": peak, "peak_source": peak_kind, **res}), flush=True)
@@ -634,6 +650,8 @@ def main():
         shape = shape.replace(prefix=("fixed", args.prefix))
     if args.state_dtype is not None:
         shape = shape.replace(state_dtype=args.state_dtype)
+    if args.input_dtype is not None:
+        shape = shape.replace(input_dtype=args.input_dtype)
     if args.window is not None:
         shape = shape.replace(W=args.window, R=max(args.window, shape.R),
                               ring_start=(0, max(args.window, shape.R)))
