@@ -247,19 +247,27 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   const bool sr_instance = quant && a->philox_rounds > 0;
   const bool q8 = quant && !use_qt;  // the four-warp one-byte kernel (both rounding modes)
   const int cw = q8 ? rsm::kQ8ConsumerWarps : rsm::kConsumerWarps;
-  const int base = static_cast<int>(use_tc ? rsm::kTcArenaBase
+  const int base = static_cast<int>(use_tc ? rsm::tc_arena_base(a->state_dtype)
                                     : use_qt ? rsm::qt_arena_base(a->max_window)
                                     : q8     ? rsm::kQ8ArenaBase
                                              : rsm::arena_base(a->dim, a->dstate, sb, cw));
   const int threads = use_tc ? rsm::kTcThreads : use_qt ? rsm::kQtThreads : 32 * (1 + cw);
   // (the one-byte tensor-core kernel: at most two CTAs of 256 TMEM columns per SM)
+  // The tensor-core kernel places items exactly (an item follows the last one
+  // where it fits), and in a B group of several heads every item after the
+  // first leaves its B rows out: two consecutive items of the longest window
+  // then take one item with B rows and one without.
+  const int need = use_tc && a->heads_per_group > 1
+                       ? item_max + static_cast<int>(rsm::item_layout(a->dim, a->dstate, sb, quant, ib, a->max_window,
+                                                                      false, 1).bytes)
+                       : 2 * item_max;
   int ctas = q8 ? 3 : 2, arena = 0;
   for (; ctas >= 1; --ctas) {
     const int per_cta = ctas == 1 ? di.smem_optin : di.smem_per_sm / ctas - di.smem_reserved;
     arena = (per_cta - base) / 128 * 128;
-    if (arena >= 2 * item_max) break;
+    if (arena >= need) break;
   }
-  if (ctas < 1) return fail(RSM_ENOTSUP, "two work items of %d bytes do not fit in shared memory", item_max);
+  if (ctas < 1) return fail(RSM_ENOTSUP, "two work items (%d bytes) do not fit in shared memory", need);
   // Six items in flight per SM (three per CTA at two CTAs per SM): measured
   // on GB300 against two and four per CTA, it is the fastest with replay at
   // every window length (four per CTA is 2% slower on the 48-layer bf16 shape).
@@ -345,7 +353,7 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
   p.philox_rounds = a->philox_rounds;
   p.num_slots = a->num_slots;
   p.tc_min_k = use_tc ? rsm::kTcMinK : use_qt ? 1 : 0;
-  p.desc0 = use_tc   ? rsm::kTcDescBase
+  p.desc0 = use_tc   ? rsm::tc_desc_base(a->state_dtype)
             : use_qt ? rsm::qt_desc_base(a->max_window)
             : q8     ? rsm::kQ8DescBase
                      : rsm::desc_base(a->dim, a->dstate, sb, cw);

@@ -133,7 +133,7 @@ __device__ __forceinline__ void load_inputs(const unsigned char* p, float* out) 
 // items are two consecutive heads of one B group: their tiles, scales and x
 // rows are adjacent in memory, so they move as one tile of 2D rows; dt and A
 // take one value per head).  Requires heads_per_group % HPI == 0.
-template <int SF, int IF, int D, int N, bool kChunked = false, int HPI = 1>
+template <int SF, int IF, int D, int N, bool kChunked = false, int HPI = 1, bool kExactFit = false>
 __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem, int lane) {
   constexpr int ES = Fmt<SF>::bytes;
   constexpr int IE = In<IF>::bytes;
@@ -197,7 +197,9 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
   // allocation has wrapped.  Releases complete in slot order (every consumer
   // warp takes the items in order), so freeing is first in, first out.
   // Placement depends on the item sizes alone (arena_next), so the consumers
-  // follow it without reading it from the descriptor.
+  // follow it without reading it from the descriptor: an item goes at the
+  // head if the bytes from there to the arena's end hold item_max (or, with
+  // kExactFit, the item itself), else at offset 0.
   const uint32_t item_max = item_layout(DI, N, ES, Q, IE, p.W, true, HPI).bytes;
   uint32_t head = 0, tail = 0, n_out = 0;
   bool wrapped = false;
@@ -224,7 +226,7 @@ __device__ __forceinline__ void run_loader(const Params& p, unsigned char* smem,
   };
   // the item's place, then a free slot and free bytes [off, off + bytes) there
   auto alloc = [&](uint32_t bytes, uint32_t& off) -> bool {
-    off = arena_next(head, item_max, p.arena_bytes);
+    off = arena_next(head, kExactFit ? bytes : item_max, p.arena_bytes);
     for (;;) {
       if (n_out == 0) break;
       if (n_out < p.stages) {

@@ -3,6 +3,8 @@
 #pragma once
 #include <cstdint>
 
+#include "../../include/replayssm.h"  // the state formats
+
 namespace rsm {
 
 constexpr int kConsumerWarps = 8;  // 16-bit and fp32 state, and the tensor-core kernel
@@ -140,14 +142,29 @@ constexpr uint32_t kTcTmemSlot = kTcBarOff + 48;  // TMEM base address written b
 // stored at chunk c ^ r.  C^T = (w x)^T (64 dim rows): one atom column, token
 // groups of 8 rows 1024 bytes apart.  A = B^T (128 dstate columns): two atom
 // columns 1024 bytes apart, token groups 2048 bytes apart.
-constexpr uint32_t kTcBOff = 4096;                       // C^T, 64 x kTcKMax bf16 (8 KiB)
-constexpr uint32_t kTcAOff = kTcBOff + 64 * kTcKMax * 2;  // A, 128 x kTcKMax bf16 (16 KiB)
-constexpr uint32_t kTcCGroup = 1024, kTcAGroup = 2048;    // bytes between token groups of 8 rows
-static_assert(kTcBarOff + 128 <= kTcBOff && kTcBOff % 1024 == 0 && kTcAOff % 1024 == 0, "operand alignment");
+// fp16 state: C = w x goes in as two bf16 operands, hi (c with its low 16
+// bits cleared) and lo (the remainder, rounded to bf16), so that each term
+// keeps 16 significant bits (2^-16 relative) instead of bf16's 8 (2^-9, coarser
+// than fp16's own 2^-11).  Token group g of C^T is then followed by its lo
+// rows (hi at 2048 g, lo at 2048 g + 1024), and one MMA (K = 16) takes eight
+// tokens: their hi and lo rows against the same eight rows of A, read twice
+// (the A descriptor's K stride is 0).
+__host__ __device__ constexpr bool tc_split_c(int sf) { return sf == RSM_F16; }
+constexpr uint32_t kTcBOff = 4096;  // C^T: 64 x kTcKMax bf16 (8 KiB), with lo rows 16 KiB
+__host__ __device__ constexpr uint32_t tc_c_group(int sf) { return tc_split_c(sf) ? 2048u : 1024u; }
+__host__ __device__ constexpr uint32_t tc_a_off(int sf) {  // A: 128 x kTcKMax bf16 (16 KiB)
+  return kTcBOff + (tc_split_c(sf) ? 2u : 1u) * 64u * kTcKMax * 2u;
+}
+constexpr uint32_t kTcAGroup = 2048;  // bytes between token groups of A
+static_assert(kTcBarOff + 128 <= kTcBOff && kTcBOff % 1024 == 0 && tc_a_off(RSM_BF16) % 1024 == 0 &&
+                  tc_a_off(RSM_F16) % 1024 == 0,
+              "operand alignment");
 constexpr uint32_t kTcAccCols = 64;               // one fp32 accumulator: 128 lanes x 64 columns
 constexpr uint32_t kTcTmemCols = 2 * kTcAccCols;  // two accumulators
-constexpr uint32_t kTcDescBase = round_up(kTcAOff + 128 * kTcKMax * 2, 128u);
-constexpr uint32_t kTcArenaBase = round_up(kTcDescBase + kMaxStages * kDescBytes, 128u);
+__host__ __device__ constexpr uint32_t tc_desc_base(int sf) { return round_up(tc_a_off(sf) + 128u * kTcKMax * 2u, 128u); }
+__host__ __device__ constexpr uint32_t tc_arena_base(int sf) {
+  return round_up(tc_desc_base(sf) + kMaxStages * kDescBytes, 128u);
+}
 constexpr int kTcMinK = 1;  // every prefix of one token or more goes through the MMA
 
 // The one-byte tensor-core kernel (rsm_q8tc_kernel.cuh): items of two heads

@@ -13,7 +13,8 @@
 //     operands in shared memory, MN-major with the 128-byte swizzle, so that
 //     a ring row is a row of the operand (A = B^T: 128 x k_pad, the bf16 ring
 //     rows of B copied exactly, rebuilt only for the first head of a B group;
-//     the second operand C^T: 64 x k_pad, w_t x_t rounded to bf16), 16 bytes
+//     the second operand C^T: 64 x k_pad, w_t x_t rounded to bf16, or for
+//     fp16 state split into two bf16 operands hi + lo), 16 bytes
 //     a thread at a time, then one thread issues ceil(k/16) tcgen05.mma
 //     (K = 16) into one of two TMEM accumulators and commits them to that
 //     accumulator's mbarrier.  (K-major operands had each 16-byte chunk
@@ -107,28 +108,30 @@ __device__ __forceinline__ void run_builder_tc(const Params& p, unsigned char* s
   const uint32_t full0 = sbase, empty0 = sbase + 8u * kMaxStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
   float* wbuf = reinterpret_cast<float*>(smem + kWeightOff) + bw * kWeightStride;
-  unsigned char* aop = smem + kTcAOff;
+  constexpr bool kSplit = tc_split_c(SF);
+  constexpr uint32_t kCGroup = tc_c_group(SF);  // bytes between token groups of C^T
+  unsigned char* aop = smem + tc_a_off(SF);
   unsigned char* bop = smem + kTcBOff;
   const int tid = bw * 32 + lane;  // over the builder group
   constexpr uint32_t kIdesc = idesc_bf16_f32(128, 64, true, true);
 
-  const uint32_t item_max = item_layout(D, N, ES, false, IE, p.W).bytes;
   uint32_t arena_head = 0;
   uint32_t stage = 0, phase = 0;
   uint32_t n_tc = 0;  // tensor-core items so far
+  int c_dirty = kTcKMax;  // leading token rows of C^T (and C_lo^T) that may hold nonzero values
   for (;;) {
     if (!tc_wait(full0 + 8u * stage, phase, abort_flag)) {
       tc_give_up(p, abort_flag, lane);
       break;
     }
-    const uint32_t off = arena_next(arena_head, item_max, p.arena_bytes);
-    const unsigned char* sb = smem + p.arena0 + off;
     const ItemDesc* desc = reinterpret_cast<const ItemDesc*>(smem + p.desc0) + stage;
     const uint32_t flags = __shfl_sync(0xFFFFFFFFu, desc->flags, 0);
     if (flags & kFlagEnd) break;
     const int k = __shfl_sync(0xFFFFFFFFu, desc->k, 0);
     const bool same_B = (flags & kFlagSameB) != 0u;  // the A operand of the previous item still holds
     const ItemLayout il = item_layout(D, N, ES, false, IE, k, !same_B);
+    const uint32_t off = arena_next(arena_head, il.bytes, p.arena_bytes);  // the loader's exact-fit placement
+    const unsigned char* sb = smem + p.arena0 + off;
     arena_head = off + il.bytes;
     const uint32_t empty_bar = empty0 + 8u * stage;
     if (++stage == p.stages) {
@@ -149,10 +152,11 @@ __device__ __forceinline__ void run_builder_tc(const Params& p, unsigned char* s
       break;
     }
     const int kp = (k + 15) & ~15;  // K padded to whole MMAs; tokens k .. kp-1 are zero
+    constexpr int kStep = 32 * kTcBuilderWarps;
     if (!same_B) {
       // A = B^T: token t's 256-byte B row is row t % 8 of atom column c / 8 of
       // token group t / 8; chunk c % 8 goes to chunk (c % 8) ^ (t % 8)
-      for (int u = tid; u < kp * 16; u += 32 * kTcBuilderWarps) {
+      for (int u = tid; u < kp * 16; u += kStep) {
         const int t = u >> 4, c = u & 15;
         const uint4 v = t < k ? *reinterpret_cast<const uint4*>(sb + il.off_B + t * (N * 2) + c * 16)
                               : make_uint4(0u, 0u, 0u, 0u);
@@ -160,17 +164,53 @@ __device__ __forceinline__ void run_builder_tc(const Params& p, unsigned char* s
                                   (((c & 7) ^ (t & 7)) << 4)) = v;
       }
     }
-    // C^T = (w x)^T: token t's 128-byte row w_t x_t, chunk c to chunk c ^ (t % 8)
-    for (int u = tid; u < kp * 8; u += 32 * kTcBuilderWarps) {
-      const int t = u >> 3, c = u & 7;
-      uint4 o = make_uint4(0u, 0u, 0u, 0u);
-      if (t < k) {
-        const uint4 xv = *reinterpret_cast<const uint4*>(sb + il.off_x + t * (D * 2) + c * 16);
-        const float w = wbuf[t];
-        o = make_uint4(pack_bf16x2(bf16lo(xv.x) * w, bf16hi(xv.x) * w), pack_bf16x2(bf16lo(xv.y) * w, bf16hi(xv.y) * w),
-                       pack_bf16x2(bf16lo(xv.z) * w, bf16hi(xv.z) * w), pack_bf16x2(bf16lo(xv.w) * w, bf16hi(xv.w) * w));
+    // C^T = (w x)^T: token t's 128-byte row w_t x_t, chunk c to chunk c ^ (t % 8);
+    // two chunks a thread at a time, both loaded before either is converted.
+    // Rows k .. kq-1 must be zero: only those a longer item left nonzero are
+    // cleared (rows past kq are not read by this item's MMAs)
+    const int kq = kSplit ? (k + 7) & ~7 : kp;  // token rows the MMAs read
+    const int rows = max(k, min(c_dirty, kq));
+    c_dirty = c_dirty > kq ? c_dirty : k;
+    const int n_chunks = rows * 8;
+    for (int u0 = tid; u0 < n_chunks; u0 += 2 * kStep) {
+      uint4 xv[2];
+      float wt[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int u = u0 + r * kStep, t = u >> 3, c = u & 7;
+        xv[r] = make_uint4(0u, 0u, 0u, 0u);
+        wt[r] = 0.0f;
+        if (u < n_chunks && t < k) {
+          xv[r] = *reinterpret_cast<const uint4*>(sb + il.off_x + t * (D * 2) + c * 16);
+          wt[r] = wbuf[t];
+        }
       }
-      *reinterpret_cast<uint4*>(bop + (t >> 3) * kTcCGroup + (t & 7) * 128 + ((c ^ (t & 7)) << 4)) = o;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int u = u0 + r * kStep, t = u >> 3, c = u & 7;
+        if (u >= n_chunks) break;
+        const uint32_t at = (t >> 3) * kCGroup + (t & 7) * 128 + ((c ^ (t & 7)) << 4);
+        const uint32_t xw[4] = {xv[r].x, xv[r].y, xv[r].z, xv[r].w};
+        const float2 w2 = make_float2(wt[r], wt[r]);
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 cc = __fmul2_rn(make_float2(bf16lo(xw[q]), bf16hi(xw[q])), w2);
+          if constexpr (kSplit) {
+            // hi = c with its low 16 bits cleared (a bf16 value), lo = c - hi
+            // (exact) rounded to bf16: hi + lo is w x within 2^-16 relative
+            const uint32_t c0 = __float_as_uint(cc.x), c1 = __float_as_uint(cc.y);
+            hw[q] = __byte_perm(c0, c1, 0x7632u);
+            const float2 ll = __ffma2_rn(make_float2(__uint_as_float(c0 & 0xFFFF0000u), __uint_as_float(c1 & 0xFFFF0000u)),
+                                         make_float2(-1.0f, -1.0f), cc);
+            lw[q] = pack_bf16x2(ll.x, ll.y);
+          } else {
+            hw[q] = pack_bf16x2(cc.x, cc.y);
+          }
+        }
+        *reinterpret_cast<uint4*>(bop + at) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        if constexpr (kSplit) *reinterpret_cast<uint4*>(bop + at + 1024) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
     }
     fence_proxy_async_smem();  // the operands, written by this thread, before the tensor cores read them
     // the group is done with the slot's x, B and dt
@@ -195,13 +235,22 @@ __device__ __forceinline__ void run_builder_tc(const Params& p, unsigned char* s
       }
       tc_fence_after();
       if (lane == 0) {
-        const uint64_t adesc0 = smem_desc_mn_sw128(sbase + kTcAOff, 1024u, kTcAGroup);
-        const uint64_t bdesc0 = smem_desc_mn_sw128(sbase + kTcBOff, 1024u, kTcCGroup);
-        // one MMA per 16 tokens, i.e. per two token groups; the start address
-        // field counts 16-byte units
-        for (int kc = 0; kc < kp / 16; ++kc)
-          tc_mma_bf16(tmem + buf * kTcAccCols, adesc0 + static_cast<uint64_t>(kc * 2 * kTcAGroup / 16),
-                      bdesc0 + static_cast<uint64_t>(kc * 2 * kTcCGroup / 16), kIdesc, kc > 0 ? 1u : 0u);
+        const uint64_t bdesc0 = smem_desc_mn_sw128(sbase + kTcBOff, 1024u, 1024u);
+        if constexpr (kSplit) {
+          // one MMA per eight tokens: K rows 0-7 of C^T are their hi rows and
+          // 8-15 their lo rows, against the eight A rows read twice (K stride
+          // 0); the start address field counts 16-byte units
+          const uint64_t adesc0 = smem_desc_mn_sw128(sbase + tc_a_off(SF), 1024u, 0u);
+          for (int g = 0; g < kq / 8; ++g)
+            tc_mma_bf16(tmem + buf * kTcAccCols, adesc0 + static_cast<uint64_t>(g * kTcAGroup / 16),
+                        bdesc0 + static_cast<uint64_t>(g * kCGroup / 16), kIdesc, g > 0 ? 1u : 0u);
+        } else {
+          // one MMA per 16 tokens, i.e. per two token groups
+          const uint64_t adesc0 = smem_desc_mn_sw128(sbase + tc_a_off(SF), 1024u, kTcAGroup);
+          for (int kc = 0; kc < kp / 16; ++kc)
+            tc_mma_bf16(tmem + buf * kTcAccCols, adesc0 + static_cast<uint64_t>(kc * 2 * kTcAGroup / 16),
+                        bdesc0 + static_cast<uint64_t>(kc * 2 * kCGroup / 16), kIdesc, kc > 0 ? 1u : 0u);
+        }
         tc_commit(sbase + kTcMmaDone + 8u * buf);
       }
       __syncwarp();
@@ -229,7 +278,6 @@ __device__ __forceinline__ void run_epilogue_tc(const Params& p, unsigned char* 
     key0 = static_cast<uint32_t>(s);
     key1 = static_cast<uint32_t>(s >> 32);
   }
-  const uint32_t item_max = item_layout(D, N, ES, false, IE, p.W).bytes;
   uint32_t arena_head = 0;
   uint32_t stage = 0, phase = 0;
   uint32_t n_tc = 0;
@@ -238,14 +286,14 @@ __device__ __forceinline__ void run_epilogue_tc(const Params& p, unsigned char* 
       tc_give_up(p, abort_flag, lane);
       break;
     }
-    const uint32_t off = arena_next(arena_head, item_max, p.arena_bytes);
-    const unsigned char* sb = smem + p.arena0 + off;
     const ItemDesc* desc = reinterpret_cast<const ItemDesc*>(smem + p.desc0) + stage;
     const uint32_t flags = __shfl_sync(0xFFFFFFFFu, desc->flags, 0);
     if (flags & kFlagEnd) break;
     const int k = __shfl_sync(0xFFFFFFFFu, desc->k, 0);
     const bool same_B = (flags & kFlagSameB) != 0u;
     const ItemLayout il = item_layout(D, N, ES, false, IE, k, !same_B);
+    const uint32_t off = arena_next(arena_head, il.bytes, p.arena_bytes);  // the loader's exact-fit placement
+    const unsigned char* sb = smem + p.arena0 + off;
     arena_head = off + il.bytes;
     unsigned char* dst_tile = reinterpret_cast<unsigned char*>(desc->dst_state);
     const bool dst_aligned = (flags & kFlagDstAligned) != 0u;
@@ -379,7 +427,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) materialize_tc_kernel(const __g
     return;
   }
   if (warp == 0) {
-    run_loader<SF, RSM_BF16, 64, 128, true>(p, smem, lane);
+    run_loader<SF, RSM_BF16, 64, 128, true, 1, true>(p, smem, lane);
   } else {
     if (warp <= kTcBuilderWarps)
       run_builder_tc<SF>(p, smem, warp - 1, lane, tmem);

@@ -660,6 +660,58 @@ def test_tensor_core_out_of_range_metadata_is_skipped_and_flagged(bad, bit):
     compare_worlds(got, run_oracle(ref_in), ref_in)
 
 
+def _bf16_bits_to_f64(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def tc_f16_error_report(hw, got, ref):
+    """fp16 state on the tensor cores: per written slot, |gpu - oracle| against
+    one fp16 ulp plus 2^-13 (sum_t dt_t |x_t[i]| |B_t[j]| + |S0[i][j]|).
+
+    With C = w x split into bf16 hi + lo (16 significant bits a term, the
+    decay weights and P in fp32, fp32 accumulation) the error before the final
+    rounding stays below 2^-14.4 of that sum, so the result is within one ulp
+    plus the sum's term; C rounded to a single bf16 operand (2^-9 a term)
+    leaves several ulps on long prefixes.  Returns (max |err|, max err/allow,
+    fraction of elements that differ from the oracle)."""
+    H, hpg = hw.H, hw.hpg
+    worst, ratio, diff, n = 0.0, 0.0, 0, 0
+    for (l, d), (b, k) in written_dsts(hw).items():
+        if k == 0:
+            continue
+        src = int(hw.src_slots[l, b])
+        pos = (int(hw.ring_start[b]) + np.arange(k)) % hw.R
+        x = np.abs(_bf16_bits_to_f64(hw.x[l][src][pos]))                      # (k, H, D)
+        B = np.abs(_bf16_bits_to_f64(hw.B[l][src][pos]))[:, np.arange(H) // hpg]  # (k, H, N)
+        dt = hw.dt[l][src][pos].astype(np.float64)                            # (k, H)
+        s0 = np.abs(hw.state[l][src].astype(np.float64))                      # (H, D, N)
+        terms = np.einsum("th,thi,thj->hij", dt, x, B)
+        g = got.state[l][d].astype(np.float64)
+        r = ref.state[l][d].astype(np.float64)
+        ulp = np.maximum(np.spacing(np.abs(g).astype(np.float16)), np.spacing(np.abs(r).astype(np.float16)))
+        allow = ulp.astype(np.float64) + 2.0 ** -13 * (terms + s0)
+        err = np.abs(g - r)
+        worst = max(worst, float(err.max()))
+        ratio = max(ratio, float((err / allow).max()))
+        diff += int((g != r).sum())
+        n += g.size
+    return worst, ratio, diff / max(n, 1)
+
+
+@pytest.mark.parametrize("k", [16, 33, 64])
+def test_tensor_core_fp16_state_error_bound(k):
+    """fp16 state: every element within one fp16 ulp of the oracle plus
+    2^-13 of the replayed terms' magnitudes (tc_f16_error_report)."""
+    shape = wl.Shape("tcprec", L=2, Bt=4, H=32, hpg=16, D=64, N=128, R=64, W=64, state_dtype="f16",
+                     n_active=4, ring_start=(0, 64), prefix=("fixed", k))
+    hw = wl.host_world(shape, seed=700 + k)
+    got, ref = run_cuda(hw), run_oracle(hw)
+    worst, ratio, frac = tc_f16_error_report(hw, got, ref)
+    print(f"fp16 tensor cores, k={k}: max |err| {worst:.3e}, max err/allow {ratio:.3f}, {frac:.2%} differ")
+    assert ratio <= 1.0
+    compare_worlds(got, ref, hw)
+
+
 @pytest.mark.parametrize("sd", ["bf16", "f16"])
 def test_tensor_core_in_place_commit(sd):
     shape = wl.Shape("tcinplace", L=2, Bt=5, H=6, hpg=3, D=64, N=128, R=64, W=64, state_dtype=sd, n_active=4,
