@@ -146,9 +146,10 @@ constexpr uint32_t kTcTmemSlot = kTcBarOff + 48;  // TMEM base address written b
 // bits cleared) and lo (the remainder, rounded to bf16), so that each term
 // keeps 16 significant bits (2^-16 relative) instead of bf16's 8 (2^-9, coarser
 // than fp16's own 2^-11).  Token group g of C^T is then followed by its lo
-// rows (hi at 2048 g, lo at 2048 g + 1024), and one MMA (K = 16) takes eight
-// tokens: their hi and lo rows against the same eight rows of A, read twice
-// (the A descriptor's K stride is 0).
+// rows (hi at 2048 g, lo at 2048 g + 1024).  Up to eight tokens, one MMA
+// (K = 16) takes their hi and lo rows against the same eight rows of A, read
+// twice (the A descriptor's K stride is 0); longer items read C^T as 128 rows
+// (hi rows, then lo rows: atom columns 1024 bytes apart) into N = 128.
 __host__ __device__ constexpr bool tc_split_c(int sf) { return sf == RSM_F16; }
 constexpr uint32_t kTcBOff = 4096;  // C^T: 64 x kTcKMax bf16 (8 KiB), with lo rows 16 KiB
 __host__ __device__ constexpr uint32_t tc_c_group(int sf) { return tc_split_c(sf) ? 2048u : 1024u; }
@@ -159,7 +160,12 @@ constexpr uint32_t kTcAGroup = 2048;  // bytes between token groups of A
 static_assert(kTcBarOff + 128 <= kTcBOff && kTcBOff % 1024 == 0 && tc_a_off(RSM_BF16) % 1024 == 0 &&
                   tc_a_off(RSM_F16) % 1024 == 0,
               "operand alignment");
-constexpr uint32_t kTcAccCols = 64;               // one fp32 accumulator: 128 lanes x 64 columns
+// One fp32 accumulator: 128 lanes x 64 columns, and for fp16 state 64 more
+// (an item of more than eight tokens takes its hi and lo products separately:
+// one MMA of N = 128 per 16 tokens, C^T's token groups read as 128 rows, hi
+// then lo; the epilogue adds the two halves).
+constexpr uint32_t kTcAccCols = 128;
+constexpr uint32_t kTcLoCols = 64;                // the lo half of an accumulator
 constexpr uint32_t kTcTmemCols = 2 * kTcAccCols;  // two accumulators
 __host__ __device__ constexpr uint32_t tc_desc_base(int sf) { return round_up(tc_a_off(sf) + 128u * kTcKMax * 2u, 128u); }
 __host__ __device__ constexpr uint32_t tc_arena_base(int sf) {

@@ -64,15 +64,21 @@ __device__ __forceinline__ uint32_t from_f32_16(float v) {
 // line (rare paths): S = P S_0 + acc for this thread's column j, with S_0 read
 // from the item's tile in shared memory.
 template <int SF>
-__device__ __noinline__ void tc_epilogue_general(int philox_rounds, uint32_t taddr, const uint16_t* s0_col, float P,
-                                                 unsigned char* out_col, bool dst_aligned, bool sr, int h, int j,
-                                                 uint32_t dst_slot_id, uint32_t layer_id, uint32_t key0,
+__device__ __noinline__ void tc_epilogue_general(int philox_rounds, uint32_t taddr, bool split_n, const uint16_t* s0_col,
+                                                 float P, unsigned char* out_col, bool dst_aligned, bool sr, int h,
+                                                 int j, uint32_t dst_slot_id, uint32_t layer_id, uint32_t key0,
                                                  uint32_t key1) {
   constexpr int D = 64, N = 128;
 #pragma unroll 1
   for (int part = 0; part < D / 16; ++part) {
     float acc[16];
     tmem_ld16(taddr + 16u * part, acc);
+    if (split_n) {  // hi and lo products in the accumulator's two halves
+      float lo16[16];
+      tmem_ld16(taddr + kTcLoCols + 16u * part, lo16);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) acc[c] += lo16[c];
+    }
 #pragma unroll 1
     for (int c = 0; c < 16; ++c) {
       const int i = 16 * part + c;
@@ -114,6 +120,7 @@ __device__ __forceinline__ void run_builder_tc(const Params& p, unsigned char* s
   unsigned char* bop = smem + kTcBOff;
   const int tid = bw * 32 + lane;  // over the builder group
   constexpr uint32_t kIdesc = idesc_bf16_f32(128, 64, true, true);
+  constexpr uint32_t kIdescN128 = idesc_bf16_f32(128, 128, true, true);
 
   uint32_t arena_head = 0;
   uint32_t stage = 0, phase = 0;
@@ -168,7 +175,7 @@ __device__ __forceinline__ void run_builder_tc(const Params& p, unsigned char* s
     // two chunks a thread at a time, both loaded before either is converted.
     // Rows k .. kq-1 must be zero: only those a longer item left nonzero are
     // cleared (rows past kq are not read by this item's MMAs)
-    const int kq = kSplit ? (k + 7) & ~7 : kp;  // token rows the MMAs read
+    const int kq = kSplit && k <= 8 ? 8 : kp;  // token rows the MMAs read
     const int rows = max(k, min(c_dirty, kq));
     c_dirty = c_dirty > kq ? c_dirty : k;
     const int n_chunks = rows * 8;
@@ -236,14 +243,19 @@ __device__ __forceinline__ void run_builder_tc(const Params& p, unsigned char* s
       tc_fence_after();
       if (lane == 0) {
         const uint64_t bdesc0 = smem_desc_mn_sw128(sbase + kTcBOff, 1024u, 1024u);
-        if constexpr (kSplit) {
-          // one MMA per eight tokens: K rows 0-7 of C^T are their hi rows and
-          // 8-15 their lo rows, against the eight A rows read twice (K stride
-          // 0); the start address field counts 16-byte units
-          const uint64_t adesc0 = smem_desc_mn_sw128(sbase + tc_a_off(SF), 1024u, 0u);
-          for (int g = 0; g < kq / 8; ++g)
-            tc_mma_bf16(tmem + buf * kTcAccCols, adesc0 + static_cast<uint64_t>(g * kTcAGroup / 16),
-                        bdesc0 + static_cast<uint64_t>(g * kCGroup / 16), kIdesc, g > 0 ? 1u : 0u);
+        if (kSplit && k <= 8) {
+          // one MMA: K rows 0-7 of C^T are the tokens' hi rows and 8-15 their
+          // lo rows, against the eight A rows read twice (K stride 0); the
+          // start address field counts 16-byte units
+          tc_mma_bf16(tmem + buf * kTcAccCols, smem_desc_mn_sw128(sbase + tc_a_off(SF), 1024u, 0u), bdesc0, kIdesc,
+                      0u);
+        } else if (kSplit) {
+          // one MMA of N = 128 per 16 tokens: C^T as 128 rows (hi, then lo)
+          const uint64_t adesc0 = smem_desc_mn_sw128(sbase + tc_a_off(SF), 1024u, kTcAGroup);
+          const uint64_t cdesc0 = smem_desc_mn_sw128(sbase + kTcBOff, 1024u, kCGroup);
+          for (int kc = 0; kc < kp / 16; ++kc)
+            tc_mma_bf16(tmem + buf * kTcAccCols, adesc0 + static_cast<uint64_t>(kc * 2 * kTcAGroup / 16),
+                        cdesc0 + static_cast<uint64_t>(kc * 2 * kCGroup / 16), kIdescN128, kc > 0 ? 1u : 0u);
         } else {
           // one MMA per 16 tokens, i.e. per two token groups
           const uint64_t adesc0 = smem_desc_mn_sw128(sbase + tc_a_off(SF), 1024u, kTcAGroup);
@@ -329,6 +341,7 @@ __device__ __forceinline__ void run_epilogue_tc(const Params& p, unsigned char* 
     const float P = decay_scan(reinterpret_cast<const float*>(sb + il.off_dt), desc->A[0], k, lane, wbuf);
     const uint32_t buf = n_tc & 1u;
     const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + buf * kTcAccCols;
+    const bool split_n = tc_split_c(SF) && k > 8;  // the accumulator's halves hold hi and lo
     unsigned char* out_col = dst_tile + static_cast<uint32_t>(j) * 2u;
     const uint16_t* s0_col = reinterpret_cast<const uint16_t*>(sb) + j;
     if (!sr && dst_aligned) {
@@ -355,6 +368,16 @@ __device__ __forceinline__ void run_epilogue_tc(const Params& p, unsigned char* 
       for (int part = 0; part < D / 16; ++part) {
         float acc[16];
         tmem_ld16(taddr + 16u * part, acc);
+        if (split_n) {  // hi and lo products in the two halves
+          float lo16[16];
+          tmem_ld16(taddr + kTcLoCols + 16u * part, lo16);
+#pragma unroll
+          for (int c = 0; c < 16; c += 2) {
+            const float2 a2 = __fadd2_rn(make_float2(acc[c], acc[c + 1]), make_float2(lo16[c], lo16[c + 1]));
+            acc[c] = a2.x;
+            acc[c + 1] = a2.y;
+          }
+        }
 #pragma unroll
         for (int c2 = 0; c2 < 8; ++c2) {
           const float a0 = acc[2 * c2], a1 = acc[2 * c2 + 1];
@@ -375,8 +398,8 @@ __device__ __forceinline__ void run_epilogue_tc(const Params& p, unsigned char* 
         break;
       }
       tc_fence_after();
-      tc_epilogue_general<SF>(p.philox_rounds, taddr, s0_col, P, out_col, dst_aligned, sr, h, j, dst_slot_id,
-                              layer_id, key0, key1);
+      tc_epilogue_general<SF>(p.philox_rounds, taddr, split_n, s0_col, P, out_col, dst_aligned, sr, h, j,
+                              dst_slot_id, layer_id, key0, key1);
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar);
     }
