@@ -437,10 +437,29 @@ INT_LANES_PER_SM = 64   # 32-bit integer lanes per SM (4 sub-partitions x 16): L
 PHILOX10_WORDS_PER_SM_CLK = 6.8
 
 
-def lane_ops(shape, active, prefix, src, dst):
-    """(fp32 lane-operations, 32-bit integer lane-operations, Philox words)
-    one call needs, counted from the method, not from the code.  Per element
-    of a replayed tile: one FMUL (the decay product) and one FFMA per token.
+# kernels whose replay (sum_t w_t x_t B_t^T) runs on the tensor cores
+TENSOR_KERNELS = {"materialize_tc_kernel", "materialize_q8tc_kernel", "gdn_commit_tc_kernel"}
+TF32_PER_BF16 = 1.1 / 2.25  # nominal dense TF32 : BF16 tensor rate of the part
+
+
+def tensor_peak_flops():
+    """Dense bf16 tensor FLOP/s: the measured burst GEMM rate, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            return float(json.load(open(path))["bf16_tflops"]) * 1e12
+        except (KeyError, ValueError):
+            pass
+    return 1.9e15
+
+
+def lane_ops(shape, active, prefix, src, dst, tensor=False):
+    """(fp32 lane-operations, 32-bit integer lane-operations, Philox words,
+    tensor FLOPs) one call needs, counted from the method, not from the code.
+    Per element of a replayed tile: one FMUL (the decay product) and one FFMA
+    per token; where the replay runs on the tensor cores (`tensor`), the
+    tokens' multiply-adds are tensor FLOPs (2 per element and token) and one
+    FFMA per element (P S_0 + the accumulator) stays on the lanes.
     With Philox rounding, one call (four words) serves 8 elements of 16-bit
     state or 16 of one-byte state, and costs philox_rounds * 6 integer
     operations (a round is two 32x32->64-bit multiplies, two three-way XORs
@@ -451,18 +470,22 @@ def lane_ops(shape, active, prefix, src, dst):
     n = int(np.argmax(active == -1)) if (active == -1).any() else len(active)
     elems = shape.H * shape.D * shape.N
     per_call = 16 if wl.ELEM_SIZE[shape.state_dtype] == 1 else 8
-    fp32 = integer = words = 0
+    fp32 = integer = words = flops = 0
     for b in active[:n]:
         b = int(b)
         k = int(prefix[b])
         if k == 0:
             continue
         live = sum(1 for l in range(shape.L) if src[l, b] != shape.pad_slot_id and dst[l, b] != shape.pad_slot_id)
-        fp32 += live * elems * (k + 1)
+        if tensor:
+            fp32 += live * elems
+            flops += live * elems * 2 * k
+        else:
+            fp32 += live * elems * (k + 1)
         if shape.philox_rounds > 0:
             integer += live * elems * shape.philox_rounds * 6 / per_call
             words += live * elems * 4 // per_call
-    return fp32, int(integer), words
+    return fp32, int(integer), words, flops
 
 
 def timed_calls(torch, call, stream, uuid, seconds=1.0):
@@ -491,7 +514,8 @@ def timed_calls(torch, call, stream, uuid, seconds=1.0):
     return e0.elapsed_time(e1) / steps, steps, info
 
 
-def _fractions(nbytes, fp32_ops, int_ops, ms, peak_gbs, sms, clock_info, words=0, rounds=0):
+def _fractions(nbytes, fp32_ops, int_ops, ms, peak_gbs, sms, clock_info, words=0, rounds=0, tensor_flops=0,
+               tensor_peak=0.0):
     mhz = (clock_info or {}).get("sm_mhz") or 2070.0
     sec = ms * 1e-3
     fr = {"hbm_frac": nbytes / sec / 1e9 / peak_gbs, "hbm_frac_spec": nbytes / sec / 1e9 / SPEC_HBM_GBS,
@@ -504,6 +528,9 @@ def _fractions(nbytes, fp32_ops, int_ops, ms, peak_gbs, sms, clock_info, words=0
     cands = [("hbm", fr["hbm_frac"]), ("fp32", fr["fp32_lane_frac"]), ("int", fr["int_lane_frac"])]
     if "philox_frac" in fr:
         cands.append(("philox", fr["philox_frac"]))
+    if tensor_flops:
+        fr["tensor_frac"] = tensor_flops / sec / tensor_peak
+        cands.append(("tensor", fr["tensor_frac"]))
     fr["bound"] = max(cands, key=lambda kv: kv[1])[0]
     return fr
 
@@ -517,10 +544,10 @@ def measure_workload(torch, rsm, shape, device, peak_gbs, sms, uuid):
     prefix = dw.replay_prefix_len.cpu().numpy()
     src, dst = dw.src_slots.cpu().numpy(), dw.dst_slots.cpu().numpy()
     state_b, ring_b, n = workload_bytes(shape, active, prefix, src, dst)
-    fp32_ops, int_ops, words = lane_ops(shape, active, prefix, src, dst)
     kw = dw.call_kwargs()
     call = rsm.prepare(**kw)
     kernel = rsm.kernel_name(**kw)
+    fp32_ops, int_ops, words, tflops = lane_ops(shape, active, prefix, src, dst, tensor=kernel in TENSOR_KERNELS)
     launch = rsm.launch_config(**kw)
     ms, steps, clock_info = timed_calls(torch, call, torch.cuda.current_stream(), uuid)
     status = int(dw.status.item())
@@ -532,8 +559,10 @@ def measure_workload(torch, rsm, shape, device, peak_gbs, sms, uuid):
            "philox_rounds": shape.philox_rounds, "pad_frac": shape.pad_frac, "ms_per_call": ms, "steps": steps,
            "algorithmic_bytes": state_b + ring_b, "state_gbs": state_b / (ms * 1e-3) / 1e9,
            "us_per_request": ms * 1e3 / max(n, 1), "fp32_lane_ops": fp32_ops, "int_lane_ops": int_ops}
+    if tflops:
+        out["tensor_flops"] = tflops
     out.update(_fractions(state_b + ring_b, fp32_ops, int_ops, ms, peak_gbs, sms, clock_info, words,
-                          shape.philox_rounds))
+                          shape.philox_rounds, tflops, tensor_peak_flops()))
     out["clocks"] = clock_info
     out["device_status"] = status
     return out
@@ -554,7 +583,11 @@ def measure_gdn(torch, rsm, shape, device, peak_gbs, sms, uuid, backend="auto"):
     tst = None if dw.track_steps is None else dw.track_steps.cpu().numpy()
     nbytes = gw.gdn_bytes(shape, idx, lens, tidx, tst)
     live = [b for b in range(shape.B) if idx[b] > shape.null_block_id and lens[b] > 0]
-    lane_ops_ = sum(int(lens[b]) for b in live) * shape.L * shape.HV * gw.DV * gw.DK * 3
+    tokens = sum(int(lens[b]) for b in live) * shape.L * shape.HV * gw.DV * gw.DK
+    if backend == "tcgen05":  # the two contractions (W = S0 K^, the rank-n update) in TF32 on the tensor cores
+        lane_ops_, tflops = tokens, 4 * tokens
+    else:
+        lane_ops_, tflops = 3 * tokens, 0
     stream = torch.cuda.current_stream()
     call = lambda st: rsm.gated_delta_rule_replayssm_commit(**kw, stream=st)
     ms, steps, clock_info = timed_calls(torch, call, stream, uuid)
@@ -566,7 +599,10 @@ def measure_gdn(torch, rsm, shape, device, peak_gbs, sms, uuid, backend="auto"):
            "layers": shape.L, "v_heads": shape.HV, "k_heads": shape.H, "window": shape.T, "batch": shape.B,
            "live_requests": len(live), "track": shape.track, "accept": list(shape.accept), "ms_per_call": ms,
            "steps": steps, "algorithmic_bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9}
-    out.update(_fractions(nbytes, lane_ops_, 0, ms, peak_gbs, sms, clock_info))
+    if tflops:
+        out["tensor_flops"] = tflops
+    out.update(_fractions(nbytes, lane_ops_, 0, ms, peak_gbs, sms, clock_info, tensor_flops=tflops,
+                          tensor_peak=tensor_peak_flops() * TF32_PER_BF16))
     out["clocks"] = clock_info
     out["device_status"] = status
     return out
@@ -781,7 +817,9 @@ def main():
         out["lane_peaks_note"] = (f"fp32: {sms} SMs x {ALU_LANES_PER_SM} lanes x the sampled SM clock; 32-bit "
                                   f"integer: {sms} SMs x {INT_LANES_PER_SM} lanes x the sampled SM clock; Philox: "
                                   f"{PHILOX10_WORDS_PER_SM_CLK} words per SM per clock at 10 rounds (measured); a word "
-                                  f"rounds two 16-bit or four one-byte elements")
+                                  f"rounds two 16-bit or four one-byte elements; tensor: the measured dense bf16 "
+                                  f"GEMM rate (MEASURED_PEAKS.json bf16_tflops), x {TF32_PER_BF16:.3f} (the nominal "
+                                  f"TF32 : BF16 ratio) for TF32")
     if rank == 0:
         print(json.dumps(out), flush=True)
     dist.barrier()

@@ -87,13 +87,21 @@ def test_lane_operations_and_philox_fraction(bench):
         n, k = 4, 3
         active, prefix, src, dst = _meta(shape, n, k, pad=(0, 1))
         prefix[2] = 0                                    # request 2 is a copy
-        fp32, integer, words = bench.lane_ops(shape, active, prefix, src, dst)
+        fp32, integer, words, flops = bench.lane_ops(shape, active, prefix, src, dst)
         elems = 256 * 64 * 128
         live = (n - 1) * shape.L - 1                     # one copy request, one padded layer
-        assert fp32 == live * elems * (k + 1)
+        assert fp32 == live * elems * (k + 1) and flops == 0
         assert integer == int(live * elems * 60 / per_call)
         assert words == live * elems * 4 // per_call
+        # the replay on the tensor cores: 2 FLOPs per element and token there,
+        # one FFMA per element on the lanes
+        fp32_t, integer_t, words_t, flops_t = bench.lane_ops(shape, active, prefix, src, dst, tensor=True)
+        assert fp32_t == live * elems and flops_t == live * elems * 2 * k
+        assert (integer_t, words_t) == (integer, words)
     fr = bench._fractions(1e9, fp32, integer, 1.0, 6790.0, 152, {"sm_mhz": 2070.0}, words, 10)
     words_peak = 6.8 * 152 * 2070e6
     assert abs(fr["philox_frac"] - words / 1e-3 / words_peak) < 1e-12
     assert "philox_frac" not in bench._fractions(1e9, 1, 0, 1.0, 6790.0, 152, None)
+    ft = bench._fractions(1e9, 1, 0, 1.0, 6790.0, 152, None, tensor_flops=1.9e12, tensor_peak=1.9e15)
+    assert abs(ft["tensor_frac"] - 1.0) < 1e-12 and ft["bound"] == "tensor"
+    assert "tensor_frac" not in bench._fractions(1e9, 1, 0, 1.0, 6790.0, 152, None)
