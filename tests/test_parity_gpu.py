@@ -127,7 +127,7 @@ def test_every_instance_long_window(sd, idt, D, N):
     check(hw)
 
 
-@pytest.mark.parametrize("sd", ["bf16", "i8"])
+@pytest.mark.parametrize("sd", ["bf16", "f16", "i8"])
 def test_stochastic_rounding_long_window(sd):
     shape = wl.Shape("srw", L=2, Bt=4, H=4, hpg=2, D=64, N=128, R=64, W=64, state_dtype=sd, n_active=4,
                      ring_start=(0, 64), prefix=("uniform", 17, 64), philox_rounds=10, rand_seed=0xABCDEF)
