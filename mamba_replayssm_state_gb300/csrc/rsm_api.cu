@@ -307,7 +307,7 @@ int plan_launch(const rsm_materialize_args* a, Launch* L) {
       if (verbose()) std::fprintf(stderr, "[replayssm] occupancy query: %d CTAs per SM\n", per_sm);
       // The occupancy query reports one CTA per SM for the tensor-core kernel,
       // while the hardware's own limits (ncu's occupancy section: shared
-      // memory 2, registers 2) let two run side by side, each holding 128 of
+      // memory 2, registers 2) let two run side by side, each holding 256 of
       // the SM's 512 TMEM columns.  Two are planned only after checking those
       // limits here; were the second not co-scheduled, the persistent grid
       // would merely take a second wave.

@@ -712,6 +712,25 @@ def test_tensor_core_fp16_state_error_bound(k):
     compare_worlds(got, ref, hw)
 
 
+@pytest.mark.parametrize("sd,hpg", [("f16", 1), ("bf16", 1), ("f16", 2)])
+def test_tensor_core_launch_plan_and_single_head_groups(sd, hpg):
+    """Groups of one head: every item carries its B rows, so two 64-token
+    items need 82 KB of arena.  fp16 state (with its 16 KB hi + lo operand)
+    then plans one CTA per SM with the whole shared memory, bf16 state two;
+    groups of two heads fit two CTAs per SM in both formats.  Results match
+    the oracle in every plan."""
+    shape = wl.Shape("tcplan", L=2, Bt=4, H=8, hpg=hpg, D=64, N=128, R=64, W=64, state_dtype=sd, n_active=4,
+                     ring_start=(0, 64), prefix=("uniform", 40, 64))
+    hw = wl.host_world(shape, seed=37 + hpg)
+    kw = wl.device_world_from_host(hw).call_kwargs()
+    assert rsm.kernel_name(**kw) == "materialize_tc_kernel"
+    cfg = rsm.launch_config(**kw)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    one_cta = sd == "f16" and hpg == 1
+    assert cfg["grid"] == (sms if one_cta else 2 * sms), cfg
+    check(hw)
+
+
 @pytest.mark.parametrize("sd", ["bf16", "f16"])
 def test_tensor_core_in_place_commit(sd):
     shape = wl.Shape("tcinplace", L=2, Bt=5, H=6, hpg=3, D=64, N=128, R=64, W=64, state_dtype=sd, n_active=4,
